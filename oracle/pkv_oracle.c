@@ -1,0 +1,337 @@
+/*
+ * pkv_oracle.c — the reference (oracle) implementation of paged GQA attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, deliberately obvious CPU
+ * implementation that the GPU library is checked against.  Only the test suite, the
+ * package's smoke check and the CPU-baseline leg of the benchmark may load it.  It
+ * shares no code, header, table or helper with the CUDA library, and the CUDA library
+ * never calls it.
+ *
+ * What it computes (sources are the pages' titles and sections):
+ *   - "Tiny-LLM-Inference Project_Status", feature list: a paged KV cache, chunked
+ *     prefill/decode; dtype contract: FP32 KV by default, BF16 KV with its own paged
+ *     attention kernel, FP32 operator boundaries.
+ *   - "tinyloop Current Status", KV cache modes table: paged attention with 16-token
+ *     pages; INT8 KV cache.  Model architecture support table: GQA (fewer KV heads,
+ *     MQA too) and chunked prefill.
+ * None of the pages writes out the attention formula, so the oracle is the textbook
+ * definition of scaled dot-product attention evaluated over the logically reassembled
+ * cache:
+ *     out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K_t[g,:]) * V_t[g,:],  g = h / G
+ * in double precision, with max subtraction inside the softmax.  K_t and V_t are the
+ * values as stored (FP32 as is, BF16 widened exactly, INT8 as code * scale in double).
+ *
+ * Physical layout (the library's documented layout, restated here from its
+ * specification and not from its code):
+ *   K cache  [num_pages][Hkv][P][D]           element (page,h,off,d)
+ *   V cache  [num_pages][Hkv][D][P]           (each page's V block is transposed)
+ *   scales   [num_pages][Hkv][P]  float32     (INT8 only; one per token and kv head)
+ *   slot = page * P + off
+ *
+ * The INT8 quantiser and the BF16 rounding run in C `float` exactly as specified
+ * (IEEE division, round-half-to-even), compiled with -ffp-contract=off and without
+ * fast-math, so the stored codes are a function of the inputs alone.
+ *
+ * Parity pins: every function here is pinned by tests that do not re-type it (dense
+ * brute force against a library attention, closed forms, permutation invariance,
+ * causality, an exhaustive nearest-code search for the quantiser, and the library
+ * float->bfloat16 cast for the rounding).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ORACLE_MUTANT selects a deliberately planted mistake; the pin tests build each one
+ * and check that some pin fails.  The default build (0) has none. */
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+enum { ODT_F32 = 0, ODT_BF16 = 1, ODT_INT8 = 2 };
+
+/* ---------------------------------------------------------------- scalar helpers */
+
+/* bfloat16 -> float: the bf16 bits are the top half of the float32 bits. */
+static float bf16_bits_to_float(uint16_t h) {
+  uint32_t u = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* float -> bfloat16 with round-to-nearest, ties to even, on the discarded 16 bits.
+ * NaN stays NaN (quiet bit forced). */
+uint16_t oracle_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+    return (uint16_t)((u >> 16) | 0x0040u);
+  uint32_t lower = u & 0xffffu;
+  uint32_t upper = u >> 16;
+#if ORACLE_MUTANT == 1 /* ties away from zero */
+  if (lower >= 0x8000u) upper += 1u;
+#else
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+#endif
+  return (uint16_t)upper;
+}
+
+/* Read element i of a buffer holding float32 or bfloat16 values. */
+static double read_real(const void* p, int dtype, size_t i) {
+  if (dtype == ODT_BF16) return (double)bf16_bits_to_float(((const uint16_t*)p)[i]);
+  return (double)((const float*)p)[i];
+}
+static float read_real_f(const void* p, int dtype, size_t i) {
+  if (dtype == ODT_BF16) return bf16_bits_to_float(((const uint16_t*)p)[i]);
+  return ((const float*)p)[i];
+}
+
+/* Symmetric per-row INT8 quantiser: s = max|x| / 127 (float division), code =
+ * clamp(round_half_even(x / s), -127, 127); a row of zeros gets s = 0 and codes 0. */
+void oracle_quantize_row_int8(const float* x, int n, int8_t* codes, float* scale_out) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  float s = amax / 127.0f;
+  for (int i = 0; i < n; ++i) {
+    int c = 0;
+    if (s != 0.0f) {
+#if ORACLE_MUTANT == 2 /* truncation instead of rounding */
+      float r = truncf(x[i] / s);
+#else
+      float r = rintf(x[i] / s);
+#endif
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+      c = (int)r;
+    }
+    codes[i] = (int8_t)c;
+  }
+  *scale_out = s;
+}
+
+/* ---------------------------------------------------------------- cache addressing */
+
+static size_t k_index(int page, int h, int off, int d, int Hkv, int P, int D) {
+  return (((size_t)page * Hkv + h) * P + off) * D + d;
+}
+static size_t v_index(int page, int h, int off, int d, int Hkv, int P, int D) {
+#if ORACLE_MUTANT == 3 /* V block not transposed */
+  return (((size_t)page * Hkv + h) * P + off) * D + d;
+#else
+  return (((size_t)page * Hkv + h) * D + d) * P + off;
+#endif
+}
+static size_t s_index(int page, int h, int off, int Hkv, int P) {
+  return ((size_t)page * Hkv + h) * P + off;
+}
+
+/* Stored K or V element as a double (after dequantisation). */
+static double cache_value(const void* cache, const float* scales, int kv_dtype, int is_v,
+                          int page, int h, int off, int d, int Hkv, int P, int D) {
+  size_t i = is_v ? v_index(page, h, off, d, Hkv, P, D) : k_index(page, h, off, d, Hkv, P, D);
+  if (kv_dtype == ODT_INT8) {
+    int8_t c = ((const int8_t*)cache)[i];
+    return (double)c * (double)scales[s_index(page, h, off, Hkv, P)];
+  }
+  return read_real(cache, kv_dtype, i);
+}
+
+/* ---------------------------------------------------------------- KV append */
+
+/*
+ * Write the new tokens' K and V rows into their slots.  Token i goes to
+ * slot = slot_mapping[i] (page = slot / P, off = slot % P) for every kv head;
+ * slot < 0 means "skip this token" (padding).  The source rows are float32 or
+ * bfloat16 [T][Hkv][D].  FP32 cache: stored as the float value; BF16 cache: rounded to
+ * nearest even; INT8 cache: quantised per (token, head) with the quantiser above.
+ * Returns the number of tokens whose slot was >= num_pages * P (those are skipped).
+ */
+int oracle_append(int kv_dtype, int num_pages, int P, int Hkv, int D, void* k_cache,
+                  void* v_cache, float* k_scale, float* v_scale, const void* k_new,
+                  const void* v_new, int new_dtype, const int32_t* slot_mapping, int T) {
+  int bad = 0;
+  float* row = (float*)malloc(sizeof(float) * (size_t)D);
+  int8_t* codes = (int8_t*)malloc((size_t)D);
+  for (int i = 0; i < T; ++i) {
+    int slot = slot_mapping[i];
+    if (slot < 0) continue;
+    if ((long long)slot >= (long long)num_pages * P) { ++bad; continue; }
+    int page = slot / P, off = slot % P;
+    for (int h = 0; h < Hkv; ++h) {
+      for (int is_v = 0; is_v < 2; ++is_v) {
+        const void* src = is_v ? v_new : k_new;
+        void* dst = is_v ? v_cache : k_cache;
+        for (int d = 0; d < D; ++d)
+          row[d] = read_real_f(src, new_dtype, ((size_t)i * Hkv + h) * D + d);
+        if (kv_dtype == ODT_INT8) {
+          float s;
+          oracle_quantize_row_int8(row, D, codes, &s);
+          for (int d = 0; d < D; ++d) {
+            size_t j = is_v ? v_index(page, h, off, d, Hkv, P, D) : k_index(page, h, off, d, Hkv, P, D);
+            ((int8_t*)dst)[j] = codes[d];
+          }
+          (is_v ? v_scale : k_scale)[s_index(page, h, off, Hkv, P)] = s;
+        } else {
+          for (int d = 0; d < D; ++d) {
+            size_t j = is_v ? v_index(page, h, off, d, Hkv, P, D) : k_index(page, h, off, d, Hkv, P, D);
+            if (kv_dtype == ODT_BF16) ((uint16_t*)dst)[j] = oracle_f32_to_bf16(row[d]);
+            else ((float*)dst)[j] = row[d];
+          }
+        }
+      }
+    }
+  }
+  free(row);
+  free(codes);
+  return bad;
+}
+
+/* ---------------------------------------------------------------- attention core */
+
+/*
+ * Softmax-weighted sum for one query vector q (length D, already in double) over the
+ * logical tokens 0..n_keys-1 of sequence b, kv head g.  Logical token t lives in
+ * physical page block_table[t / P] at offset t % P.
+ */
+static void attend_one(const double* q, int n_keys, const int32_t* block_table, int g,
+                       const void* k_cache, const void* v_cache, const float* k_scale,
+                       const float* v_scale, int kv_dtype, int Hkv, int P, int D,
+                       double scale, double* scores, double* out) {
+  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  if (n_keys <= 0) return;
+  double m = -INFINITY;
+  for (int t = 0; t < n_keys; ++t) {
+#if ORACLE_MUTANT == 8 /* pages taken in physical instead of logical order */
+    int page = (int)(t / P), off = t % P;
+    (void)block_table;
+#else
+    int page = block_table[t / P], off = t % P;
+#endif
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d)
+      dot += q[d] * cache_value(k_cache, k_scale, kv_dtype, 0, page, g, off, d, Hkv, P, D);
+#if ORACLE_MUTANT == 4 /* scale dropped */
+    scores[t] = dot;
+#else
+    scores[t] = scale * dot;
+#endif
+    if (scores[t] > m) m = scores[t];
+  }
+  double denom = 0.0;
+#if ORACLE_MUTANT == 7 /* no max subtraction */
+  m = 0.0;
+#endif
+  for (int t = 0; t < n_keys; ++t) {
+    scores[t] = exp(scores[t] - m);
+    denom += scores[t];
+  }
+  for (int t = 0; t < n_keys; ++t) {
+    int page = block_table[t / P], off = t % P;
+    double w = scores[t] / denom;
+    for (int d = 0; d < D; ++d)
+      out[d] += w * cache_value(v_cache, v_scale, kv_dtype, 1, page, g, off, d, Hkv, P, D);
+  }
+}
+
+/*
+ * Batched decode: one query token per sequence.  q is [B][Hq][D] (float32 or
+ * bfloat16), out is [B][Hq][D] doubles.  Sequence b attends over its first
+ * context_lens[b] logical tokens (the current token included).  GQA: query head h
+ * reads kv head h / (Hq / Hkv).  A sequence with context length 0 gets a zero row.
+ * Sequences for which context_lens[b] is negative or above max_blocks * P, or whose
+ * block table holds a page outside [0, num_pages), get NaN rows; the return value
+ * counts them.
+ */
+int oracle_decode(int kv_dtype, int num_pages, int P, int Hkv, int D, const void* k_cache,
+                  const void* v_cache, const float* k_scale, const float* v_scale,
+                  const void* q, int q_dtype, int B, int Hq, const int32_t* block_tables,
+                  int max_blocks, const int32_t* context_lens, double scale, double* out,
+                  int b_begin, int b_end) {
+  int G = Hq / Hkv, bad = 0;
+  int max_len = max_blocks * P;
+  double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+  double* scores = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+  if (b_end > B) b_end = B;
+  for (int b = b_begin; b < b_end; ++b) {
+    int L = context_lens[b];
+    const int32_t* bt = block_tables + (size_t)b * max_blocks;
+    int ok = (L >= 0 && L <= max_len);
+    for (int j = 0; ok && j < (L + P - 1) / P; ++j)
+      if (bt[j] < 0 || bt[j] >= num_pages) ok = 0;
+    for (int h = 0; h < Hq; ++h) {
+      double* o = out + ((size_t)b * Hq + h) * D;
+      if (!ok) {
+        for (int d = 0; d < D; ++d) o[d] = NAN;
+        continue;
+      }
+      for (int d = 0; d < D; ++d) qd[d] = read_real(q, q_dtype, ((size_t)b * Hq + h) * D + d);
+#if ORACLE_MUTANT == 5 /* GQA heads interleaved instead of grouped */
+      int g = h % Hkv;
+#else
+      int g = h / G;
+#endif
+      attend_one(qd, L, bt, g, k_cache, v_cache, k_scale, v_scale, kv_dtype, Hkv, P, D,
+                 scale, scores, o);
+    }
+    if (!ok) ++bad;
+  }
+  free(qd);
+  free(scores);
+  return bad;
+}
+
+/*
+ * Chunked prefill: sequence b owns query rows q_start_loc[b] .. q_start_loc[b+1]-1 of q
+ * ([total_q][Hq][D]).  Its context_lens[b] counts every cached token including the
+ * chunk, so query row i of the chunk (Lq = chunk length) sits at absolute position
+ * p_i = context_lens[b] - Lq + i and attends to the logical tokens 0..p_i (the causal
+ * mask is inclusive of its own position).  out is [total_q][Hq][D] doubles.  Sequences
+ * with an inconsistent chunk (Lq < 0 or Lq > context length) or bad pages get NaN
+ * rows; the return value counts them.
+ */
+int oracle_prefill(int kv_dtype, int num_pages, int P, int Hkv, int D, const void* k_cache,
+                   const void* v_cache, const float* k_scale, const float* v_scale,
+                   const void* q, int q_dtype, int B, int Hq, const int32_t* q_start_loc,
+                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                   double scale, double* out, int b_begin, int b_end) {
+  int G = Hq / Hkv, bad = 0;
+  int max_len = max_blocks * P;
+  double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+  double* scores = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+  if (b_end > B) b_end = B;
+  for (int b = b_begin; b < b_end; ++b) {
+    int L = context_lens[b];
+    int q0 = q_start_loc[b], Lq = q_start_loc[b + 1] - q_start_loc[b];
+    const int32_t* bt = block_tables + (size_t)b * max_blocks;
+    int ok = (L >= 0 && L <= max_len && Lq >= 0 && Lq <= L);
+    for (int j = 0; ok && j < (L + P - 1) / P; ++j)
+      if (bt[j] < 0 || bt[j] >= num_pages) ok = 0;
+    if (!ok) ++bad;
+    for (int i = 0; i < (Lq > 0 ? Lq : 0); ++i) {
+      int pos = L - Lq + i;
+      for (int h = 0; h < Hq; ++h) {
+        size_t row = ((size_t)(q0 + i) * Hq + h) * D;
+        double* o = out + row;
+        if (!ok) {
+          for (int d = 0; d < D; ++d) o[d] = NAN;
+          continue;
+        }
+        for (int d = 0; d < D; ++d) qd[d] = read_real(q, q_dtype, row + d);
+#if ORACLE_MUTANT == 6 /* causal mask excludes the diagonal */
+        int n_keys = pos;
+#else
+        int n_keys = pos + 1;
+#endif
+        attend_one(qd, n_keys, bt, h / G, k_cache, v_cache, k_scale, v_scale, kv_dtype,
+                   Hkv, P, D, scale, scores, o);
+      }
+    }
+  }
+  free(qd);
+  free(scores);
+  return bad;
+}

@@ -1,0 +1,426 @@
+"""Pins for the CPU oracle: each ties it to something other than itself.
+
+- BF16 rounding against torch's float->bfloat16 cast (a library routine) on random
+  values and on constructed ties.
+- The INT8 quantiser against an exhaustive nearest-code search, hand-made ties, and the
+  round-trip bound |x - code*s| <= s/2.
+- Attention against torch's scaled_dot_product_attention in float64 on the logically
+  reassembled cache (dense brute force), for decode and for causal chunks.
+- Closed forms: uniform V, a single token, q = 0, one dominating key.
+- Structure: physical page order does not matter; GQA equals MHA with replicated heads;
+  causality (future keys do not matter, the last chunk row equals decode, Lq = 1 equals
+  decode).
+- Planted mistakes: each deliberately broken oracle build fails at least one pin.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import BF16, F32, INT8, HostCache
+from paged_kv_attention_09_gb300 import workloads as W
+
+P = 16
+
+
+# --------------------------------------------------------------------------- helpers
+
+def bf16_to_f32(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def logical_kv(cache: HostCache, bt_row, L, g):
+    """Reassemble logical K/V [L, D] (float64, dequantised) from the documented layout."""
+    t = np.arange(L)
+    pages, offs = bt_row[t // P], t % P
+    k = cache.k[pages, g, offs, :]
+    v = cache.v[pages, g, :, offs]  # fancy indices first -> [L, D]
+    if cache.kv_dtype == BF16:
+        k, v = bf16_to_f32(k), bf16_to_f32(v)
+    k = k.astype(np.float64)
+    v = v.astype(np.float64)
+    if cache.kv_dtype == INT8:
+        k = k * cache.k_scale[pages, g, offs].astype(np.float64)[:, None]
+        v = v * cache.v_scale[pages, g, offs].astype(np.float64)[:, None]
+    return k, v
+
+
+def q_f64(q, q_dtype):
+    return (bf16_to_f32(q) if q_dtype == BF16 else np.asarray(q, np.float32)).astype(np.float64)
+
+
+def sdpa(q, k, v, scale, mask=None):
+    """torch SDPA in float64: q [n, D], k/v [L, D]."""
+    qt = torch.from_numpy(q)[None, None]
+    kt = torch.from_numpy(k)[None, None]
+    vt = torch.from_numpy(v)[None, None]
+    m = None if mask is None else torch.from_numpy(mask)[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m,
+                                                            scale=scale)[0, 0].numpy()
+
+
+def decode_bruteforce(cache, batch, Hq, Hkv, scale):
+    G = Hq // Hkv
+    q = q_f64(batch.q, batch.q_dtype)
+    out = np.zeros_like(q)
+    for b in range(batch.num_seqs):
+        L = int(batch.context_lens[b])
+        for g in range(Hkv):
+            k, v = logical_kv(cache, batch.block_tables[b], L, g)
+            out[b, g * G:(g + 1) * G] = sdpa(q[b, g * G:(g + 1) * G], k, v, scale)
+    return out
+
+
+def prefill_bruteforce(cache, batch, Hq, Hkv, scale):
+    G = Hq // Hkv
+    q = q_f64(batch.q, batch.q_dtype)
+    out = np.zeros_like(q)
+    for b in range(batch.num_seqs):
+        L = int(batch.context_lens[b])
+        q0, q1 = int(batch.q_start_loc[b]), int(batch.q_start_loc[b + 1])
+        Lq = q1 - q0
+        pos = L - Lq + np.arange(Lq)
+        mask = np.arange(L)[None, :] <= pos[:, None]
+        for g in range(Hkv):
+            k, v = logical_kv(cache, batch.block_tables[b], L, g)
+            for hh in range(G):
+                h = g * G + hh
+                out[q0:q1, h] = sdpa(q[q0:q1, h], k, v, scale, mask)
+    return out
+
+
+def run_decode(cache, wl, batch):
+    return oracle.decode(cache, batch.q, batch.q_dtype, batch.block_tables,
+                         batch.context_lens, wl.scale)
+
+
+def run_prefill(cache, wl, batch):
+    return oracle.prefill(cache, batch.q, batch.q_dtype, batch.q_start_loc,
+                          batch.block_tables, batch.context_lens, wl.scale)
+
+
+# --------------------------------------------------------------------------- BF16 rounding
+
+def check_bf16_rounding():
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32),
+        (rng.standard_normal(500) * 1e30).astype(np.float32),
+        (rng.standard_normal(500) * 1e-38).astype(np.float32),  # subnormals
+        np.array([0.0, -0.0, np.inf, -np.inf, 3.4e38, -3.4e38], np.float32),
+    ])
+    # constructed ties: lower 16 bits exactly 0x8000, with even and odd upper halves
+    ties = ((rng.integers(0x0080, 0x7f00, 400).astype(np.uint32) << 16) | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, -ties])
+    ours = oracle.f32_to_bf16(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return np.array_equal(ours, ref)
+
+
+def test_bf16_rounding_matches_library_cast():
+    assert check_bf16_rounding()
+
+
+# --------------------------------------------------------------------------- INT8 quantiser
+
+def check_quantiser():
+    rng = np.random.default_rng(11)
+    cand = np.arange(-127, 128, dtype=np.float64)
+    for trial in range(200):
+        n = 64 if trial % 2 == 0 else 128
+        x = (rng.standard_normal(n) * (10.0 ** rng.uniform(-3, 3))).astype(np.float32)
+        codes, s = oracle.quantize_row_int8(x)
+        amax = np.max(np.abs(x))
+        if s != np.float32(amax) / np.float32(127.0):
+            return False
+        if np.any(np.abs(codes.astype(np.int32)) > 127):
+            return False
+        if np.abs(codes[np.argmax(np.abs(x))]) != 127:
+            return False
+        # exhaustive nearest code: the chosen code must be (one of) the closest
+        r = x.astype(np.float64) / np.float64(s)
+        dist = np.abs(r[:, None] - cand[None, :])
+        best = dist.min(axis=1)
+        mine = np.abs(r - codes.astype(np.float64))
+        if np.any(mine > best + 1e-5):
+            return False
+        # round-trip bound
+        if np.any(np.abs(x - codes.astype(np.float64) * s) > 0.5 * s * (1 + 1e-5)):
+            return False
+    # hand-made ties with s == 1 exactly (max|x| = 127): halves go to the even code
+    x = np.zeros(64, np.float32)
+    x[0] = 127.0
+    x[1:7] = [2.5, 3.5, -2.5, -3.5, 0.5, -0.5]
+    codes, s = oracle.quantize_row_int8(x)
+    if s != 1.0 or list(codes[:7]) != [127, 2, 4, -2, -4, 0, 0]:
+        return False
+    # all-zero row
+    codes, s = oracle.quantize_row_int8(np.zeros(64, np.float32))
+    return s == 0.0 and not codes.any()
+
+
+def test_int8_quantiser_nearest_code_and_ties():
+    assert check_quantiser()
+
+
+# --------------------------------------------------------------------------- append
+
+def test_append_places_rows_at_documented_positions():
+    wl = W.small_workload(5, num_q_heads=4, num_kv_heads=2, head_dim=64, kv_dtype=F32,
+                          q_dtype=F32, decode_lens=[20, 37])
+    c = HostCache(F32, wl.num_pages, P, 2, 64, fill=np.float32(-7.0))
+    rows = np.arange(wl.slots.shape[0])
+    sm = wl.slots.copy()
+    sm[::5] = -1  # padding tokens are skipped
+    assert oracle.append(c, wl.k_src, wl.v_src, F32, sm) == 0
+    touched = np.zeros((wl.num_pages, P), bool)
+    for i in rows:
+        if sm[i] < 0:
+            continue
+        pg, off = divmod(int(sm[i]), P)
+        touched[pg, off] = True
+        assert np.array_equal(c.k[pg, :, off, :], wl.k_src[i])
+        assert np.array_equal(c.v[pg, :, :, off], wl.v_src[i])
+    assert np.all(c.k.transpose(0, 2, 1, 3)[~touched] == -7.0)
+    assert np.all(c.v.transpose(0, 3, 1, 2)[~touched] == -7.0)
+    # out-of-range slot is reported and skipped
+    bad = np.array([wl.num_pages * P + 3], np.int32)
+    assert oracle.append(c, wl.k_src[:1], wl.v_src[:1], F32, bad) == 1
+
+
+def test_append_bf16_and_int8_stored_values():
+    wl = W.small_workload(6, num_q_heads=2, num_kv_heads=2, head_dim=64, kv_dtype=INT8,
+                          q_dtype=F32, new_dtype=F32, decode_lens=[33])
+    ci = oracle.cache_from_workload(wl)
+    cb = HostCache(BF16, wl.num_pages, P, 2, 64)
+    oracle.append(cb, wl.k_src, wl.v_src, F32, wl.slots)
+    for i in range(wl.slots.shape[0]):
+        pg, off = divmod(int(wl.slots[i]), P)
+        for h in range(2):
+            codes, s = oracle.quantize_row_int8(wl.k_src[i, h])
+            assert np.array_equal(ci.k[pg, h, off], codes) and ci.k_scale[pg, h, off] == s
+            codes, s = oracle.quantize_row_int8(wl.v_src[i, h])
+            assert np.array_equal(ci.v[pg, h, :, off], codes) and ci.v_scale[pg, h, off] == s
+            ref = torch.from_numpy(wl.k_src[i, h]).to(torch.bfloat16).view(torch.int16)
+            assert np.array_equal(cb.k[pg, h, off], ref.numpy().view(np.uint16))
+
+
+# --------------------------------------------------------------------------- dense brute force
+
+CASES = [
+    # (kv_dtype, q_dtype, Hq, Hkv, D, decode lens)
+    (F32, F32, 9, 3, 64, [1, 15, 16, 17, 37, 64]),
+    (BF16, BF16, 12, 2, 128, [5, 31, 32, 33, 70]),
+    (BF16, F32, 8, 8, 64, [3, 48]),
+    (INT8, F32, 32, 4, 64, [2, 16, 40]),
+    (INT8, BF16, 6, 1, 128, [19, 50]),
+]
+
+
+def check_decode_bruteforce():
+    for i, (kv, qd, Hq, Hkv, D, lens) in enumerate(CASES):
+        wl = W.small_workload(100 + i, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                              kv_dtype=kv, q_dtype=qd, decode_lens=lens)
+        c = oracle.cache_from_workload(wl)
+        bt = wl.batches[0]
+        got = run_decode(c, wl, bt)
+        ref = decode_bruteforce(c, bt, Hq, Hkv, wl.scale)
+        if not np.max(np.abs(got - ref)) <= 1e-12:
+            return False
+    return True
+
+
+def test_decode_matches_dense_sdpa():
+    assert check_decode_bruteforce()
+
+
+def check_prefill_bruteforce():
+    for i, (kv, qd, Hq, Hkv, D) in enumerate([(BF16, BF16, 12, 2, 128), (F32, F32, 4, 2, 64),
+                                              (INT8, F32, 8, 2, 64)]):
+        wl = W.small_workload(200 + i, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                              kv_dtype=kv, q_dtype=qd, prefill=[(20, 13), (0, 17), (33, 1)])
+        c = oracle.cache_from_workload(wl)
+        bt = wl.batches[0]
+        got = run_prefill(c, wl, bt)
+        ref = prefill_bruteforce(c, bt, Hq, Hkv, wl.scale)
+        if not np.max(np.abs(got - ref)) <= 1e-12:
+            return False
+    return True
+
+
+def test_prefill_matches_dense_causal_sdpa():
+    assert check_prefill_bruteforce()
+
+
+# --------------------------------------------------------------------------- closed forms
+
+def _single_seq_cache(D, L, k_rows, v_rows, kv_dtype=F32, Hkv=1):
+    npages = (L + P - 1) // P + 2
+    c = HostCache(kv_dtype, npages, P, Hkv, D)
+    perm = np.random.default_rng(L).permutation(npages).astype(np.int32)
+    bt = perm[:(L + P - 1) // P][None, :]
+    t = np.arange(L)
+    slots = (bt[0, t // P] * P + t % P).astype(np.int32)
+    oracle.append(c, k_rows, v_rows, F32, slots)
+    return c, bt
+
+
+def check_closed_forms():
+    rng = np.random.default_rng(3)
+    D, L = 64, 45
+    k = rng.standard_normal((L, 1, D)).astype(np.float32)
+    q = rng.standard_normal((1, 1, D)).astype(np.float32)
+    lens = np.array([L], np.int32)
+    # uniform V: output equals that V row
+    vrow = rng.standard_normal(D).astype(np.float32)
+    c, bt = _single_seq_cache(D, L, k, np.broadcast_to(vrow, (L, 1, D)).copy())
+    out = oracle.decode(c, q, F32, bt, lens, 0.125)
+    if np.max(np.abs(out[0, 0] - vrow)) > 1e-12:
+        return False
+    # single token: output equals V_0
+    v = rng.standard_normal((L, 1, D)).astype(np.float32)
+    c, bt = _single_seq_cache(D, L, k, v)
+    out = oracle.decode(c, q, F32, bt, np.array([1], np.int32), 0.125)
+    if np.max(np.abs(out[0, 0] - v[0, 0])) > 1e-12:
+        return False
+    # q = 0: uniform weights, output equals the mean of V
+    out = oracle.decode(c, np.zeros_like(q), F32, bt, lens, 0.125)
+    if np.max(np.abs(out[0, 0] - v[:, 0].astype(np.float64).mean(axis=0))) > 1e-12:
+        return False
+    # one key dominating by far more than the exp range: output equals its V row
+    kd = np.zeros((L, 1, D), np.float32)
+    kd[29, 0, 0] = 1.0e4
+    qd = np.zeros((1, 1, D), np.float32)
+    qd[0, 0, 0] = 1.0e4
+    c, bt = _single_seq_cache(D, L, kd, v)
+    out = oracle.decode(c, qd, F32, bt, lens, 1.0)  # score gap 1e8 >> 700 ln 2
+    return bool(np.max(np.abs(out[0, 0] - v[29, 0])) <= 1e-12)
+
+
+def test_closed_forms():
+    assert check_closed_forms()
+
+
+# --------------------------------------------------------------------------- structure
+
+def check_page_permutation_invariance():
+    wl = W.small_workload(300, num_q_heads=6, num_kv_heads=2, head_dim=64, kv_dtype=INT8,
+                          q_dtype=F32, decode_lens=[50, 17, 64])
+    c1 = oracle.cache_from_workload(wl)
+    b1 = wl.batches[0]
+    out1 = run_decode(c1, wl, b1)
+    # remap every page through a fixed permutation and rebuild
+    rng = np.random.default_rng(1)
+    sigma = rng.permutation(wl.num_pages).astype(np.int32)
+    bt2 = np.where(b1.block_tables >= 0, sigma[np.maximum(b1.block_tables, 0)], -1)
+    slots2 = (sigma[wl.slots // P] * P + wl.slots % P).astype(np.int32)
+    c2 = HostCache(INT8, wl.num_pages, P, 2, 64)
+    oracle.append(c2, wl.k_src, wl.v_src, F32, slots2)
+    out2 = oracle.decode(c2, b1.q, F32, bt2, b1.context_lens, wl.scale)
+    return np.array_equal(out1, out2)
+
+
+def test_page_permutation_invariance_bit_identical():
+    assert check_page_permutation_invariance()
+
+
+def check_gqa_equals_replicated_mha():
+    Hq, Hkv, D = 8, 2, 64
+    G = Hq // Hkv
+    wl = W.small_workload(301, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, kv_dtype=F32,
+                          q_dtype=F32, decode_lens=[23, 40])
+    c = oracle.cache_from_workload(wl)
+    b = wl.batches[0]
+    out = run_decode(c, wl, b)
+    mha = HostCache(F32, wl.num_pages, P, Hq, D)
+    oracle.append(mha, np.repeat(wl.k_src, G, axis=1), np.repeat(wl.v_src, G, axis=1), F32,
+                  wl.slots)
+    out2 = oracle.decode(mha, b.q, F32, b.block_tables, b.context_lens, wl.scale)
+    return np.array_equal(out, out2)
+
+
+def test_gqa_equals_mha_with_replicated_kv():
+    assert check_gqa_equals_replicated_mha()
+
+
+def check_causality():
+    Hq, Hkv, D = 4, 2, 64
+    wl = W.small_workload(302, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, kv_dtype=BF16,
+                          q_dtype=BF16, prefill=[(19, 14)])
+    c = oracle.cache_from_workload(wl)
+    b = wl.batches[0]
+    out = run_prefill(c, wl, b)
+    L, Lq = 33, 14
+    # perturb the K/V of logical positions > p_i for i = 5 -> row 5 unchanged, row 13 changed
+    i = 5
+    pos = L - Lq + i
+    k2 = wl.k_src.copy()
+    v2 = wl.v_src.copy()
+    k2[pos + 1:] ^= np.uint16(0x1234)
+    v2[pos + 1:] ^= np.uint16(0x0f0f)
+    c2 = HostCache(BF16, wl.num_pages, P, Hkv, D)
+    oracle.append(c2, k2, v2, BF16, wl.slots)
+    out2 = run_prefill(c2, wl, b)
+    if not np.array_equal(out[:i + 1], out2[:i + 1]) or np.array_equal(out[Lq - 1], out2[Lq - 1]):
+        return False
+    # the last chunk row equals decode at context L
+    dec = oracle.decode(c, b.q[Lq - 1:Lq], BF16, b.block_tables, b.context_lens, wl.scale)
+    if not np.array_equal(dec[0], out[Lq - 1]):
+        return False
+    # every chunk row equals decode with context p_i + 1
+    for r in range(Lq):
+        d = oracle.decode(c, b.q[r:r + 1], BF16, b.block_tables,
+                          np.array([L - Lq + r + 1], np.int32), wl.scale)
+        if not np.array_equal(d[0], out[r]):
+            return False
+    return True
+
+
+def test_causality_and_prefill_decode_agreement():
+    assert check_causality()
+
+
+def test_invalid_inputs_give_nan_rows_and_counts():
+    wl = W.small_workload(303, num_q_heads=2, num_kv_heads=1, head_dim=64, kv_dtype=F32,
+                          q_dtype=F32, decode_lens=[20, 20, 0])
+    c = oracle.cache_from_workload(wl)
+    b = wl.batches[0]
+    bt = b.block_tables.copy()
+    bt[1, 1] = wl.num_pages + 5
+    out = oracle.decode(c, b.q, F32, bt, b.context_lens, wl.scale)
+    assert oracle.decode.last_bad == 1
+    assert np.all(np.isfinite(out[0])) and np.all(np.isnan(out[1])) and np.all(out[2] == 0)
+    lens = b.context_lens.copy()
+    lens[0] = bt.shape[1] * P + 1
+    out = oracle.decode(c, b.q, F32, b.block_tables, lens, wl.scale)
+    assert oracle.decode.last_bad == 1 and np.all(np.isnan(out[0]))
+
+
+# --------------------------------------------------------------------------- planted mistakes
+
+PINS = [check_bf16_rounding, check_quantiser, check_decode_bruteforce,
+        check_prefill_bruteforce, check_closed_forms, check_page_permutation_invariance,
+        check_gqa_equals_replicated_mha, check_causality]
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_planted_mistake_is_caught(mutant, monkeypatch):
+    path = oracle.build(defines=[f"ORACLE_MUTANT={mutant}"], name=f"liboracle_m{mutant}.so")
+    monkeypatch.setattr(oracle, "_lib", oracle.load(path))
+    failed = []
+    for pin in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                ok = pin()
+        except Exception:
+            ok = False
+        if not ok:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {mutant} passed every pin"
+
+
+def test_default_build_passes_every_pin():
+    for pin in PINS:
+        assert pin(), pin.__name__
