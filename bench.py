@@ -1,0 +1,456 @@
+"""Benchmark: paged decode attention (append + decode [+ chunked prefill]) on GB300.
+
+One step = one pass of the hot path over one batch: append the step's new K/V rows into
+the paged cache, then run every batch of the workload (decode and, for the mixed
+workload, chunked prefill).  The default workload is the batch-256 TinyLlama-shaped INT8
+decode.  Inputs are synthetic and seeded; R replicas of every input rotate so that each
+step reads data that is not in L2.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attn achieved HBM GB/s & seq-tokens/s vs 8 TB/s roofline, 1 GB300"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="tinyllama-int8")
+    ap.add_argument("--replicas", type=int, default=0, help="0 = enough to exceed 4x L2")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- bytes
+
+def esz(code):
+    return {0: 4, 1: 2, 2: 1}[code]
+
+
+def decode_bytes(wl, b):
+    """Algorithmic HBM bytes of one decode call: every cached token's K and V (and INT8
+    scales) once, q, out, the used block-table entries and the lengths."""
+    Hkv, D, Hq = wl.num_kv_heads, wl.head_dim, wl.num_q_heads
+    per_tok = Hkv * D * esz(wl.kv_dtype) * 2 + (Hkv * 8 if wl.kv_dtype == 2 else 0)
+    toks = int(b.context_lens.sum())
+    pages = int(sum(math.ceil(int(L) / 16) for L in b.context_lens))
+    qb = b.q.size * (2 if b.q.dtype == np.uint16 else 4)
+    return toks * per_tok + qb + b.q.shape[0] * Hq * D * 4 + pages * 4 + b.num_seqs * 4
+
+
+def prefill_bytes(wl, b):
+    Hkv, D, Hq = wl.num_kv_heads, wl.head_dim, wl.num_q_heads
+    per_tok = Hkv * D * esz(wl.kv_dtype) * 2
+    toks = int(b.context_lens.sum())
+    pages = int(sum(math.ceil(int(L) / 16) for L in b.context_lens))
+    qb = b.q.size * (2 if b.q.dtype == np.uint16 else 4)
+    return toks * per_tok + qb + b.q.shape[0] * Hq * D * 4 + pages * 4 + (2 * b.num_seqs + 1) * 4
+
+
+def prefill_flops(wl, b):
+    f = 0
+    for s in range(b.num_seqs):
+        L, Lq = int(b.context_lens[s]), int(b.chunk_lens[s])
+        keys = sum(L - Lq + i + 1 for i in range(Lq))
+        f += 4 * keys * wl.head_dim * wl.num_q_heads
+    return f
+
+
+def append_bytes(wl):
+    T = int(wl.step_rows.shape[0])
+    Hkv, D = wl.num_kv_heads, wl.head_dim
+    src = T * Hkv * D * esz(wl.new_dtype) * 2
+    dst = T * Hkv * D * esz(wl.kv_dtype) * 2 + (T * Hkv * 8 if wl.kv_dtype == 2 else 0)
+    return src + dst + T * 4
+
+
+def step_accounting(wl):
+    acc = {"append": append_bytes(wl), "decode": 0, "prefill": 0, "prefill_flops": 0,
+           "kv_tokens": 0, "seqs": 0}
+    for b in wl.batches:
+        if b.kind == "decode":
+            acc["decode"] += decode_bytes(wl, b)
+            acc["kv_tokens"] += int(b.context_lens.sum())
+            acc["seqs"] += b.num_seqs
+        else:
+            acc["prefill"] += prefill_bytes(wl, b)
+            acc["prefill_flops"] += prefill_flops(wl, b)
+    acc["total"] = acc["append"] + acc["decode"] + acc["prefill"]
+    return acc
+
+
+# ----------------------------------------------------------------------------- peaks, clocks
+
+def measured_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r[1:])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+def traffic_from_profiles(kernel_tag, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (its sha256 is recorded in the summary)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    src = os.path.join(ROOT, "paged_kv_attention_09_gb300", "csrc", f"{kernel_tag}.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+        if m and s and s.group(1) == sha:
+            return float(m.group(1))
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_rate(wl, seconds, threads):
+    """Time the oracle (as it stands) on a bounded sample of the workload: whole
+    sequences of the decode batch (and prefill rows as whole sequences), taken in order
+    until about ``seconds`` of wall time.  Returns (GB/s, tokens/s, sample description)."""
+    import oracle
+    oc = oracle.cache_from_workload(wl)
+    done_bytes, done_tok, t_total, sample = 0, 0, 0.0, []
+    for b in wl.batches:
+        B = b.num_seqs
+        n = 1
+        while True:
+            seqs = list(range(min(B, n)))
+            t0 = time.perf_counter()
+            if b.kind == "decode":
+                oracle.decode(oc, b.q, b.q_dtype, b.block_tables, b.context_lens, wl.scale,
+                              seqs=seqs, threads=threads)
+            else:
+                oracle.prefill(oc, b.q, b.q_dtype, b.q_start_loc, b.block_tables,
+                               b.context_lens, wl.scale, seqs=seqs, threads=threads)
+            dt = time.perf_counter() - t0
+            if dt >= seconds / len(wl.batches) or len(seqs) == B:
+                break
+            n = max(n + 1, min(B, int(n * max(2.0, 0.8 * seconds / len(wl.batches) / max(dt, 1e-3)))))
+        toks = int(sum(int(b.context_lens[s]) for s in seqs))
+        per_tok = wl.num_kv_heads * wl.head_dim * esz(wl.kv_dtype) * 2 + \
+            (wl.num_kv_heads * 8 if wl.kv_dtype == 2 else 0)
+        done_bytes += toks * per_tok
+        done_tok += toks
+        t_total += dt
+        sample.append(f"{len(seqs)}/{B} {b.kind} sequences")
+    return done_bytes / t_total / 1e9, done_tok / t_total, ", ".join(sample), t_total
+
+
+# ----------------------------------------------------------------------------- GPU run
+
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_attention_09_gb300 import pkv, runner
+    from paged_kv_attention_09_gb300 import workloads as W
+
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    pkv.load()
+    wl = W.workload(args.workload)
+    acc = step_accounting(wl)
+    ws_bytes = acc["total"]
+    R = args.replicas or max(2, math.ceil(4 * L2_BYTES / max(ws_bytes, 1)))
+    base = runner.upload(wl, f"cuda:{dev}")
+    rows = base.step_rows
+    step_k, step_v, step_s = (base.k_src[rows].contiguous(), base.v_src[rows].contiguous(),
+                              base.slots[rows].contiguous())
+    reps = [base]
+    for _ in range(R - 1):
+        c = base.cache
+        cache = pkv.KVCache(c.k.clone(), c.v.clone(),
+                            None if c.k_scale is None else c.k_scale.clone(),
+                            None if c.v_scale is None else c.v_scale.clone())
+        batches = [runner.DeviceBatch(b.kind, b.q.clone(), b.block_tables.clone(),
+                                      b.context_lens.clone(),
+                                      None if b.q_start_loc is None else b.q_start_loc.clone(),
+                                      b.max_q_len, torch.empty_like(b.out),
+                                      None if b.workspace is None else torch.zeros_like(b.workspace))
+                   for b in base.batches]
+        reps.append(runner.DeviceWorkload(wl, cache, base.k_src, base.v_src, base.slots,
+                                          base.step_rows, batches, base.dev_status))
+    # release the source rows that are not needed for the timed steps
+    stream = torch.cuda.current_stream()
+    n_batches = len(wl.batches)
+
+    def step(i, ev=None):
+        dw = reps[i % R]
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
+        for j in range(n_batches):
+            if ev is not None:
+                ev[1 + j].record(stream)
+            runner.run_batch(dw, j, stream)
+        if ev is not None:
+            ev[1 + n_batches].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    status = int(base.dev_status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_batches + 2)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        start.record(stream)
+        for i in range(K):
+            step(args.warmup + i, evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    kern_ms = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]
+               for j in range(n_batches + 1)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=f"cuda:{dev}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / K
+
+    # ---- end to end through the C ABI with host buffers: H2D of the step's inputs
+    # (q, new K/V, slots, tables, lengths) from pinned memory, the calls, D2H of outputs
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (step_k, step_v, step_s)]
+        for b in base.batches:
+            host_in += [b.q.cpu().pin_memory(), b.block_tables.cpu().pin_memory(),
+                        b.context_lens.cpu().pin_memory()]
+            if b.q_start_loc is not None:
+                host_in.append(b.q_start_loc.cpu().pin_memory())
+        host_out = [b.out.cpu().pin_memory() for b in base.batches]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step(i):
+            dw = reps[i % R]
+            dev_in = [step_k, step_v, step_s]
+            for b in dw.batches:
+                dev_in += [b.q, b.block_tables, b.context_lens]
+                if b.q_start_loc is not None:
+                    dev_in.append(b.q_start_loc)
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
+            for j in range(n_batches):
+                runner.run_batch(dw, j, stream)
+            for b, h in zip(dw.batches, host_out):
+                h.copy_(b.out, non_blocking=True)
+
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for i in range(K):
+            e2e_step(i)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s2.elapsed_time(e2) / K
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=f"cuda:{dev}")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(acc["total"] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 5)}
+    status = int(base.dev_status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+    return wl, acc, R, ms, kern_ms, clk.summary(), e2e
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return main_reference(args)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    wl, acc, R, ms, kern_ms, clocks, e2e = run_ours(args, rank, world)
+    K = args.steps
+    names = ["append"] + [b.kind for b in wl.batches]
+    avg = {n: statistics.fmean(v) for n, v in zip(names, kern_ms)}
+    peak, peak_kind = measured_hbm()
+    value = acc["total"] * world / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {0: "f32", 1: "bf16", 2: "int8"}[wl.kv_dtype] + "-kv/f32-acc",
+        "data": "synthetic (seeded N(0,1) values, shapes of the named model family)",
+        "config": {
+            "workload": wl.name, "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
+            "head_dim": wl.head_dim, "page_size": wl.page_size, "num_pages": wl.num_pages,
+            "batches": [{"kind": b.kind, "num_seqs": b.num_seqs,
+                         "context_tokens": int(b.context_lens.sum())} for b in wl.batches],
+            "step": "append new K/V rows, then attention over every batch",
+            "bytes_per_step": acc["total"], "replicas": R,
+            "l2": f"rotating {R} replicas of every input ({R} x {acc['total'] / 1e6:.1f} MB "
+                  f"per cycle > {L2_BYTES / 2**20:.0f} MiB L2)",
+            "parallelism": "replicas" if world > 1 else "single",
+        },
+        "seq_tokens_per_s": round(acc["kv_tokens"] * world / (ms * 1e-3), 1),
+        "decode_steps_per_s": round(acc["seqs"] * world / (ms * 1e-3), 1),
+        "kernel_ms": {n: round(v, 5) for n, v in avg.items()},
+        "gpu_launches": K * (1 + len(wl.batches)),
+    }
+    dec = avg.get("decode")
+    if dec:
+        achieved = acc["decode"] / (dec * 1e-3) / 1e9
+        line["roofline"] = {"bound": "hbm", "kernel": "decode_kernel",
+                            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                            "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                            "frac_of_8tbs": round(achieved / 8000.0, 4),
+                            "traffic": traffic_from_profiles("decode", wl.name),
+                            "algorithmic_bytes_per_launch": acc["decode"]}
+    if "prefill" in avg:
+        line["prefill"] = {"ms": round(avg["prefill"], 5),
+                           "tflops": round(acc["prefill_flops"] / (avg["prefill"] * 1e-3) / 1e12, 1)}
+    if e2e:
+        line["e2e"] = e2e
+    line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = len(os.sched_getaffinity(0))
+        gbs, tps, sample, secs = cpu_oracle_rate(wl, args.cpu_sample_seconds, threads)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": sample + f" ({secs:.1f} s wall)",
+                                "seq_tokens_per_s": round(tps, 1)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main_reference(args):
+    """The oracle as it stands, on the host cores, one bounded sample per step."""
+    from paged_kv_attention_09_gb300 import workloads as W
+    wl = W.workload(args.workload)
+    threads = len(os.sched_getaffinity(0))
+    per_step = max(0.5, args.cpu_sample_seconds / max(1, args.steps + args.warmup) * 4)
+    for _ in range(args.warmup):
+        cpu_oracle_rate(wl, per_step / 4, threads)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        gbs, tps, sample, s = cpu_oracle_rate(wl, per_step, threads)
+        vals.append(gbs)
+        secs += s
+    v = statistics.fmean(vals)
+    line = {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "impl": "reference",
+            "dtype": {0: "f64", 1: "f64", 2: "f64"}[wl.kv_dtype],
+            "data": "synthetic (seeded N(0,1) values, shapes of the named model family)",
+            "config": {"workload": wl.name, "num_q_heads": wl.num_q_heads,
+                       "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * pkv.h — C ABI of the GB300 paged-KV attention library (libpkv.so).
+ *
+ * Three operations make up the hot path of GQA attention over a paged KV cache:
+ *
+ *   pkv_append              write new tokens' K/V rows into cache pages via a slot map
+ *   pkv_decode_attn         one query token per sequence against its paged context
+ *   pkv_prefill_chunk_attn  a causal chunk of query tokens against its paged context
+ *
+ * Sources (page title, section):
+ *   "Tiny-LLM-Inference Project_Status", feature list and dtype contract: paged KV
+ *     cache, chunked prefill/decode scheduling, FP32 KV by default, a dedicated BF16
+ *     paged-attention kernel, FP32 operator boundaries, explicit failure instead of a
+ *     silent fallback, preallocated buffers that fail fast instead of reallocating.
+ *   "tinyloop Current Status", KV cache modes table: paged attention with 16-token
+ *     pages and an INT8 KV cache; model architecture support table: GQA/MQA and
+ *     chunked prefill.
+ *   "mini-llm-inference-engine" README, architectural highlights: true batched decode
+ *     (no per-sequence host loop).
+ * The attention itself is the textbook definition (the pages do not write it out):
+ *     out[h] = sum_t softmax_t(scale * q[h] . K_t[g]) V_t[g],   g = h / (Hq / Hkv).
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is caller-owned DEVICE memory unless stated otherwise.
+ *     The library allocates nothing and frees nothing.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Host-checkable errors (null pointers, shapes, dtypes, alignment, workspace size)
+ *     return a status synchronously and launch nothing.
+ *   - Device-detectable errors (a page id outside [0, num_pages), a context length
+ *     outside [0, max_blocks_per_seq * page_size], a slot outside the pool, an
+ *     inconsistent prefill chunk) are OR-ed into *dev_status as PKV_DEV_* bits; the
+ *     affected rows are written as NaN (attention) or skipped (append).  The kernels
+ *     never trap or assert.  `dev_status` may be NULL to ignore such reports.
+ *   - There is no fallback: an unsupported combination returns PKV_ERR_UNSUPPORTED.
+ *   - Only page_size 16 and head_dim 64 or 128 are supported.
+ *
+ * Cache layout (struct pkv_cache)
+ *   k_cache  [num_pages][num_kv_heads][page_size][head_dim]   row per token
+ *   v_cache  [num_pages][num_kv_heads][head_dim][page_size]   each page block transposed
+ *   k_scale, v_scale  float32 [num_pages][num_kv_heads][page_size]   INT8 only
+ *   Token t of a sequence lives in page block_tables[b][t / page_size] at offset
+ *   t % page_size; its slot number is page * page_size + offset.
+ *   Element types: PKV_F32 float32, PKV_BF16 bfloat16, PKV_INT8 int8 code c whose value
+ *   is c * scale, scale = max|x| / 127 per (token, kv head).
+ *   All cache pointers must be 16-byte aligned.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_INT8 = 2 } pkv_dtype;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_NULL = 1,        /* a required pointer is NULL */
+  PKV_ERR_SHAPE = 2,       /* a size is negative / zero where it must not be, or Hq % Hkv != 0 */
+  PKV_ERR_DTYPE = 3,       /* unknown dtype code */
+  PKV_ERR_PAGE_SIZE = 4,   /* page_size != 16 */
+  PKV_ERR_ALIGN = 5,       /* a pointer is not 16-byte aligned */
+  PKV_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than the *_workspace_size answer */
+  PKV_ERR_UNSUPPORTED = 7, /* valid but unsupported combination (e.g. head_dim 96) */
+  PKV_ERR_LAUNCH = 8,      /* the CUDA launch itself failed */
+  PKV_ERR_DEVICE = 9       /* no usable CUDA device / attribute query failed */
+} pkv_status;
+
+/* Device-side error bits OR-ed into *dev_status. */
+#define PKV_DEV_BAD_PAGE 0x1 /* block table entry outside [0, num_pages) */
+#define PKV_DEV_BAD_LEN 0x2  /* context length < 0 or > max_blocks_per_seq * page_size */
+#define PKV_DEV_BAD_SLOT 0x4 /* append slot >= num_pages * page_size */
+#define PKV_DEV_BAD_CHUNK 0x8 /* prefill chunk length < 0 or > context length */
+#define PKV_DEV_TIMEOUT 0x10 /* a bounded wait on an asynchronous copy gave up */
+
+typedef struct pkv_cache {
+  void* k_cache;
+  void* v_cache;
+  float* k_scale; /* INT8 only, else NULL */
+  float* v_scale; /* INT8 only, else NULL */
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t kv_dtype; /* pkv_dtype */
+} pkv_cache;
+
+/*
+ * KV append ("Tiny-LLM-Inference Project_Status": paged KV cache; "tinyloop Current
+ * Status": INT8 KV cache).
+ *   k_new, v_new   [num_tokens][num_kv_heads][head_dim], element type new_dtype
+ *                  (PKV_F32 or PKV_BF16).  FP32 cache: stored as is (BF16 widened
+ *                  exactly).  BF16 cache: rounded to nearest even.  INT8 cache: per
+ *                  (token, kv head) s = max|x| / 127 (IEEE division), code =
+ *                  clamp(rint(x / s), -127, 127), s and codes stored; an all-zero row
+ *                  stores s = 0 and zero codes.
+ *   slot_mapping   int32 [num_tokens]; slot < 0 skips that token (padding);
+ *                  slot >= num_pages * page_size sets PKV_DEV_BAD_SLOT and is skipped.
+ *   Slots within one call must be distinct.  num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_append(const pkv_cache* cache, const void* k_new, const void* v_new,
+                      int32_t new_dtype, const int32_t* slot_mapping, int32_t num_tokens,
+                      int32_t* dev_status, void* stream);
+
+/*
+ * Scratch bytes pkv_decode_attn needs for this shape on the current device (host
+ * call, no launch).  The split of long contexts across thread blocks is a fixed
+ * function of (shape, device SM count, pkv_set_decode_chunk_pages), so equal
+ * arguments give bit-identical results.  Writes the size to *bytes (0 is possible).
+ */
+pkv_status pkv_decode_workspace_size(const pkv_cache* cache, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                     size_t* bytes);
+
+/*
+ * Batched decode attention ("mini-llm-inference-engine" README: true batched decode;
+ * "tinyloop Current Status": 16-token paged attention, GQA).
+ *   q              [num_seqs][num_q_heads][head_dim], q_dtype PKV_F32 or PKV_BF16.
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                  ceil(context_lens[b] / page_size) entries of a row are read.
+ *   context_lens   int32 [num_seqs]; tokens of sequence b in cache, the current one
+ *                  included (append it first).  0 gives a zero output row.
+ *   scale          softmax scale (typically 1 / sqrt(head_dim)).
+ *   out            float32 [num_seqs][num_q_heads][head_dim].
+ *   workspace      device scratch of at least pkv_decode_workspace_size bytes, 16-byte
+ *                  aligned.  It must be zero-filled before its first use; every call
+ *                  leaves it ready for the next (its counters return to zero).  Calls
+ *                  that share a workspace must not run concurrently.
+ */
+pkv_status pkv_decode_attn(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                           int32_t num_seqs, int32_t num_q_heads, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           float scale, float* out, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream);
+
+/*
+ * Scratch bytes pkv_prefill_chunk_attn needs (host call, no launch); see above.
+ */
+pkv_status pkv_prefill_workspace_size(const pkv_cache* cache, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t max_q_len,
+                                      int32_t max_blocks_per_seq, size_t* bytes);
+
+/*
+ * Chunked-prefill attention ("Tiny-LLM-Inference Project_Status": chunked prefill,
+ * chunked-prefill SDPA path; "tinyloop Current Status": chunked prefill at chunk 512).
+ *   q              [total_q][num_q_heads][head_dim] (q_dtype PKV_BF16 or PKV_F32),
+ *                  sequence b owning rows q_start_loc[b] .. q_start_loc[b+1]-1.
+ *   q_start_loc    int32 [num_seqs + 1], non-decreasing, q_start_loc[0] == 0.
+ *   max_q_len      an upper bound of the chunk lengths (sizes the launch).
+ *   context_lens   int32 [num_seqs]: cached tokens INCLUDING the chunk (append the
+ *                  chunk first).  Chunk row i (chunk length Lq) sits at position
+ *                  context_lens[b] - Lq + i and attends to positions 0..that position.
+ *   out            float32 [total_q][num_q_heads][head_dim].
+ *   workspace      as for decode (pkv_prefill_workspace_size bytes; may be 0).
+ */
+pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                                  int32_t num_seqs, int32_t num_q_heads,
+                                  const int32_t* q_start_loc, int32_t max_q_len,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, float scale, float* out,
+                                  void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream);
+
+/*
+ * Tuning override: pages per thread block for the decode split (0 = automatic, the
+ * default).  Process-wide; affects pkv_decode_workspace_size.  Meant for tests and
+ * sweeps, not for changing results (splits only reorder floating-point sums).
+ */
+void pkv_set_decode_chunk_pages(int32_t pages);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* pkv_status_string(pkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

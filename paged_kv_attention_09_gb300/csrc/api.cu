@@ -1,0 +1,222 @@
+// api.cu — the extern "C" boundary declared in include/pkv.h: argument validation,
+// planning and launches.  Allocates nothing; every buffer belongs to the caller
+// ("Tiny-LLM-Inference Project_Status", runtime notes: buffers are preallocated from the
+// resolved capacity and an oversized request fails fast instead of reallocating).
+#include <atomic>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "pkv.h"
+
+namespace {
+
+std::atomic<int> g_chunk_override{0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+pkv_status check_cache(const pkv_cache* c) {
+  if (!c || !c->k_cache || !c->v_cache) return PKV_ERR_NULL;
+  if (c->kv_dtype < PKV_F32 || c->kv_dtype > PKV_INT8) return PKV_ERR_DTYPE;
+  if (c->page_size != 16) return PKV_ERR_PAGE_SIZE;
+  if (c->num_pages < 1 || c->num_kv_heads < 1 || c->head_dim < 1) return PKV_ERR_SHAPE;
+  if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (c->kv_dtype == PKV_INT8 && (!c->k_scale || !c->v_scale)) return PKV_ERR_NULL;
+  if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PKV_ERR_ALIGN;
+  if (c->kv_dtype == PKV_INT8 && (!aligned16(c->k_scale) || !aligned16(c->v_scale)))
+    return PKV_ERR_ALIGN;
+  // every page block must stay addressable with 32-bit slot numbers
+  if (static_cast<long long>(c->num_pages) * c->page_size > 0x7fffffffLL) return PKV_ERR_SHAPE;
+  return PKV_OK;
+}
+
+pkv::CacheView view(const pkv_cache* c) {
+  return pkv::CacheView{c->k_cache, c->v_cache, c->k_scale, c->v_scale,
+                        c->num_pages, c->num_kv_heads, c->head_dim, c->kv_dtype};
+}
+
+pkv_status current_device(int* dev) {
+  return cudaGetDevice(dev) == cudaSuccess ? PKV_OK : PKV_ERR_DEVICE;
+}
+
+pkv_status check_decode_shape(const pkv_cache* c, int32_t num_seqs, int32_t Hq, int32_t MB) {
+  if (num_seqs < 0 || Hq < 1 || MB < 1) return PKV_ERR_SHAPE;
+  if (Hq % c->num_kv_heads != 0) return PKV_ERR_SHAPE;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;  // grid.y limit
+  if (static_cast<long long>(MB) * c->page_size > 0x7fffffffLL) return PKV_ERR_SHAPE;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_append(const pkv_cache* cache, const void* k_new, const void* v_new,
+                      int32_t new_dtype, const int32_t* slot_mapping, int32_t num_tokens,
+                      int32_t* dev_status, void* stream) {
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (new_dtype != PKV_F32 && new_dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping) return PKV_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned4(slot_mapping)) return PKV_ERR_ALIGN;
+  if (dev_status && !aligned4(dev_status)) return PKV_ERR_ALIGN;
+  const cudaError_t e = pkv::launch_append(
+      view(cache), cache->k_cache, cache->v_cache, cache->k_scale, cache->v_scale, k_new, v_new,
+      new_dtype, slot_mapping, num_tokens, dev_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+pkv_status pkv_decode_workspace_size(const pkv_cache* cache, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                     size_t* bytes) {
+  if (!bytes) return PKV_ERR_NULL;
+  *bytes = 0;
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
+  if (s != PKV_OK) return s;
+  int dev = 0;
+  if ((s = current_device(&dev)) != PKV_OK) return s;
+  pkv::DecodePlan plan{};
+  if (!pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, PKV_F32, dev,
+                        g_chunk_override.load(), &plan))
+    return PKV_ERR_DEVICE;
+  *bytes = plan.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_attn(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                           int32_t num_seqs, int32_t num_q_heads, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           float scale, float* out, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream) {
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
+  if (s != PKV_OK) return s;
+  if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !block_tables || !context_lens || !out) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(block_tables) || !aligned4(context_lens))
+    return PKV_ERR_ALIGN;
+  if (dev_status && !aligned4(dev_status)) return PKV_ERR_ALIGN;
+  int dev = 0;
+  if ((s = current_device(&dev)) != PKV_OK) return s;
+  pkv::DecodePlan plan{};
+  if (!pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, q_dtype, dev,
+                        g_chunk_override.load(), &plan))
+    return PKV_ERR_DEVICE;
+  if (static_cast<long long>(cache->num_kv_heads) * plan.head_groups > 65535)
+    return PKV_ERR_UNSUPPORTED;
+  if (plan.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.ws_bytes) return PKV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PKV_ERR_ALIGN;
+  }
+  pkv::DecodeArgs a{};
+  a.c = view(cache);
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.B = num_seqs;
+  a.Hq = num_q_heads;
+  a.MB = max_blocks_per_seq;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.scale = scale;
+  a.out = out;
+  a.ws = workspace;
+  a.dev_status = dev_status;
+  const cudaError_t e = pkv::launch_decode(a, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+pkv_status pkv_prefill_workspace_size(const pkv_cache* cache, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t max_q_len,
+                                      int32_t max_blocks_per_seq, size_t* bytes) {
+  if (!bytes) return PKV_ERR_NULL;
+  *bytes = 0;
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
+  if (s != PKV_OK) return s;
+  if (max_q_len < 0) return PKV_ERR_SHAPE;
+  int dev = 0;
+  if ((s = current_device(&dev)) != PKV_OK) return s;
+  pkv::PrefillPlan plan{};
+  if (!pkv::plan_prefill(view(cache), num_seqs, num_q_heads, max_q_len, max_blocks_per_seq,
+                         PKV_BF16, dev, &plan))
+    return PKV_ERR_UNSUPPORTED;
+  *bytes = plan.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                                  int32_t num_seqs, int32_t num_q_heads,
+                                  const int32_t* q_start_loc, int32_t max_q_len,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, float scale, float* out,
+                                  void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream) {
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
+  if (s != PKV_OK) return s;
+  if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (max_q_len < 0) return PKV_ERR_SHAPE;
+  if (num_seqs == 0 || max_q_len == 0) return PKV_OK;
+  if (!q || !q_start_loc || !block_tables || !context_lens || !out) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(q_start_loc) || !aligned4(block_tables) ||
+      !aligned4(context_lens))
+    return PKV_ERR_ALIGN;
+  if (dev_status && !aligned4(dev_status)) return PKV_ERR_ALIGN;
+  int dev = 0;
+  if ((s = current_device(&dev)) != PKV_OK) return s;
+  pkv::PrefillPlan plan{};
+  if (!pkv::plan_prefill(view(cache), num_seqs, num_q_heads, max_q_len, max_blocks_per_seq,
+                         q_dtype, dev, &plan))
+    return PKV_ERR_UNSUPPORTED;
+  if (plan.n_row_tiles > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+  if (plan.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.ws_bytes) return PKV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PKV_ERR_ALIGN;
+  }
+  pkv::PrefillArgs a{};
+  a.c = view(cache);
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.B = num_seqs;
+  a.Hq = num_q_heads;
+  a.MB = max_blocks_per_seq;
+  a.max_q_len = max_q_len;
+  a.q_start_loc = q_start_loc;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.scale = scale;
+  a.out = out;
+  a.ws = workspace;
+  a.dev_status = dev_status;
+  const cudaError_t e = pkv::launch_prefill(a, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+void pkv_set_decode_chunk_pages(int32_t pages) { g_chunk_override.store(pages > 0 ? pages : 0); }
+
+const char* pkv_status_string(pkv_status status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_NULL: return "PKV_ERR_NULL: a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE: invalid size or head counts";
+    case PKV_ERR_DTYPE: return "PKV_ERR_DTYPE: unknown dtype code";
+    case PKV_ERR_PAGE_SIZE: return "PKV_ERR_PAGE_SIZE: page_size must be 16";
+    case PKV_ERR_ALIGN: return "PKV_ERR_ALIGN: pointer not 16-byte aligned";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: workspace missing or too small";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: combination not supported";
+    case PKV_ERR_LAUNCH: return "PKV_ERR_LAUNCH: CUDA launch failed";
+    case PKV_ERR_DEVICE: return "PKV_ERR_DEVICE: no usable CUDA device";
+  }
+  return "PKV_UNKNOWN_STATUS";
+}
+
+}  // extern "C"

@@ -1,0 +1,194 @@
+"""Python binding of libpkv.so: the C ABI of include/pkv.h, same names, argument
+marshalling only.  Tensors are torch CUDA tensors (torch supplies device memory and
+streams); every computation runs in the library's CUDA kernels.  There is no fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpkv.so")
+
+F32, BF16, INT8 = 0, 1, 2
+_TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16, INT8: torch.int8}
+_CODE = {torch.float32: F32, torch.bfloat16: BF16, torch.int8: INT8}
+
+DEV_BAD_PAGE, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_BAD_CHUNK, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
+STATUS = {0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_DTYPE",
+          4: "PKV_ERR_PAGE_SIZE", 5: "PKV_ERR_ALIGN", 6: "PKV_ERR_WORKSPACE",
+          7: "PKV_ERR_UNSUPPORTED", 8: "PKV_ERR_LAUNCH", 9: "PKV_ERR_DEVICE"}
+EXPORTS = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn",
+           "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn",
+           "pkv_set_decode_chunk_pages", "pkv_status_string")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class pkv_cache(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libpkv.so (build it with __graft_entry__.build()); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libpkv.so not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, I32, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    C = ctypes.POINTER(pkv_cache)
+    lib.pkv_append.argtypes = [C, P, P, I32, P, I32, P, P]
+    lib.pkv_decode_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
+    lib.pkv_decode_attn.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, P, SZ, P, P]
+    lib.pkv_prefill_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
+    lib.pkv_prefill_chunk_attn.argtypes = [C, P, I32, I32, I32, P, I32, P, I32, P, F, P, P, SZ,
+                                           P, P]
+    for fn in ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn",
+               "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn"):
+        getattr(lib, fn).restype = ctypes.c_int
+    lib.pkv_set_decode_chunk_pages.argtypes = [I32]
+    lib.pkv_set_decode_chunk_pages.restype = None
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise PkvError(code, what)
+
+
+class KVCache:
+    """Device tensors of one paged cache in the library's layout.
+
+    k: [num_pages, Hkv, 16, D]; v: [num_pages, Hkv, D, 16] (page blocks transposed);
+    k_scale, v_scale: float32 [num_pages, Hkv, 16] for INT8 caches.
+    """
+
+    def __init__(self, k, v, k_scale=None, v_scale=None):
+        self.k, self.v, self.k_scale, self.v_scale = k, v, k_scale, v_scale
+        self.num_pages, self.num_kv_heads, self.page_size, self.head_dim = k.shape
+        self.kv_dtype = _CODE[k.dtype]
+
+    @classmethod
+    def allocate(cls, num_pages, num_kv_heads, head_dim, kv_dtype, device="cuda",
+                 page_size=16):
+        dt = _TORCH_DTYPE[kv_dtype]
+        k = torch.zeros(num_pages, num_kv_heads, page_size, head_dim, dtype=dt, device=device)
+        v = torch.zeros(num_pages, num_kv_heads, head_dim, page_size, dtype=dt, device=device)
+        ks = vs = None
+        if kv_dtype == INT8:
+            ks = torch.zeros(num_pages, num_kv_heads, page_size, dtype=torch.float32, device=device)
+            vs = torch.zeros_like(ks)
+        return cls(k, v, ks, vs)
+
+    def struct(self) -> pkv_cache:
+        return pkv_cache(self.k.data_ptr(), self.v.data_ptr(),
+                         None if self.k_scale is None else self.k_scale.data_ptr(),
+                         None if self.v_scale is None else self.v_scale.data_ptr(),
+                         self.num_pages, self.page_size, self.num_kv_heads, self.head_dim,
+                         self.kv_dtype)
+
+
+def pkv_status_string(code: int) -> str:
+    return load().pkv_status_string(code).decode()
+
+
+def pkv_set_decode_chunk_pages(pages: int) -> None:
+    load().pkv_set_decode_chunk_pages(int(pages))
+
+
+def pkv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+               slot_mapping: torch.Tensor, dev_status: Optional[torch.Tensor] = None,
+               stream=None) -> None:
+    c = cache.struct()
+    _check(load().pkv_append(ctypes.byref(c), _ptr(k_new), _ptr(v_new), _CODE[k_new.dtype],
+                             _ptr(slot_mapping), int(slot_mapping.shape[0]), _ptr(dev_status),
+                             _stream(stream)), "pkv_append")
+
+
+def pkv_decode_workspace_size(cache: KVCache, num_seqs: int, num_q_heads: int,
+                              max_blocks_per_seq: int) -> int:
+    c = cache.struct()
+    n = ctypes.c_size_t(0)
+    _check(load().pkv_decode_workspace_size(ctypes.byref(c), num_seqs, num_q_heads,
+                                            max_blocks_per_seq, ctypes.byref(n)),
+           "pkv_decode_workspace_size")
+    return int(n.value)
+
+
+def pkv_decode_attn(cache: KVCache, q: torch.Tensor, block_tables: torch.Tensor,
+                    context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                    workspace: Optional[torch.Tensor] = None,
+                    dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    c = cache.struct()
+    B, Hq, _ = q.shape
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_decode_attn(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
+                                  _ptr(block_tables), int(block_tables.shape[1]),
+                                  _ptr(context_lens), float(scale), _ptr(out), _ptr(workspace),
+                                  wb, _ptr(dev_status), _stream(stream)), "pkv_decode_attn")
+
+
+def pkv_prefill_workspace_size(cache: KVCache, num_seqs: int, num_q_heads: int,
+                               max_q_len: int, max_blocks_per_seq: int) -> int:
+    c = cache.struct()
+    n = ctypes.c_size_t(0)
+    _check(load().pkv_prefill_workspace_size(ctypes.byref(c), num_seqs, num_q_heads, max_q_len,
+                                             max_blocks_per_seq, ctypes.byref(n)),
+           "pkv_prefill_workspace_size")
+    return int(n.value)
+
+
+def pkv_prefill_chunk_attn(cache: KVCache, q: torch.Tensor, q_start_loc: torch.Tensor,
+                           max_q_len: int, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                           workspace: Optional[torch.Tensor] = None,
+                           dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    c = cache.struct()
+    B = int(context_lens.shape[0])
+    Hq = int(q.shape[1])
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_prefill_chunk_attn(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
+                                         _ptr(q_start_loc), int(max_q_len), _ptr(block_tables),
+                                         int(block_tables.shape[1]), _ptr(context_lens),
+                                         float(scale), _ptr(out), _ptr(workspace), wb,
+                                         _ptr(dev_status), _stream(stream)),
+           "pkv_prefill_chunk_attn")
+
+
+def workspace_for(nbytes: int, device="cuda") -> Optional[torch.Tensor]:
+    """A zero-filled workspace tensor of at least nbytes (16-byte aligned), or None."""
+    if nbytes == 0:
+        return None
+    return torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.int32, device=device)

@@ -1,0 +1,103 @@
+"""The C ABI without a GPU: the library loads, exports every function include/pkv.h
+declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_attention_09_gb300 import pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(pkv.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return pkv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(pkv.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in pkv.STATUS.items():
+        assert pkv.pkv_status_string(code).startswith(name)
+    assert pkv.pkv_status_string(1234) == "PKV_UNKNOWN_STATUS"
+
+
+def _cache(**kw):
+    base = dict(k_cache=0x10000, v_cache=0x20000, k_scale=0x30000, v_scale=0x40000,
+                num_pages=8, page_size=16, num_kv_heads=2, head_dim=64, kv_dtype=pkv.BF16)
+    base.update(kw)
+    return pkv.pkv_cache(**base)
+
+
+def _append(lib, c, k=0x50000, v=0x60000, new_dtype=pkv.F32, slots=0x70000, n=4):
+    return lib.pkv_append(ctypes.byref(c) if c is not None else None, k, v, new_dtype, slots, n,
+                          None, None)
+
+
+def test_host_validation_codes(lib):
+    assert _append(lib, None) == 1                                  # NULL cache
+    assert _append(lib, _cache(k_cache=None)) == 1                  # NULL k_cache
+    assert _append(lib, _cache(kv_dtype=7)) == 3                    # dtype
+    assert _append(lib, _cache(page_size=8)) == 4                   # page size
+    assert _append(lib, _cache(head_dim=96)) == 7                   # unsupported D
+    assert _append(lib, _cache(num_pages=0)) == 2                   # shape
+    assert _append(lib, _cache(k_cache=0x10008)) == 5               # alignment
+    assert _append(lib, _cache(kv_dtype=pkv.INT8, k_scale=None)) == 1
+    assert _append(lib, _cache(), new_dtype=pkv.INT8) == 3          # INT8 sources
+    assert _append(lib, _cache(), k=0x50004) == 5
+    assert _append(lib, _cache(), n=-1) == 2
+    assert _append(lib, _cache(), k=None, n=0) == 0                 # empty call: no-op
+
+
+def test_decode_and_prefill_validation(lib):
+    c = _cache()
+    P = None
+    n = ctypes.c_size_t(0)
+    # Hq not a multiple of Hkv
+    assert lib.pkv_decode_attn(ctypes.byref(c), 0x80000, pkv.F32, 2, 3, 0x90000, 4, 0xA0000,
+                               0.1, 0xB0000, P, 0, P, P) == 2
+    assert lib.pkv_decode_workspace_size(ctypes.byref(c), 2, 3, 4, ctypes.byref(n)) == 2
+    # bad q dtype
+    assert lib.pkv_decode_attn(ctypes.byref(c), 0x80000, pkv.INT8, 2, 4, 0x90000, 4, 0xA0000,
+                               0.1, 0xB0000, P, 0, P, P) == 3
+    # zero sequences: no-op
+    assert lib.pkv_decode_attn(ctypes.byref(c), P, pkv.F32, 0, 4, P, 4, P, 0.1, P, P, 0, P,
+                               P) == 0
+    # misaligned output
+    assert lib.pkv_decode_attn(ctypes.byref(c), 0x80000, pkv.F32, 2, 4, 0x90000, 4, 0xA0000,
+                               0.1, 0xB0004, P, 0, P, P) == 5
+    # max_blocks_per_seq < 1
+    assert lib.pkv_decode_attn(ctypes.byref(c), 0x80000, pkv.F32, 2, 4, 0x90000, 0, 0xA0000,
+                               0.1, 0xB0000, P, 0, P, P) == 2
+    # prefill: negative max_q_len, misaligned q
+    assert lib.pkv_prefill_chunk_attn(ctypes.byref(c), 0x80000, pkv.BF16, 2, 4, 0xC0000, -1,
+                                      0x90000, 4, 0xA0000, 0.1, 0xB0000, P, 0, P, P) == 2
+    assert lib.pkv_prefill_chunk_attn(ctypes.byref(c), 0x80008, pkv.BF16, 2, 4, 0xC0000, 8,
+                                      0x90000, 4, 0xA0000, 0.1, 0xB0000, P, 0, P, P) == 5
+    assert lib.pkv_decode_workspace_size(ctypes.byref(c), 2, 4, 4, None) == 1
+
+
+def test_no_device_is_reported_not_crashed(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    c = _cache()
+    n = ctypes.c_size_t(0)
+    assert lib.pkv_decode_workspace_size(ctypes.byref(c), 2, 4, 4, ctypes.byref(n)) == 9

@@ -1,0 +1,83 @@
+"""Chunked-prefill attention on the GPU vs the FP64 oracle (BF16 KV cache).
+
+Chunks of assorted lengths (1 token, page-aligned, ragged, longer than a tile) over
+assorted prior contexts (none, partial page, several tiles); FP32 and BF16 queries;
+NaN-poisoned padding; device-side errors; sampled rows of the full-size mixed workload.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_attention_09_gb300 import pkv
+from paged_kv_attention_09_gb300 import workloads as W
+
+from gpu_util import gpu_outputs, max_err, oracle_outputs
+
+pytestmark = pytest.mark.gpu
+
+CHUNKS = [(0, 1), (0, 16), (5, 1), (20, 13), (16, 48), (33, 70), (130, 65), (0, 150)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,qd", [(12, 2, 128, W.BF16), (12, 2, 128, W.F32),
+                                         (8, 8, 64, W.BF16), (4, 1, 64, W.F32),
+                                         (16, 2, 128, W.BF16)])
+def test_prefill_small_parity(Hq, Hkv, D, qd):
+    wl = W.small_workload(3000 + Hq + D + qd, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                          kv_dtype=W.BF16, q_dtype=qd, prefill=CHUNKS)
+    ref = oracle_outputs(wl)[0]
+    got, status, _ = gpu_outputs(wl)
+    assert status == 0
+    assert max_err(got[0], ref) <= 2e-3
+
+
+def test_prefill_poisoned_padding():
+    wl = W.small_workload(3100, num_q_heads=6, num_kv_heads=2, head_dim=128, kv_dtype=W.BF16,
+                          q_dtype=W.BF16, prefill=[(3, 9), (40, 21)], max_prefill_len=128)
+    ref = oracle_outputs(wl)[0]
+    got, status, _ = gpu_outputs(wl, cache_fill=float("nan"))
+    assert status == 0
+    assert np.all(np.isfinite(got[0]))
+    assert max_err(got[0], ref) <= 2e-3
+
+
+def test_prefill_bad_inputs_give_nan_rows_and_status():
+    wl = W.small_workload(3101, num_q_heads=4, num_kv_heads=2, head_dim=64, kv_dtype=W.BF16,
+                          q_dtype=W.BF16, prefill=[(10, 10), (10, 10), (10, 10)],
+                          max_prefill_len=64)
+    b = wl.batches[0]
+    b.block_tables[0, 1] = -5                  # bad page
+    b.context_lens[1] = 5                      # chunk (10) longer than the context
+    got, status, _ = gpu_outputs(wl)
+    assert status & pkv.DEV_BAD_PAGE and status & pkv.DEV_BAD_CHUNK
+    assert np.all(np.isnan(got[0][0:10])) and np.all(np.isnan(got[0][10:20]))
+    assert np.all(np.isfinite(got[0][20:30]))
+
+
+def test_prefill_lq1_matches_decode():
+    """A one-token chunk is a decode step: both kernels must agree within tolerance."""
+    wl = W.small_workload(3102, num_q_heads=12, num_kv_heads=2, head_dim=128, kv_dtype=W.BF16,
+                          q_dtype=W.BF16, prefill=[(77, 1), (0, 1), (300, 1)])
+    got_p, _, _ = gpu_outputs(wl)
+    b = wl.batches[0]
+    dec = W.Batch("decode", b.context_lens, b.block_tables, b.q, b.q_dtype)
+    wl.batches = [dec]
+    got_d, _, _ = gpu_outputs(wl)
+    assert max_err(got_p[0], got_d[0]) <= 2e-3
+
+
+def test_mixed_full_size_prefill_sampled_rows():
+    wl = W.workload("mixed")
+    got, status, _ = gpu_outputs(wl)
+    assert status == 0
+    i = [k for k, b in enumerate(wl.batches) if b.kind == "prefill"][0]
+    b = wl.batches[i]
+    oc = oracle.cache_from_workload(wl)
+    # the oracle recomputes chosen rows as one-token chunks at their positions
+    rows = [0, 1, 255, 511, 512, 700, 1023]
+    for r in rows:
+        s = 0 if r < 512 else 1
+        pos = int(b.context_lens[s]) - 512 + (r - 512 * s)
+        ref = oracle.decode(oc, b.q[r:r + 1], b.q_dtype, b.block_tables[s:s + 1],
+                            np.array([pos + 1], np.int32), wl.scale)
+        assert max_err(got[i][r], ref[0]) <= 2e-3, r
+    assert np.all(np.isfinite(got[i]))
