@@ -1,30 +1,36 @@
 // decode.cu — batched paged decode attention with split-K over pages.
 //
 // Sources: "mini-llm-inference-engine" README (true batched decode, one launch for the
-// whole batch); "tinyloop Current Status" (paged attention with 16-token pages; GQA);
-// "Tiny-LLM-Inference Project_Status" (FP32 default KV, dedicated BF16 paged kernel,
-// FP32 operator boundaries).  The attention is the textbook softmax(scale q.K^T) V,
-// evaluated with a running max / running sum (online softmax) so that every K/V byte is
-// read from HBM exactly once.
+// whole batch); "tinyloop Current Status" (paged attention with 16-token pages; GQA;
+// INT8 KV cache); "Tiny-LLM-Inference Project_Status" (FP32 default KV, dedicated BF16
+// paged kernel, FP32 operator boundaries).  The attention is the textbook
+// softmax(scale q.K^T) V, evaluated with a running max / running sum (online softmax)
+// so that every K/V byte is read from HBM exactly once.
 //
 // Thread-block layout: grid (split, sequence, kv-head x head-group).  A block owns up to
 // 8 query heads that share one kv head, and a contiguous range of the sequence's
-// logical pages.  Each of its 4 warps streams every 4th page of that range through its
-// own ring of shared-memory stages filled by 1-D bulk copies (TMA engine, one copy per
-// K block and per V block of a (page, kv-head)), so each warp keeps several pages in
-// flight without any block-wide synchronisation.  Warps merge their (max, sum, acc)
+// logical pages.  Each of its 4 warps streams every 4th group of PPI pages of that range
+// through its own ring of shared-memory stages filled by 1-D bulk copies (TMA engine,
+// one copy per K block, V block and scale vector of a (page, kv-head)).  The producer
+// lane validates every page id just before issuing its copies, so the first copies are
+// in flight before the queries are even loaded.  Warps merge their (max, sum, acc)
 // states at the end; when a sequence is split over several blocks, the block that
 // arrives last (an atomic ticket, no waiting) merges the partial states in split order.
 //
-// Two compute paths:
-//   FP32 KV  — CUDA cores.  8 lanes per token compute the q.k dot products (3 shuffle
-//              steps), lanes own head_dim columns for P.V.
-//   BF16/INT8 KV — warp-level tensor-core MMA (m16n8k16).  The query heads of the group
-//              form the A rows (high part in rows 0-7, the rounding remainder in rows
-//              8-15, so the product is accurate to ~2^-16 relative), a 16-token page
-//              forms two n8 tiles of keys.  INT8 codes are converted exactly to f16
-//              (|code| <= 127); per-token scales are applied to the scores (K) and to the
-//              probabilities (V) in FP32.
+// Three compute paths:
+//   FP32 KV — CUDA cores.  8 lanes per token compute the q.k dot products (3 shuffle
+//             steps), lanes own head_dim columns for P.V.
+//   BF16 KV — warp-level tensor-core MMA (m16n8k16, BF16).  The query heads of the group
+//             form the A rows: the BF16 high part in rows 0-7, the rounding remainder in
+//             rows 8-15, so FP32 queries keep ~16 bits; the probabilities use the same
+//             hi/lo split for P.V.
+//   INT8 KV — q.k on the s8 tensor-core MMA (m16n8k32): the query row is quantised as
+//             hi + lo/254 (two int8 codes per element, rows 0-7 and 8-15), so the cached
+//             codes feed the MMA without conversion; per-token K scales multiply the
+//             scores in FP32.  P.V on f16 MMA: codes become the exact f16 values
+//             1152 + code with two byte permutes, the probabilities (times the V scales)
+//             are split hi/lo in f16, and the 1152 * sum(P) bias is removed once at the
+//             end.
 // The order of every floating-point reduction depends only on logical token positions,
 // the split size and the warp count, so results are bit-identical under any physical
 // page permutation.
@@ -67,24 +73,51 @@ struct ElemSize {
   static constexpr int value = KVT == kF32 ? 4 : (KVT == kBF16 ? 2 : 1);
 };
 
+// Pages per iteration of a warp, stages (iterations in flight) per warp, and the
+// resident blocks per SM the kernel is compiled for.  The copies always land well
+// before a warp needs them, so the stage depth is kept small in favour of more
+// resident warps (the per-page math is what bounds these kernels).
+#ifndef PKV_INT8_PPI
+#define PKV_INT8_PPI 1
+#endif
+#ifndef PKV_INT8_STAGES
+#define PKV_INT8_STAGES 3
+#endif
+#ifndef PKV_BF16_STAGES
+#define PKV_BF16_STAGES 2
+#endif
+template <int KVT, int D>
+struct Tune {
+  static constexpr int PPI = KVT == kINT8 ? PKV_INT8_PPI : 1;
+  static constexpr int S = KVT == kINT8 ? PKV_INT8_STAGES
+                         : KVT == kBF16 ? (D == 64 ? 3 : PKV_BF16_STAGES)
+                                        : (D == 64 ? 3 : 2);
+  static constexpr int minBlocks = (KVT == kINT8 && D == 64) ? 7 : (KVT == kBF16 && D == 128) ? 3 : 1;
+};
+
 template <int KVT, int D>
 struct Layout {
   static constexpr int esz = ElemSize<KVT>::value;
-  static constexpr int kBytes = kPage * D * esz;          // K block of one (page, head)
-  static constexpr int vBytes = kPage * D * esz;          // V block of one (page, head)
+  static constexpr int kBytes = kPage * D * esz;               // K block of one (page, head)
+  static constexpr int vBytes = kPage * D * esz;               // V block of one (page, head)
   static constexpr int sBytes = KVT == kINT8 ? kPage * 4 : 0;  // one scale vector
-  static constexpr int stageBytes = kBytes + vBytes + 2 * sBytes;
+  static constexpr int pageBytes = kBytes + vBytes + 2 * sBytes;
+  static constexpr int PPI = Tune<KVT, D>::PPI;
+  static constexpr int S = Tune<KVT, D>::S;
+  static constexpr int stageBytes = PPI * pageBytes;
 };
 
-template <int KVT, int D, int S>
+template <int KVT, int D>
 struct Smem {
   using Lo = Layout<KVT, D>;
-  static constexpr int stages = kW * S * Lo::stageBytes;
-  static constexpr int combine = kW * kMaxHeads * (D + 2) * 4;
+  static constexpr int stages = kW * Lo::S * Lo::stageBytes;
+  // merge area: per-warp max[8], sum[8], acc[8][D+2] floats
+  static constexpr int combine = (2 * kW * kMaxHeads + kW * kMaxHeads * (D + 2)) * 4;
   static constexpr int big = stages > combine ? stages : combine;
   static constexpr int probs = KVT == kF32 ? kW * kMaxHeads * kPage * 4 : 0;
-  static constexpr int bars = kW * S * 8;
-  static constexpr int total = big + probs + bars;
+  static constexpr int flags = kW * Lo::S * 4;
+  static constexpr int bars = kW * Lo::S * 8;
+  static constexpr int total = big + probs + flags + bars;
 };
 
 __device__ __forceinline__ float4 load_q4(const void* q, int q_dtype, size_t i) {
@@ -96,6 +129,40 @@ __device__ __forceinline__ float4 load_q4(const void* q, int q_dtype, size_t i) 
     return make_float4(a.x, a.y, b.x, b.y);
   }
   return *reinterpret_cast<const float4*>(static_cast<const float*>(q) + i);
+}
+
+// Split two floats into a packed high part and a packed remainder (f16 or bf16).
+__device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 f = __half22float2(h);
+  const __half2 r = __floats2half2_rn(a - f.x, b - f.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ void split_b2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 f = __bfloat1622float2(h);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(a - f.x, b - f.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// D(16x8,s32) += A(16x32,s8, row) * B(32x8,s8, col).
+__device__ __forceinline__ void mma_s8(int (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                       uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four int8 codes (a 32-bit word) -> two f16x2 words holding 1152 + code exactly:
+// byte b (biased by ^0x80) becomes the low byte of the f16 0x64XX = 1024 + (b ^ 0x80).
+__device__ __forceinline__ void s8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t biased = w ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(biased), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(biased), "r"(0x64646464u));
 }
 
 // ------------------------------------------------------------------ FP32 (CUDA cores)
@@ -233,77 +300,30 @@ struct F32Warp {
   }
 };
 
-// ------------------------------------------------------------------ BF16 / INT8 (MMA)
+// ------------------------------------------------------------------ BF16 (MMA)
 
-template <int KVT, int D>
-struct MmaWarp {
+template <int D>
+struct Bf16Warp {
   static constexpr int KS = D / 16;  // k-steps of the q.k product
   static constexpr int NT = D / 8;   // n-tiles of the P.V product
   uint32_t qa[KS][4];
   float o[NT][4];
   float m, l, row_scale;
 
-  // Which head_dim index the k-slot pair {2c, 2c+1} of k-step ks refers to.  The
-  // k-slot -> d map is a permutation chosen so that each lane's K operand is one
-  // contiguous 16-byte shared-memory load; q uses the same map.
-  __device__ static int kslot_d(int ks, int c) {
-    if constexpr (KVT == kINT8) return 64 * (ks >> 2) + 16 * c + 4 * (ks & 3);
-    else return 32 * (ks >> 1) + 8 * c + 4 * (ks & 1);
-  }
-
   __device__ void init(const DParams& p, int b, int h0, int nh, int lane) {
     const int r = lane >> 2, c = lane & 3;
     const bool has = r < nh;
-    float4 qv[KS];
-    float qmax = 0.f;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qv[ks] = has ? load_q4(p.q, p.q_dtype,
-                             (static_cast<size_t>(b) * p.Hq + h0 + r) * D + kslot_d(ks, c))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(qv[ks].x), fabsf(qv[ks].y)),
-                               fmaxf(fabsf(qv[ks].z), fabsf(qv[ks].w))));
+      // k-slot pair {2c, 2c+1} of k-step ks <-> head_dim 32(ks/2) + 8c + 4(ks%2): each
+      // lane's K operand is then one contiguous 16-byte shared-memory load.
+      const int d0 = 32 * (ks >> 1) + 8 * c + 4 * (ks & 1);
+      const float4 v = has ? load_q4(p.q, p.q_dtype, (static_cast<size_t>(b) * p.Hq + h0 + r) * D + d0)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      split_b2(v.x, v.y, qa[ks][0], qa[ks][1]);
+      split_b2(v.z, v.w, qa[ks][2], qa[ks][3]);
     }
     row_scale = p.scale_log2;
-    if constexpr (KVT == kINT8) {
-      // f16 operands: bring the row's largest |q| into [0.5, 1) by an exact power of two
-      // and fold the factor into the score scale.
-      qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
-      qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
-      int e = 0;
-      if (qmax > 0.f) frexpf(qmax, &e);
-      row_scale = ldexpf(p.scale_log2, e);
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const float x[4] = {ldexpf(qv[ks].x, -e), ldexpf(qv[ks].y, -e), ldexpf(qv[ks].z, -e),
-                            ldexpf(qv[ks].w, -e)};
-        __half hi[4], lo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          hi[j] = __float2half_rn(x[j]);
-          lo[j] = __float2half_rn(x[j] - __half2float(hi[j]));
-        }
-        qa[ks][0] = pack_half2(hi[0], hi[1]);
-        qa[ks][1] = pack_half2(lo[0], lo[1]);
-        qa[ks][2] = pack_half2(hi[2], hi[3]);
-        qa[ks][3] = pack_half2(lo[2], lo[3]);
-      }
-    } else {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const float x[4] = {qv[ks].x, qv[ks].y, qv[ks].z, qv[ks].w};
-        __nv_bfloat16 hi[4], lo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          hi[j] = __float2bfloat16_rn(x[j]);
-          lo[j] = __float2bfloat16_rn(x[j] - __bfloat162float(hi[j]));
-        }
-        qa[ks][0] = pack_bf162(hi[0], hi[1]);
-        qa[ks][1] = pack_bf162(lo[0], lo[1]);
-        qa[ks][2] = pack_bf162(hi[2], hi[3]);
-        qa[ks][3] = pack_bf162(lo[2], lo[3]);
-      }
-    }
     m = -CUDART_INF_F;
     l = 0.f;
 #pragma unroll
@@ -311,54 +331,41 @@ struct MmaWarp {
   }
 
   __device__ void page(const uint8_t* st, int valid, int lane) {
-    using Lo = Layout<KVT, D>;
+    using Lo = Layout<kBF16, D>;
     const int r = lane >> 2, c = lane & 3;
     const uint8_t* Ks = st;
     const uint8_t* Vs = st + Lo::kBytes;
-    // ---- S = Q K^T over the page's 16 tokens: n-tile j column n holds token
-    //      4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3.
-    float sacc[2][4];
+    // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
+    // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3.
+    // two accumulator chains per n-tile (even / odd k-steps) halve the MMA latency chain
+    float sacc[2][2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) sacc[j][h][0] = sacc[j][h][1] = sacc[j][h][2] = sacc[j][h][3] = 0.f;
       const int tok = 4 * (r >> 1) + (r & 1) + 2 * j;
-      const uint8_t* krow = Ks + tok * D * Lo::esz;
-      if constexpr (KVT == kINT8) {
+      const uint8_t* krow = Ks + tok * D * 2;
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk) {
-          const uint4 w = *reinterpret_cast<const uint4*>(krow + blk * 64 + c * 16);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            uint32_t b0, b1;
-            s8x4_to_f16x4(ws[s], b0, b1);
-            mma_f16(sacc[j], qa[4 * blk + s], b0, b1);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int blk = 0; blk < D / 32; ++blk) {
-          const uint4 w = *reinterpret_cast<const uint4*>(krow + (blk * 32 + c * 8) * 2);
-          mma_bf16(sacc[j], qa[2 * blk + 0], w.x, w.y);
-          mma_bf16(sacc[j], qa[2 * blk + 1], w.z, w.w);
-        }
+      for (int blk = 0; blk < D / 32; ++blk) {
+        const uint4 w = *reinterpret_cast<const uint4*>(krow + (blk * 32 + c * 8) * 2);
+        mma_bf16(sacc[j][0], qa[2 * blk + 0], w.x, w.y);
+        mma_bf16(sacc[j][1], qa[2 * blk + 1], w.z, w.w);
       }
     }
     float x[4];
-    x[0] = (sacc[0][0] + sacc[0][2]) * row_scale;
-    x[1] = (sacc[0][1] + sacc[0][3]) * row_scale;
-    x[2] = (sacc[1][0] + sacc[1][2]) * row_scale;
-    x[3] = (sacc[1][1] + sacc[1][3]) * row_scale;
-    float vsc[4] = {1.f, 1.f, 1.f, 1.f};
-    if constexpr (KVT == kINT8) {
-      const float4 k4 = *reinterpret_cast<const float4*>(st + 2 * Lo::kBytes + c * 16);
-      const float4 v4 = *reinterpret_cast<const float4*>(st + 2 * Lo::kBytes + Lo::sBytes + c * 16);
-      x[0] *= k4.x; x[1] *= k4.y; x[2] *= k4.z; x[3] *= k4.w;
-      vsc[0] = v4.x; vsc[1] = v4.y; vsc[2] = v4.z; vsc[3] = v4.w;
-    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = (4 * c + i) < valid ? x[i] : -CUDART_INF_F;
-    // ---- online softmax (rows r and r+8 both belong to head r)
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        x[2 * j + e] = ((sacc[j][0][e] + sacc[j][0][2 + e]) + (sacc[j][1][e] + sacc[j][1][2 + e])) *
+                       row_scale;
+    uint32_t vmask0 = 0xffffffffu, vmask1 = 0xffffffffu;
+    if (valid < kPage) {  // padding tokens may hold NaN: mask scores, zero their V entries
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = (4 * c + i) < valid ? x[i] : -CUDART_INF_F;
+      vmask0 = (4 * c + 0 < valid ? 0x0000ffffu : 0u) | (4 * c + 1 < valid ? 0xffff0000u : 0u);
+      vmask1 = (4 * c + 2 < valid ? 0x0000ffffu : 0u) | (4 * c + 3 < valid ? 0xffff0000u : 0u);
+    }
     float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -369,55 +376,20 @@ struct MmaWarp {
 #pragma unroll
     for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(x[i] - mn);
     l = l * corr + (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      o[j][0] *= corr; o[j][1] *= corr; o[j][2] *= corr; o[j][3] *= corr;
+      for (int j = 0; j < NT; ++j) {
+        o[j][0] *= corr; o[j][1] *= corr; o[j][2] *= corr; o[j][3] *= corr;
+      }
     }
-    // ---- P.V: A rows r = high part, r+8 = remainder; k = the page's 16 tokens.
     uint32_t pa[4];
-    if constexpr (KVT == kINT8) {
-      __half hi[4], lo[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float pp = (4 * c + i) < valid ? pr[i] * vsc[i] : 0.f;
-        hi[i] = __float2half_rn(pp);
-        lo[i] = __float2half_rn(pp - __half2float(hi[i]));
-      }
-      pa[0] = pack_half2(hi[0], hi[1]);
-      pa[1] = pack_half2(lo[0], lo[1]);
-      pa[2] = pack_half2(hi[2], hi[3]);
-      pa[3] = pack_half2(lo[2], lo[3]);
-    } else {
-      __nv_bfloat16 hi[4], lo[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        hi[i] = __float2bfloat16_rn(pr[i]);
-        lo[i] = __float2bfloat16_rn(pr[i] - __bfloat162float(hi[i]));
-      }
-      pa[0] = pack_bf162(hi[0], hi[1]);
-      pa[1] = pack_bf162(lo[0], lo[1]);
-      pa[2] = pack_bf162(hi[2], hi[3]);
-      pa[3] = pack_bf162(lo[2], lo[3]);
-    }
-    uint32_t vmask0 = 0xffffffffu, vmask1 = 0xffffffffu;
-    if constexpr (KVT == kBF16) {
-      if (valid < kPage) {  // padding tokens may hold NaN: zero their V entries
-        vmask0 = (4 * c + 0 < valid ? 0x0000ffffu : 0u) | (4 * c + 1 < valid ? 0xffff0000u : 0u);
-        vmask1 = (4 * c + 2 < valid ? 0x0000ffffu : 0u) | (4 * c + 3 < valid ? 0xffff0000u : 0u);
-      }
-    }
+    split_b2(pr[0], pr[1], pa[0], pa[1]);
+    split_b2(pr[2], pr[3], pa[2], pa[3]);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const int d = 8 * j + r;
-      if constexpr (KVT == kINT8) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + d * kPage + 4 * c);
-        uint32_t b0, b1;
-        s8x4_to_f16x4(w, b0, b1);
-        mma_f16(o[j], pa, b0, b1);
-      } else {
-        const uint2 w = *reinterpret_cast<const uint2*>(Vs + (d * kPage + 4 * c) * 2);
-        mma_bf16(o[j], pa, w.x & vmask0, w.y & vmask1);
-      }
+      const uint2 w = *reinterpret_cast<const uint2*>(Vs + (d * kPage + 4 * c) * 2);
+      mma_bf16(o[j], pa, w.x & vmask0, w.y & vmask1);
     }
   }
 
@@ -438,26 +410,209 @@ struct MmaWarp {
   }
 };
 
-template <int KVT, int D>
-struct WarpOf {
-  using type = MmaWarp<KVT, D>;
+// ------------------------------------------------------------------ INT8 (s8 + f16 MMA)
+
+template <int D>
+struct Int8Warp {
+  static constexpr int KB = D / 64;  // 64-column blocks of head_dim
+  static constexpr int NT = D / 8;   // n-tiles of the P.V product
+  static constexpr int PPI = Tune<kINT8, D>::PPI;  // pages per iteration
+  uint32_t qa[2 * KB][4];            // s8 A fragments: [k-step][a0..a3]
+  float o[NT][4];
+  float m, l, sp, row_scale;
+
+  __device__ void init(const DParams& p, int b, int h0, int nh, int lane) {
+    const int r = lane >> 2, c = lane & 3;
+    const bool has = r < nh;
+    // lane (r, c) needs q[r][64 blk + 16c .. +15]; k-step 2 blk + h covers head_dim
+    // 64 blk + 16c + 8h + {0..3} (k-slots 4c..4c+3) and {4..7} (k-slots 16+4c..).
+    float qv[KB][16];
+    float qmax = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < KB; ++blk)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = has ? load_q4(p.q, p.q_dtype,
+                                       (static_cast<size_t>(b) * p.Hq + h0 + r) * D + 64 * blk +
+                                           16 * c + 4 * i)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[blk][4 * i + 0] = v.x; qv[blk][4 * i + 1] = v.y;
+        qv[blk][4 * i + 2] = v.z; qv[blk][4 * i + 3] = v.w;
+        qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+      }
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+    // q ~= (qmax / 127) * (hi + lo / 254), hi and lo int8 codes
+    const float inv = qmax > 0.f ? 127.f / qmax : 0.f;
+#pragma unroll
+    for (int blk = 0; blk < KB; ++blk)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float t = qv[blk][8 * h + e] * inv;
+          const float hi = rintf(t);
+          const float lo = rintf((t - hi) * 254.f);
+          const uint32_t hb = static_cast<uint32_t>(static_cast<int>(hi)) & 0xffu;
+          const uint32_t lb = static_cast<uint32_t>(static_cast<int>(lo)) & 0xffu;
+          hw[e >> 2] |= hb << (8 * (e & 3));
+          lw[e >> 2] |= lb << (8 * (e & 3));
+        }
+        qa[2 * blk + h][0] = hw[0];  // row r,   k-slots 4c..4c+3
+        qa[2 * blk + h][1] = lw[0];  // row r+8
+        qa[2 * blk + h][2] = hw[1];  // row r,   k-slots 16+4c..
+        qa[2 * blk + h][3] = lw[1];  // row r+8
+      }
+    row_scale = p.scale_log2 * (qmax * (1.f / 127.f));
+    m = -CUDART_INF_F;
+    l = 0.f;
+    sp = 0.f;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  }
+
+  // PPI consecutive pages at st + pg * pageBytes; valid[pg] tokens each (a page with
+  // valid 0 was not loaded and its stage memory is stale).
+  __device__ void pages(const uint8_t* st, const int (&valid)[PPI], int lane) {
+    using Lo = Layout<kINT8, D>;
+    const int r = lane >> 2, c = lane & 3;
+    float x[PPI][4];
+    float ksc[PPI][4], vsc[PPI][4];
+#pragma unroll
+    for (int pg = 0; pg < PPI; ++pg) {
+      const uint8_t* Ks = st + pg * Lo::pageBytes;
+      const float4 k4 = *reinterpret_cast<const float4*>(Ks + 2 * Lo::kBytes + c * 16);
+      const float4 v4 = *reinterpret_cast<const float4*>(Ks + 2 * Lo::kBytes + Lo::sBytes + c * 16);
+      ksc[pg][0] = k4.x; ksc[pg][1] = k4.y; ksc[pg][2] = k4.z; ksc[pg][3] = k4.w;
+      vsc[pg][0] = v4.x; vsc[pg][1] = v4.y; vsc[pg][2] = v4.z; vsc[pg][3] = v4.w;
+      int sacc[2][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0;
+        const int tok = 4 * (r >> 1) + (r & 1) + 2 * j;
+        const uint8_t* krow = Ks + tok * D;
+#pragma unroll
+        for (int blk = 0; blk < KB; ++blk) {
+          const uint4 w = *reinterpret_cast<const uint4*>(krow + blk * 64 + c * 16);
+          mma_s8(sacc[j], qa[2 * blk + 0], w.x, w.y);
+          mma_s8(sacc[j], qa[2 * blk + 1], w.z, w.w);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          x[pg][2 * j + e] =
+              fmaf(static_cast<float>(sacc[j][2 + e]), 1.f / 254.f, static_cast<float>(sacc[j][e])) *
+              (row_scale * ksc[pg][2 * j + e]);
+    }
+    bool partial = false;
+#pragma unroll
+    for (int pg = 0; pg < PPI; ++pg) partial |= valid[pg] < kPage;
+    if (partial) {  // padding may hold NaN scales: mask by select
+#pragma unroll
+      for (int pg = 0; pg < PPI; ++pg)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const bool ok = (4 * c + i) < valid[pg];
+          x[pg][i] = ok ? x[pg][i] : -CUDART_INF_F;
+          vsc[pg][i] = ok ? vsc[pg][i] : 0.f;
+        }
+    }
+    float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
+#pragma unroll
+    for (int pg = 1; pg < PPI; ++pg)
+      mx = fmaxf(mx, fmaxf(fmaxf(x[pg][0], x[pg][1]), fmaxf(x[pg][2], x[pg][3])));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m, mx);
+    const float corr = fast_exp2(m - mn);
+    m = mn;
+    float pr[PPI][4], pv[PPI][4];
+    float ls = 0.f, ps = 0.f;
+#pragma unroll
+    for (int pg = 0; pg < PPI; ++pg)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        pr[pg][i] = fast_exp2(x[pg][i] - mn);
+        pv[pg][i] = pr[pg][i] * vsc[pg][i];
+        ls += pr[pg][i];
+        ps += pv[pg][i];
+      }
+    l = l * corr + ls;
+    sp = sp * corr + ps;
+    if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        o[j][0] *= corr; o[j][1] *= corr; o[j][2] *= corr; o[j][3] *= corr;
+      }
+    }
+#pragma unroll
+    for (int pg = 0; pg < PPI; ++pg) {
+      uint32_t pa[4];
+      split_h2(pv[pg][0], pv[pg][1], pa[0], pa[1]);
+      split_h2(pv[pg][2], pv[pg][3], pa[2], pa[3]);
+      const uint8_t* Vs = st + pg * Lo::pageBytes + Lo::kBytes;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int d = 8 * j + r;
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + d * kPage + 4 * c);
+        uint32_t b0, b1;
+        s8x4_to_f16x4_biased(w, b0, b1);
+        mma_f16(o[j], pa, b0, b1);
+      }
+    }
+  }
+
+  __device__ void store(float* cm, float* cl, float* cO, int lane) {
+    const int r = lane >> 2, c = lane & 3;
+    float lt = l, st = sp;
+    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    st += __shfl_xor_sync(0xffffffffu, st, 1);
+    st += __shfl_xor_sync(0xffffffffu, st, 2);
+    if (c == 0) {
+      cm[r] = m;
+      cl[r] = lt;
+    }
+    const float bias = 1152.f * st;  // V entered the MMA as 1152 + code
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      cO[r * (D + 2) + 8 * j + 2 * c + 0] = (o[j][0] + o[j][2]) - bias;
+      cO[r * (D + 2) + 8 * j + 2 * c + 1] = (o[j][1] + o[j][3]) - bias;
+    }
+  }
 };
+
+template <int KVT, int D>
+struct WarpOf;
 template <int D>
 struct WarpOf<kF32, D> {
   using type = F32Warp<D>;
 };
+template <int D>
+struct WarpOf<kBF16, D> {
+  using type = Bf16Warp<D>;
+};
+template <int D>
+struct WarpOf<kINT8, D> {
+  using type = Int8Warp<D>;
+};
 
 // ------------------------------------------------------------------ the kernel
 
-template <int KVT, int D, int S>
-__global__ void __launch_bounds__(kThreads)
+template <int KVT, int D>
+__global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
     decode_kernel(const __grid_constant__ DParams p) {
   using Lo = Layout<KVT, D>;
-  using Sm = Smem<KVT, D, S>;
+  using Sm = Smem<KVT, D>;
+  constexpr int S = Lo::S, PPI = Lo::PPI;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   float* probs_all = reinterpret_cast<float*>(smem + Sm::big);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::big + Sm::probs);
+  int* bad_all = reinterpret_cast<int*>(smem + Sm::big + Sm::probs);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::big + Sm::probs + Sm::flags);
   __shared__ int s_flag, s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -473,60 +628,101 @@ __global__ void __launch_bounds__(kThreads)
   if (split >= nsplit) return;
   const int pb = split * p.chunk, pe = min(np, pb + p.chunk);
   const int32_t* bt = p.bt + static_cast<size_t>(b) * p.MB;
-
-  // Validate this block's page ids before any copy is issued.
   if (tid == 0) s_flag = len_ok ? 0 : 0x2 /*PKV_DEV_BAD_LEN*/;
-  __syncthreads();
-  for (int j = pb + tid; j < pe; j += kThreads) {
-    const int pg = bt[j];
-    if (pg < 0 || pg >= p.num_pages) atomicOr(&s_flag, 0x1 /*PKV_DEV_BAD_PAGE*/);
-  }
-  __syncthreads();
-  const int bad = s_flag;
 
-  typename WarpOf<KVT, D>::type st;
   uint8_t* my_stages = stages + static_cast<size_t>(w) * S * Lo::stageBytes;
   uint64_t* my_bars = bars + w * S;
+  int* my_bad = bad_all + w * S;
   float* probs = probs_all + w * kMaxHeads * kPage;
-  bool timed_out = false;
-  st.init(p, b, h0, nh, lane);
+  // this warp's iterations: page groups w, w + kW, ... of PPI pages each
+  const int ngroups = (pe - pb + PPI - 1) / PPI;
+  const int n_my = ngroups > w ? (ngroups - w + kW - 1) / kW : 0;
 
-  if (!bad) {
-    const int span = pe - pb;
-    const int n_my = span > w ? (span - w + kW - 1) / kW : 0;
+  // ---- page ids: lane l holds those of this warp's iteration 32 k + l (batch k), for
+  // the current and the next batch, so the producer lane never waits on the block
+  // table.  -1 marks an id outside the pool, -2 a page past the block's range.
+  auto load_ids = [&](int batch, int (&ids)[PPI]) {
+    const int it = 32 * batch + lane;
+#pragma unroll
+    for (int q = 0; q < PPI; ++q) {
+      const int j = pb + (w + it * kW) * PPI + q;
+      int id = -2;
+      if (it < n_my && j < pe) {
+        id = bt[j];
+        if (id < 0 || id >= p.num_pages) id = -1;
+      }
+      ids[q] = id;
+    }
+  };
+  int ids_cur[PPI], ids_nxt[PPI];
+  load_ids(0, ids_cur);
+  load_ids(1, ids_nxt);
+
+  // ---- producer lane: barriers, then the first S groups' copies, before anything else
+  uint64_t pol = 0;
+  auto issue = [&](int i, const int (&pid)[PPI]) {
+    uint8_t* dst = my_stages + (i % S) * Lo::stageBytes;
+    uint64_t* bar = &my_bars[i % S];
+    int bad = 0, bytes = 0;
+#pragma unroll
+    for (int q = 0; q < PPI; ++q) {
+      bad |= pid[q] == -1;
+      bytes += pid[q] >= 0 ? Lo::pageBytes : 0;
+    }
+    my_bad[i % S] = bad;
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int q = 0; q < PPI; ++q) {
+      if (pid[q] < 0) continue;
+      const size_t blk = static_cast<size_t>(pid[q]) * p.Hkv + g;
+      uint8_t* d = dst + q * Lo::pageBytes;
+      bulk_g2s(d, p.k + blk * Lo::kBytes, Lo::kBytes, bar, pol);
+      bulk_g2s(d + Lo::kBytes, p.v + blk * Lo::vBytes, Lo::vBytes, bar, pol);
+      if constexpr (KVT == kINT8) {
+        bulk_g2s(d + 2 * Lo::kBytes, p.ks + blk * kPage, Lo::sBytes, bar, pol);
+        bulk_g2s(d + 2 * Lo::kBytes + Lo::sBytes, p.vs + blk * kPage, Lo::sBytes, bar, pol);
+      }
+    }
+  };
+  // ids of iteration i (warp-collective); i is at most one batch ahead of `cur`
+  auto ids_of = [&](int i, int cur_batch, int (&pid)[PPI]) {
+    const bool in_cur = (i >> 5) == cur_batch;
+#pragma unroll
+    for (int q = 0; q < PPI; ++q)
+      pid[q] = __shfl_sync(0xffffffffu, in_cur ? ids_cur[q] : ids_nxt[q], i & 31);
+  };
+  if (n_my > 0) {
     if (lane == 0) {
       for (int i = 0; i < S; ++i) mbar_init(&my_bars[i], 1);
       fence_barrier_init();
+      pol = l2_evict_first_policy();
     }
-    __syncwarp();
-    const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int i) {
-      const int j = pb + w + i * kW;
-      const size_t blk = static_cast<size_t>(bt[j]) * p.Hkv + g;
-      uint8_t* dst = my_stages + (i % S) * Lo::stageBytes;
-      uint64_t* bar = &my_bars[i % S];
-      mbar_arrive_expect_tx(bar, Lo::stageBytes);
-      bulk_g2s(dst, p.k + blk * Lo::kBytes, Lo::kBytes, bar, pol);
-      bulk_g2s(dst + Lo::kBytes, p.v + blk * Lo::vBytes, Lo::vBytes, bar, pol);
-      if constexpr (KVT == kINT8) {
-        bulk_g2s(dst + 2 * Lo::kBytes, p.ks + blk * kPage, Lo::sBytes, bar, pol);
-        bulk_g2s(dst + 2 * Lo::kBytes + Lo::sBytes, p.vs + blk * kPage, Lo::sBytes, bar, pol);
-      }
-    };
-    if (lane == 0) {
-      for (int i = 0; i < min(S, n_my); ++i) issue(i);
+    for (int i = 0; i < min(S, n_my); ++i) {
+      int pid[PPI];
+      ids_of(i, 0, pid);
+      if (lane == 0) issue(i, pid);
     }
-    int i = 0;
-    for (; i < n_my; ++i) {
-      const bool ok = mbar_wait(&my_bars[i % S], (i / S) & 1);
-      if (!__all_sync(0xffffffffu, ok)) {
-        timed_out = true;
-        break;
-      }
-      const int j = pb + w + i * kW;
-      const int valid = min(kPage, L - j * kPage);
-      const uint8_t* sp = my_stages + (i % S) * Lo::stageBytes;
+  }
+
+  typename WarpOf<KVT, D>::type st;
+  st.init(p, b, h0, nh, lane);
+  __syncwarp();
+
+  int werr = 0;
+  int i = 0;
+  for (; i < n_my; ++i) {
+    const bool ok = mbar_wait(&my_bars[i % S], (i / S) & 1);
+    if (!__all_sync(0xffffffffu, ok)) {
+      werr |= 0x10;  // PKV_DEV_TIMEOUT
+      break;
+    }
+    const uint8_t* sp = my_stages + (i % S) * Lo::stageBytes;
+    if (my_bad[i % S]) {
+      werr |= 0x1;  // PKV_DEV_BAD_PAGE
+    } else {
+      const int j0 = pb + (w + i * kW) * PPI;
       if constexpr (KVT == kF32) {
+        const int valid = min(kPage, L - j0 * kPage);
         constexpr int HM = f32_head_cap<D>();
         switch (nh) {  // the FP32 path unrolls over the block's head count
           case 1: st.template page<1>(sp, probs, valid, p.scale_log2, lane); break;
@@ -535,25 +731,39 @@ __global__ void __launch_bounds__(kThreads)
           case 4: st.template page<4>(sp, probs, valid, p.scale_log2, lane); break;
           default: st.template page<HM>(sp, probs, valid, p.scale_log2, lane); break;
         }
+      } else if constexpr (KVT == kBF16) {
+        st.page(sp, min(kPage, L - j0 * kPage), lane);
       } else {
-        st.page(sp, valid, lane);
+        int valid[PPI];
+#pragma unroll
+        for (int q = 0; q < PPI; ++q) valid[q] = j0 + q < pe ? min(kPage, L - (j0 + q) * kPage) : 0;
+        st.pages(sp, valid, lane);
       }
-      __syncwarp();
-      if (lane == 0 && i + S < n_my) issue(i + S);
     }
-    if (timed_out) {
-      // Drain (bounded) whatever this warp still has in flight before leaving.
-      for (int k = i + 1; k < min(n_my, i + S); ++k) (void)mbar_wait(&my_bars[k % S], (k / S) & 1);
+    if (i + S < n_my) {
+      if (((i + S) & 31) == 0 && i + S >= 32) {
+        // the issue index enters a new batch: it becomes the current one, prefetch the next
+#pragma unroll
+        for (int q = 0; q < PPI; ++q) ids_cur[q] = ids_nxt[q];
+        load_ids(((i + S) >> 5) + 1, ids_nxt);
+      }
+      int pid[PPI];
+      ids_of(i + S, (i + S) >> 5, pid);
+      __syncwarp();
+      if (lane == 0) issue(i + S, pid);
     }
   }
-  if (timed_out && lane == 0) atomicOr(&s_flag, 0x10 /*PKV_DEV_TIMEOUT*/);
+  if (werr & 0x10) {
+    // Drain (bounded) whatever this warp still has in flight before leaving.
+    for (int k = i + 1; k < min(n_my, i + S); ++k) (void)mbar_wait(&my_bars[k % S], (k / S) & 1);
+  }
+  if (werr && lane == 0) atomicOr(&s_flag, werr);
 
   // ---- merge the warps' states (the stage memory is reused once every warp is done)
   __syncthreads();
   float* cm = reinterpret_cast<float*>(stages);
   float* cl = cm + kW * kMaxHeads;
   float* cO = cl + kW * kMaxHeads;
-  // Combine area: cm[kW][8], cl[kW][8], cO[kW][8][D+2] (fits in the stage area).
   st.store(cm + w * kMaxHeads, cl + w * kMaxHeads, cO + w * kMaxHeads * (D + 2), lane);
   __syncthreads();
   const int err = s_flag;
@@ -595,61 +805,87 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int idx = tid; idx < nh * D; idx += kThreads) {
-    const int r = idx / D, d = idx % D;
-    const size_t row = static_cast<size_t>(b) * p.Hq + h0 + r;
+  // The merge reads every split's (max, sum) once into shared memory, turns them into
+  // weights, then accumulates the partial outputs with independent loads.
+  {
+    float* wts = reinterpret_cast<float*>(stages);  // [nsplit][8] weights, then [8] 1/L
     const size_t stride = static_cast<size_t>(p.B) * p.Hq;
-    float M = -CUDART_INF_F;
-    bool poisoned = false;
-    for (int s = 0; s < nsplit; ++s) {
-      const float ms = __ldcg(p.ws_m + s * stride + row);
-      poisoned |= isnan(ms);
-      M = fmaxf(M, ms);
+    const size_t row0 = static_cast<size_t>(b) * p.Hq + h0;
+    __syncthreads();
+    for (int idx = tid; idx < nsplit * nh; idx += kThreads) {
+      const int s = idx / nh, r = idx % nh;
+      wts[s * kMaxHeads + r] = __ldcg(p.ws_m + s * stride + row0 + r);
     }
-    float Ls = 0.f, O = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float ms = __ldcg(p.ws_m + s * stride + row);
-      const float f = ms == -CUDART_INF_F ? 0.f : fast_exp2(ms - M);
-      Ls += __ldcg(p.ws_l + s * stride + row) * f;
-      O += __ldcg(p.ws_o + (s * stride + row) * D + d) * f;
+    __syncthreads();
+    if (tid < nh) {
+      const int r = tid;
+      float M = -CUDART_INF_F;
+      bool poisoned = false;
+      for (int s = 0; s < nsplit; ++s) {
+        const float ms = wts[s * kMaxHeads + r];
+        poisoned |= isnan(ms);
+        M = fmaxf(M, ms);
+      }
+      float Ls = 0.f;
+      for (int s = 0; s < nsplit; ++s) {
+        const float ms = wts[s * kMaxHeads + r];
+        const float f = ms == -CUDART_INF_F ? 0.f : fast_exp2(ms - M);
+        wts[s * kMaxHeads + r] = f;
+        Ls += __ldcg(p.ws_l + s * stride + row0 + r) * f;
+      }
+      wts[nsplit * kMaxHeads + r] = poisoned ? CUDART_NAN_F : (Ls > 0.f ? 1.f / Ls : 0.f);
     }
-    p.out[row * D + d] = poisoned ? CUDART_NAN_F : (Ls > 0.f ? O / Ls : 0.f);
+    __syncthreads();
+    for (int idx = tid; idx < nh * D; idx += kThreads) {
+      const int r = idx / D, d = idx % D;
+      const float* src = p.ws_o + (row0 + r) * D + d;
+      float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
+      int s = 0;
+      for (; s + 4 <= nsplit; s += 4) {
+        O0 += __ldcg(src + (s + 0) * stride * D) * wts[(s + 0) * kMaxHeads + r];
+        O1 += __ldcg(src + (s + 1) * stride * D) * wts[(s + 1) * kMaxHeads + r];
+        O2 += __ldcg(src + (s + 2) * stride * D) * wts[(s + 2) * kMaxHeads + r];
+        O3 += __ldcg(src + (s + 3) * stride * D) * wts[(s + 3) * kMaxHeads + r];
+      }
+      for (; s < nsplit; ++s) O0 += __ldcg(src + s * stride * D) * wts[s * kMaxHeads + r];
+      p.out[(row0 + r) * D + d] = ((O0 + O1) + (O2 + O3)) * wts[nsplit * kMaxHeads + r];
+    }
   }
   if (tid == 0) *ticket = 0;  // leave the counter ready for the next call
 }
 
 template <int KVT, int D>
-constexpr int stages_for() {
-  return Layout<KVT, D>::stageBytes >= 8192 ? (Layout<KVT, D>::stageBytes >= 16384 ? 2 : 3) : 4;
-}
-
-template <int KVT, int D>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_kernel<KVT, D, stages_for<KVT, D>()>);
-}
-
-template <int KVT, int D>
-int smem_bytes() {
-  return Smem<KVT, D, stages_for<KVT, D>()>::total;
+  return reinterpret_cast<const void*>(&decode_kernel<KVT, D>);
 }
 
 struct Variant {
   const void* fn;
   int smem;
   int index;
+  int ppi;
+  int max_splits;  // the last block's merge keeps (splits + 1) x 8 weights in shared memory
 };
 
+template <int KVT, int D>
+constexpr int max_splits_of() {
+  return Smem<KVT, D>::big / (kMaxHeads * 4) - 1;
+}
+
+#define PKV_VARIANT(T, D, I) \
+  {kernel_ptr<T, D>(), Smem<T, D>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>()}
 Variant variant(int dtype, int D) {
   switch (dtype * 1000 + D) {
-    case kF32 * 1000 + 64: return {kernel_ptr<kF32, 64>(), smem_bytes<kF32, 64>(), 0};
-    case kF32 * 1000 + 128: return {kernel_ptr<kF32, 128>(), smem_bytes<kF32, 128>(), 1};
-    case kBF16 * 1000 + 64: return {kernel_ptr<kBF16, 64>(), smem_bytes<kBF16, 64>(), 2};
-    case kBF16 * 1000 + 128: return {kernel_ptr<kBF16, 128>(), smem_bytes<kBF16, 128>(), 3};
-    case kINT8 * 1000 + 64: return {kernel_ptr<kINT8, 64>(), smem_bytes<kINT8, 64>(), 4};
-    case kINT8 * 1000 + 128: return {kernel_ptr<kINT8, 128>(), smem_bytes<kINT8, 128>(), 5};
-    default: return {nullptr, 0, -1};
+    case kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, 0);
+    case kF32 * 1000 + 128: return PKV_VARIANT(kF32, 128, 1);
+    case kBF16 * 1000 + 64: return PKV_VARIANT(kBF16, 64, 2);
+    case kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, 3);
+    case kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, 4);
+    case kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, 5);
+    default: return {nullptr, 0, -1, 1, 1};
   }
 }
+#undef PKV_VARIANT
 
 // Per-device facts queried once: SM count, and for each kernel variant its resident
 // blocks per SM (after raising its dynamic shared-memory limit).
@@ -700,17 +936,20 @@ bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int dev
   if (chunk_override > 0) {
     chunk = chunk_override;
   } else {
-    // Aim for about two waves of blocks (upper-bound estimate: every sequence at the
-    // table's full length), but never fewer than two pages per warp.
+    // Blocks resident at once: split only as far as needed to fill them with every
+    // sequence at the table's full length, and never below 8 pages per warp, so that
+    // the partial merges stay a small fraction of the streamed bytes.
     const long long units = static_cast<long long>(B) * c.Hkv * plan->head_groups;
-    const long long target = 2LL * sms * occ;
-    long long splits = units > 0 ? (target + units - 1) / units : 1;
-    const long long max_splits = (mb + 2 * kW - 1) / (2 * kW);
+    const long long slots = static_cast<long long>(sms) * occ;
+    long long splits = units > 0 ? slots / units : 1;
+    const int min_chunk = 8 * kW * v.ppi;
+    const long long max_splits = (mb + min_chunk - 1) / min_chunk;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
     chunk = static_cast<int>((mb + splits - 1) / splits);
   }
   if (chunk < 1) chunk = 1;
+  if ((mb + chunk - 1) / chunk > v.max_splits) chunk = (mb + v.max_splits - 1) / v.max_splits;
   plan->chunk_pages = chunk;
   plan->n_splits = (mb + chunk - 1) / chunk;
   size_t ws = 0;

@@ -148,3 +148,16 @@ def test_full_size_sampled_parity(name, seqs):
     rows = list(range(b.num_seqs)) if seqs is None else seqs
     assert max_err(got[i], ref, rows) <= TOL[wl.kv_dtype]
     assert np.all(np.isfinite(got[i]))
+
+
+@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8])
+@pytest.mark.parametrize("chunk", [0, 1000])
+def test_long_context_many_iterations_per_warp(kv, chunk):
+    """A single block streaming ~300 pages gives each warp more than two batches of 32
+    iterations (the page-id prefetch rolls over); chunk 0 is the automatic split."""
+    wl = W.small_workload(99 + kv, num_q_heads=8, num_kv_heads=1, head_dim=64, kv_dtype=kv,
+                          q_dtype=W.F32, decode_lens=[16 * 300 - 5, 16 * 97 + 3])
+    ref = oracle_outputs(wl)[0]
+    got, status, _ = gpu_outputs(wl, chunk_pages=chunk)
+    assert status == 0
+    assert max_err(got[0], ref) <= TOL[kv]
