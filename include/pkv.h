@@ -165,6 +165,32 @@ pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t
                                   int32_t* dev_status, void* stream);
 
 /*
+ * Decode attention without caller-provided scratch.  (The pages describe no such
+ * call; it exists for embedding.)  Some host programs cannot call cudaMalloc or lend
+ * the library a buffer: a plugin inside an engine whose pool owns all device memory
+ * and offers no allocation hook, or a loop whose owner forbids allocation after
+ * start-up.  This entry point computes exactly what pkv_decode_attn computes, with the
+ * split-K scratch taken from a fixed array of PKV_NOALLOC_SCRATCH_BYTES in the
+ * library's own device memory (reserved on every GPU that loads the library, until the
+ * process exits).  It allocates nothing and calls no allocating routine.
+ *   - Shapes whose split scratch (what pkv_decode_workspace_size reports) exceeds
+ *     PKV_NOALLOC_SCRATCH_BYTES return PKV_ERR_WORKSPACE and launch nothing.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU (other
+ *     streams, other threads) race and must be serialised by the caller.  Each call
+ *     clears the merge counters it needs on `stream` before its kernel.
+ * Other arguments, errors and results are those of pkv_decode_attn.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (4u << 20)
+pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                                   int32_t num_seqs, int32_t num_q_heads,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, float scale, float* out,
+                                   int32_t* dev_status, void* stream);
+
+/*
  * Tuning override: pages per thread block for the decode split (0 = automatic, the
  * default).  Process-wide; affects pkv_decode_workspace_size.  Meant for tests and
  * sweeps, not for changing results (splits only reorder floating-point sums).

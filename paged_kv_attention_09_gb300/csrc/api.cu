@@ -50,6 +50,10 @@ pkv_status check_decode_shape(const pkv_cache* c, int32_t num_seqs, int32_t Hq, 
 
 }  // namespace
 
+namespace pkv {
+int decode_chunk_override() { return g_chunk_override.load(); }
+}  // namespace pkv
+
 extern "C" {
 
 pkv_status pkv_append(const pkv_cache* cache, const void* k_new, const void* v_new,

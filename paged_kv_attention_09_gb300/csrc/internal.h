@@ -47,6 +47,8 @@ struct DecodeArgs {
 // Fills `plan` for this shape on `device`; returns false for unsupported shapes.
 bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int device,
                  int chunk_override, DecodePlan* plan);
+// The process-wide split override set by pkv_set_decode_chunk_pages (0 = automatic).
+int decode_chunk_override();
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st);
 
 // ---------------------------------------------------------------- prefill

@@ -24,7 +24,8 @@ STATUS = {0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_DTYPE"
           7: "PKV_ERR_UNSUPPORTED", 8: "PKV_ERR_LAUNCH", 9: "PKV_ERR_DEVICE"}
 EXPORTS = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn",
            "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn",
-           "pkv_set_decode_chunk_pages", "pkv_status_string")
+           "pkv_decode_attn_noalloc", "pkv_set_decode_chunk_pages", "pkv_status_string")
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class PkvError(RuntimeError):
@@ -63,6 +64,8 @@ def load(path: str = LIB_PATH):
     for fn in ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn",
                "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn"):
         getattr(lib, fn).restype = ctypes.c_int
+    lib.pkv_decode_attn_noalloc.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, P, P]
+    lib.pkv_decode_attn_noalloc.restype = ctypes.c_int
     lib.pkv_set_decode_chunk_pages.argtypes = [I32]
     lib.pkv_set_decode_chunk_pages.restype = None
     lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -158,6 +161,20 @@ def pkv_decode_attn(cache: KVCache, q: torch.Tensor, block_tables: torch.Tensor,
                                   _ptr(block_tables), int(block_tables.shape[1]),
                                   _ptr(context_lens), float(scale), _ptr(out), _ptr(workspace),
                                   wb, _ptr(dev_status), _stream(stream)), "pkv_decode_attn")
+
+
+def pkv_decode_attn_noalloc(cache: KVCache, q: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                            dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """pkv_decode_attn with its split scratch in the library's fixed device array (for
+    callers that cannot allocate); see include/pkv.h for the size limit and sharing."""
+    c = cache.struct()
+    B, Hq, _ = q.shape
+    _check(load().pkv_decode_attn_noalloc(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
+                                          _ptr(block_tables), int(block_tables.shape[1]),
+                                          _ptr(context_lens), float(scale), _ptr(out),
+                                          _ptr(dev_status), _stream(stream)),
+           "pkv_decode_attn_noalloc")
 
 
 def pkv_prefill_workspace_size(cache: KVCache, num_seqs: int, num_q_heads: int,
