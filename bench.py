@@ -36,8 +36,8 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="tinyllama-int8")
     ap.add_argument("--replicas", type=int, default=0, help="0 = enough to exceed 4x L2")
@@ -258,51 +258,71 @@ def run_ours(args, rank, world):
                    for b in base.batches]
         reps.append(runner.DeviceWorkload(wl, cache, base.k_src, base.v_src, base.slots,
                                           base.step_rows, batches, base.dev_status))
-    # release the source rows that are not needed for the timed steps
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=f"cuda:{dev}")
+    stream.wait_stream(torch.cuda.current_stream())
     n_batches = len(wl.batches)
 
-    def step(i, ev=None):
+    def append_only(i):
         dw = reps[i % R]
-        if ev is not None:
-            ev[0].record(stream)
         pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
-        for j in range(n_batches):
-            if ev is not None:
-                ev[1 + j].record(stream)
-            runner.run_batch(dw, j, stream)
-        if ev is not None:
-            ev[1 + n_batches].record(stream)
 
-    for i in range(args.warmup):
-        step(i)
+    def batch_only(j):
+        return lambda i: runner.run_batch(reps[i % R], j, stream)
+
+    def step(i):
+        append_only(i)
+        for j in range(n_batches):
+            runner.run_batch(reps[i % R], j, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
     torch.cuda.synchronize()
     status = int(base.dev_status.item())
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_batches + 2)] for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                fn(args.warmup + i)
+        return g
+
+    def replay_ms(g):
+        # replay() launches on the current stream: make it the stream the events use
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    # The K timed steps are one CUDA graph (launch overhead out of the timed region);
+    # every kernel in it is ours.  Per-kernel averages come from graphs of that kernel
+    # alone over the same rotating replicas.
+    g_step = capture(step)
+    g_kern = [capture(append_only)] + [capture(batch_only(j)) for j in range(n_batches)]
+    with torch.cuda.stream(stream):
+        g_step.replay()
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev) as clk:
-        start.record(stream)
-        for i in range(K):
-            step(args.warmup + i, evs[i])
-        end.record(stream)
-        torch.cuda.synchronize()
+        total_ms = replay_ms(g_step)
     if world > 1:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
-    kern_ms = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]
-               for j in range(n_batches + 1)]
+    kern_ms = [[replay_ms(g) / K] for g in g_kern]
     if world > 1:
         t = torch.tensor([total_ms], device=f"cuda:{dev}")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms = total_ms / K
+    del g_step, g_kern
 
     # ---- end to end through the C ABI with host buffers: H2D of the step's inputs
     # (q, new K/V, slots, tables, lengths) from pinned memory, the calls, D2H of outputs
@@ -326,22 +346,23 @@ def run_ours(args, rank, world):
                 if b.q_start_loc is not None:
                     dev_in.append(b.q_start_loc)
             for d, h in zip(dev_in, host_in):
-                d.copy_(h, non_blocking=True)
+                d.copy_(h, non_blocking=True)  # on `stream` (the current stream here)
             pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
             for j in range(n_batches):
                 runner.run_batch(dw, j, stream)
             for b, h in zip(dw.batches, host_out):
                 h.copy_(b.out, non_blocking=True)
 
-        for i in range(args.warmup):
-            e2e_step(i)
-        torch.cuda.synchronize()
-        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s2.record(stream)
-        for i in range(K):
-            e2e_step(i)
-        e2.record(stream)
-        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                e2e_step(i)
+            torch.cuda.synchronize()
+            s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s2.record(stream)
+            for i in range(K):
+                e2e_step(i)
+            e2.record(stream)
+            torch.cuda.synchronize()
         e2e_ms = s2.elapsed_time(e2) / K
         if world > 1:
             t = torch.tensor([e2e_ms], device=f"cuda:{dev}")
@@ -385,6 +406,7 @@ def main():
             "batches": [{"kind": b.kind, "num_seqs": b.num_seqs,
                          "context_tokens": int(b.context_lens.sum())} for b in wl.batches],
             "step": "append new K/V rows, then attention over every batch",
+            "timing": "CUDA events around one CUDA-graph replay of the K steps",
             "bytes_per_step": acc["total"], "replicas": R,
             "l2": f"rotating {R} replicas of every input ({R} x {acc['total'] / 1e6:.1f} MB "
                   f"per cycle > {L2_BYTES / 2**20:.0f} MiB L2)",

@@ -611,7 +611,6 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   float* probs_all = reinterpret_cast<float*>(smem + Sm::big);
-  int* bad_all = reinterpret_cast<int*>(smem + Sm::big + Sm::probs);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::big + Sm::probs + Sm::flags);
   __shared__ int s_flag, s_last;
 
@@ -632,15 +631,14 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
 
   uint8_t* my_stages = stages + static_cast<size_t>(w) * S * Lo::stageBytes;
   uint64_t* my_bars = bars + w * S;
-  int* my_bad = bad_all + w * S;
   float* probs = probs_all + w * kMaxHeads * kPage;
   // this warp's iterations: page groups w, w + kW, ... of PPI pages each
   const int ngroups = (pe - pb + PPI - 1) / PPI;
   const int n_my = ngroups > w ? (ngroups - w + kW - 1) / kW : 0;
 
   // ---- page ids: lane l holds those of this warp's iteration 32 k + l (batch k), for
-  // the current and the next batch, so the producer lane never waits on the block
-  // table.  -1 marks an id outside the pool, -2 a page past the block's range.
+  // the current and the next batch, so the copies never wait on the block table.
+  // -1 marks an id outside the pool, -2 a page past the block's range.
   auto load_ids = [&](int batch, int (&ids)[PPI]) {
     const int it = 32 * batch + lane;
 #pragma unroll
@@ -658,50 +656,46 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   load_ids(0, ids_cur);
   load_ids(1, ids_nxt);
 
-  // ---- producer lane: barriers, then the first S groups' copies, before anything else
+  // ---- copy issue: every lane computes the same (warp-uniform) addresses and only
+  // lane 0's predicate is set, so there is no divergent branch.  Bit (i & 31) of
+  // `badmask` records whether iteration i met an invalid page id.
   uint64_t pol = 0;
-  auto issue = [&](int i, const int (&pid)[PPI]) {
-    uint8_t* dst = my_stages + (i % S) * Lo::stageBytes;
-    uint64_t* bar = &my_bars[i % S];
+  uint32_t badmask = 0;
+  const bool leader = lane == 0;
+  auto issue = [&](int i, int stage) {
+    uint8_t* dst = my_stages + stage * Lo::stageBytes;
+    uint64_t* bar = &my_bars[stage];
+    int pid[PPI];
     int bad = 0, bytes = 0;
 #pragma unroll
     for (int q = 0; q < PPI; ++q) {
+      pid[q] = __shfl_sync(0xffffffffu, ids_cur[q], i & 31);
       bad |= pid[q] == -1;
       bytes += pid[q] >= 0 ? Lo::pageBytes : 0;
     }
-    my_bad[i % S] = bad;
-    mbar_arrive_expect_tx(bar, bytes);
+    badmask = (badmask & ~(1u << (i & 31))) | (static_cast<uint32_t>(bad) << (i & 31));
+    mbar_arrive_expect_tx_if(leader, bar, bytes);
 #pragma unroll
     for (int q = 0; q < PPI; ++q) {
-      if (pid[q] < 0) continue;
-      const size_t blk = static_cast<size_t>(pid[q]) * p.Hkv + g;
+      const bool go = leader && pid[q] >= 0;
+      const size_t blk = static_cast<size_t>(pid[q] >= 0 ? pid[q] : 0) * p.Hkv + g;
       uint8_t* d = dst + q * Lo::pageBytes;
-      bulk_g2s(d, p.k + blk * Lo::kBytes, Lo::kBytes, bar, pol);
-      bulk_g2s(d + Lo::kBytes, p.v + blk * Lo::vBytes, Lo::vBytes, bar, pol);
+      bulk_g2s_if(go, d, p.k + blk * Lo::kBytes, Lo::kBytes, bar, pol);
+      bulk_g2s_if(go, d + Lo::kBytes, p.v + blk * Lo::vBytes, Lo::vBytes, bar, pol);
       if constexpr (KVT == kINT8) {
-        bulk_g2s(d + 2 * Lo::kBytes, p.ks + blk * kPage, Lo::sBytes, bar, pol);
-        bulk_g2s(d + 2 * Lo::kBytes + Lo::sBytes, p.vs + blk * kPage, Lo::sBytes, bar, pol);
+        bulk_g2s_if(go, d + 2 * Lo::kBytes, p.ks + blk * kPage, Lo::sBytes, bar, pol);
+        bulk_g2s_if(go, d + 2 * Lo::kBytes + Lo::sBytes, p.vs + blk * kPage, Lo::sBytes, bar, pol);
       }
     }
   };
-  // ids of iteration i (warp-collective); i is at most one batch ahead of `cur`
-  auto ids_of = [&](int i, int cur_batch, int (&pid)[PPI]) {
-    const bool in_cur = (i >> 5) == cur_batch;
-#pragma unroll
-    for (int q = 0; q < PPI; ++q)
-      pid[q] = __shfl_sync(0xffffffffu, in_cur ? ids_cur[q] : ids_nxt[q], i & 31);
-  };
   if (n_my > 0) {
-    if (lane == 0) {
+    if (leader) {
       for (int i = 0; i < S; ++i) mbar_init(&my_bars[i], 1);
       fence_barrier_init();
-      pol = l2_evict_first_policy();
     }
-    for (int i = 0; i < min(S, n_my); ++i) {
-      int pid[PPI];
-      ids_of(i, 0, pid);
-      if (lane == 0) issue(i, pid);
-    }
+    pol = l2_evict_first_policy();
+    __syncwarp();
+    for (int i = 0; i < min(S, n_my); ++i) issue(i, i);
   }
 
   typename WarpOf<KVT, D>::type st;
@@ -709,15 +703,16 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   __syncwarp();
 
   int werr = 0;
-  int i = 0;
+  int i = 0, stage = 0;
+  uint32_t phase = 0;
   for (; i < n_my; ++i) {
-    const bool ok = mbar_wait(&my_bars[i % S], (i / S) & 1);
+    const bool ok = mbar_wait(&my_bars[stage], phase);
     if (!__all_sync(0xffffffffu, ok)) {
       werr |= 0x10;  // PKV_DEV_TIMEOUT
       break;
     }
-    const uint8_t* sp = my_stages + (i % S) * Lo::stageBytes;
-    if (my_bad[i % S]) {
+    const uint8_t* sp = my_stages + stage * Lo::stageBytes;
+    if ((badmask >> (i & 31)) & 1u) {
       werr |= 0x1;  // PKV_DEV_BAD_PAGE
     } else {
       const int j0 = pb + (w + i * kW) * PPI;
@@ -740,22 +735,30 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
         st.pages(sp, valid, lane);
       }
     }
-    if (i + S < n_my) {
-      if (((i + S) & 31) == 0 && i + S >= 32) {
-        // the issue index enters a new batch: it becomes the current one, prefetch the next
+    const int nxt = i + S;
+    if (nxt < n_my) {
+      if ((nxt & 31) == 0) {
+        // the issue index enters a new batch of ids: it becomes the current one
 #pragma unroll
         for (int q = 0; q < PPI; ++q) ids_cur[q] = ids_nxt[q];
-        load_ids(((i + S) >> 5) + 1, ids_nxt);
+        load_ids((nxt >> 5) + 1, ids_nxt);
       }
-      int pid[PPI];
-      ids_of(i + S, (i + S) >> 5, pid);
       __syncwarp();
-      if (lane == 0) issue(i + S, pid);
+      issue(nxt, stage);
+    }
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
   if (werr & 0x10) {
     // Drain (bounded) whatever this warp still has in flight before leaving.
-    for (int k = i + 1; k < min(n_my, i + S); ++k) (void)mbar_wait(&my_bars[k % S], (k / S) & 1);
+    int s2 = stage;
+    uint32_t ph2 = phase;
+    for (int k = i; k < min(n_my, i + S); ++k) {
+      if (k > i) (void)mbar_wait(&my_bars[s2], ph2);
+      if (++s2 == S) { s2 = 0; ph2 ^= 1u; }
+    }
   }
   if (werr && lane == 0) atomicOr(&s_flag, werr);
 
@@ -805,35 +808,36 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // The merge reads every split's (max, sum) once into shared memory, turns them into
-  // weights, then accumulates the partial outputs with independent loads.
+  // The merge: warp w handles heads w and w + 4; its lanes stride over the splits, so
+  // the max and the weighted sum are shuffle reductions and every load is independent.
+  // The weights go to shared memory, then all threads accumulate the partial outputs.
   {
     float* wts = reinterpret_cast<float*>(stages);  // [nsplit][8] weights, then [8] 1/L
     const size_t stride = static_cast<size_t>(p.B) * p.Hq;
     const size_t row0 = static_cast<size_t>(b) * p.Hq + h0;
     __syncthreads();
-    for (int idx = tid; idx < nsplit * nh; idx += kThreads) {
-      const int s = idx / nh, r = idx % nh;
-      wts[s * kMaxHeads + r] = __ldcg(p.ws_m + s * stride + row0 + r);
-    }
-    __syncthreads();
-    if (tid < nh) {
-      const int r = tid;
+    for (int r = w; r < nh; r += kW) {
       float M = -CUDART_INF_F;
       bool poisoned = false;
-      for (int s = 0; s < nsplit; ++s) {
-        const float ms = wts[s * kMaxHeads + r];
+      for (int s = lane; s < nsplit; s += 32) {
+        const float ms = __ldcg(p.ws_m + s * stride + row0 + r);
         poisoned |= isnan(ms);
         M = fmaxf(M, ms);
+        wts[s * kMaxHeads + r] = ms;
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      poisoned = __any_sync(0xffffffffu, poisoned);
       float Ls = 0.f;
-      for (int s = 0; s < nsplit; ++s) {
+      for (int s = lane; s < nsplit; s += 32) {
         const float ms = wts[s * kMaxHeads + r];
         const float f = ms == -CUDART_INF_F ? 0.f : fast_exp2(ms - M);
         wts[s * kMaxHeads + r] = f;
         Ls += __ldcg(p.ws_l + s * stride + row0 + r) * f;
       }
-      wts[nsplit * kMaxHeads + r] = poisoned ? CUDART_NAN_F : (Ls > 0.f ? 1.f / Ls : 0.f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      if (lane == 0) wts[nsplit * kMaxHeads + r] = poisoned ? CUDART_NAN_F : (Ls > 0.f ? 1.f / Ls : 0.f);
     }
     __syncthreads();
     for (int idx = tid; idx < nh * D; idx += kThreads) {
@@ -936,16 +940,20 @@ bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int dev
   if (chunk_override > 0) {
     chunk = chunk_override;
   } else {
-    // Blocks resident at once: split only as far as needed to fill them with every
-    // sequence at the table's full length, and never below 8 pages per warp, so that
-    // the partial merges stay a small fraction of the streamed bytes.
+    // When the (sequence, head group) units alone nearly fill the resident block slots,
+    // do not split: merges cost more than the last partial wave.  Otherwise aim for
+    // about two blocks per slot at full table length, with at least 8 pages per warp and
+    // at most 32 splits, so that the partial merge stays short.
     const long long units = static_cast<long long>(B) * c.Hkv * plan->head_groups;
     const long long slots = static_cast<long long>(sms) * occ;
-    long long splits = units > 0 ? slots / units : 1;
-    const int min_chunk = 8 * kW * v.ppi;
-    const long long max_splits = (mb + min_chunk - 1) / min_chunk;
-    if (splits > max_splits) splits = max_splits;
-    if (splits < 1) splits = 1;
+    long long splits = 1;
+    if (units > 0 && 4 * units < 3 * slots) {
+      splits = (2 * slots + units - 1) / units;
+      const long long by_len = mb / (8 * kW * v.ppi);
+      if (splits > by_len) splits = by_len;
+      if (splits > 32) splits = 32;
+      if (splits < 1) splits = 1;
+    }
     chunk = static_cast<int>((mb + splits - 1) / splits);
   }
   if (chunk < 1) chunk = 1;
