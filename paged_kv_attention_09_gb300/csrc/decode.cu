@@ -24,13 +24,13 @@
 //             form the A rows: the BF16 high part in rows 0-7, the rounding remainder in
 //             rows 8-15, so FP32 queries keep ~16 bits; the probabilities use the same
 //             hi/lo split for P.V.
-//   INT8 KV — q.k on the s8 tensor-core MMA (m16n8k32): the query row is quantised as
-//             hi + lo/254 (two int8 codes per element, rows 0-7 and 8-15), so the cached
-//             codes feed the MMA without conversion; per-token K scales multiply the
-//             scores in FP32.  P.V on f16 MMA: codes become the exact f16 values
-//             1152 + code with two byte permutes, the probabilities (times the V scales)
-//             are split hi/lo in f16, and the 1152 * sum(P) bias is removed once at the
-//             end.
+//   INT8 KV — f16 MMA for both products.  Codes become the exact f16 values 1152 + code
+//             with one xor and two byte permutes (no subtraction); the bias is removed
+//             afterwards: 1152 * sum(q) from each score, 1152 * sum(P) from the output.
+//             Queries are scaled by a power of two into [0.5, 1) and split hi/lo in f16
+//             (rows 0-7 / 8-15); per-token K scales multiply the scores and V scales the
+//             probabilities (split hi/lo) in FP32.  (The s8 MMA path is far slower on
+//             this part.)
 // The order of every floating-point reduction depends only on logical token positions,
 // the split size and the warp count, so results are bit-identical under any physical
 // page permutation.
@@ -115,9 +115,11 @@ struct Smem {
   static constexpr int combine = (2 * kW * kMaxHeads + kW * kMaxHeads * (D + 2)) * 4;
   static constexpr int big = stages > combine ? stages : combine;
   static constexpr int probs = KVT == kF32 ? kW * kMaxHeads * kPage * 4 : 0;
-  static constexpr int flags = kW * Lo::S * 4;
+  // INT8: the query fragments (one uint4 per k-step and lane) and per-row constants,
+  // built once by warp 0 and read by every warp
+  static constexpr int aux = KVT == kINT8 ? (D / 16) * 32 * 16 + 2 * kMaxHeads * 4 : 0;
   static constexpr int bars = kW * Lo::S * 8;
-  static constexpr int total = big + probs + flags + bars;
+  static constexpr int total = big + probs + aux + bars;
 };
 
 __device__ __forceinline__ float4 load_q4(const void* q, int q_dtype, size_t i) {
@@ -147,16 +149,6 @@ __device__ __forceinline__ void split_b2(float a, float b, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// D(16x8,s32) += A(16x32,s8, row) * B(32x8,s8, col).
-__device__ __forceinline__ void mma_s8(int (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                       uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // Four int8 codes (a 32-bit word) -> two f16x2 words holding 1152 + code exactly:
 // byte b (biased by ^0x80) becomes the low byte of the f16 0x64XX = 1024 + (b ^ 0x80).
 __device__ __forceinline__ void s8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -181,7 +173,8 @@ struct F32Warp {
   float m[HM], l[HM];
   float o[HM][NC];
 
-  __device__ void init(const DParams& p, int b, int h0, int nh, int lane) {
+  __device__ void finish(const uint8_t*, int) {}
+  __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t*, int) {
     const int c8 = lane & 7;
 #pragma unroll
     for (int h = 0; h < HM; ++h) {
@@ -310,7 +303,8 @@ struct Bf16Warp {
   float o[NT][4];
   float m, l, row_scale;
 
-  __device__ void init(const DParams& p, int b, int h0, int nh, int lane) {
+  __device__ void finish(const uint8_t*, int) {}
+  __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t*, int) {
     const int r = lane >> 2, c = lane & 3;
     const bool has = r < nh;
 #pragma unroll
@@ -414,62 +408,74 @@ struct Bf16Warp {
 
 template <int D>
 struct Int8Warp {
-  static constexpr int KB = D / 64;  // 64-column blocks of head_dim
+  static constexpr int KS = D / 16;  // k-steps of the q.k product
   static constexpr int NT = D / 8;   // n-tiles of the P.V product
   static constexpr int PPI = Tune<kINT8, D>::PPI;  // pages per iteration
-  uint32_t qa[2 * KB][4];            // s8 A fragments: [k-step][a0..a3]
+  const uint4* qs;                   // [k-step][lane] f16 A fragments in shared memory
   float o[NT][4];
-  float m, l, sp, row_scale;
+  float m, l, sp, row_scale, kbias;
 
-  __device__ void init(const DParams& p, int b, int h0, int nh, int lane) {
-    const int r = lane >> 2, c = lane & 3;
-    const bool has = r < nh;
-    // lane (r, c) needs q[r][64 blk + 16c .. +15]; k-step 2 blk + h covers head_dim
-    // 64 blk + 16c + 8h + {0..3} (k-slots 4c..4c+3) and {4..7} (k-slots 16+4c..).
-    float qv[KB][16];
-    float qmax = 0.f;
+  // k-slot pair {2c, 2c+1} of k-step ks <-> head_dim 64(ks/4) + 16c + 4(ks%4): each lane's
+  // K operand is then one contiguous 16-byte shared-memory load per n-tile.
+  __device__ static int kslot_d(int ks, int c) { return 64 * (ks >> 2) + 16 * c + 4 * (ks & 3); }
+
+  // Warp 0 builds the fragments and the per-row constants; the caller synchronises the
+  // block before any warp reads them (finish()).
+  __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t* aux, int w) {
+    uint4* frag = reinterpret_cast<uint4*>(aux);
+    float* rowc = reinterpret_cast<float*>(aux + KS * 32 * 16);
+    qs = frag;
+    if (w == 0) {
+      const int r = lane >> 2, c = lane & 3;
+      const bool has = r < nh;
+      float4 qv[KS];
+      float qmax = 0.f;
 #pragma unroll
-    for (int blk = 0; blk < KB; ++blk)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 v = has ? load_q4(p.q, p.q_dtype,
-                                       (static_cast<size_t>(b) * p.Hq + h0 + r) * D + 64 * blk +
-                                           16 * c + 4 * i)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        qv[blk][4 * i + 0] = v.x; qv[blk][4 * i + 1] = v.y;
-        qv[blk][4 * i + 2] = v.z; qv[blk][4 * i + 3] = v.w;
-        qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+      for (int ks = 0; ks < KS; ++ks) {
+        qv[ks] = has ? load_q4(p.q, p.q_dtype, (static_cast<size_t>(b) * p.Hq + h0 + r) * D + kslot_d(ks, c))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(qv[ks].x), fabsf(qv[ks].y)),
+                                 fmaxf(fabsf(qv[ks].z), fabsf(qv[ks].w))));
       }
-    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
-    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
-    // q ~= (qmax / 127) * (hi + lo / 254), hi and lo int8 codes
-    const float inv = qmax > 0.f ? 127.f / qmax : 0.f;
+      qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+      qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+      // f16 operands: bring the row's largest |q| into [0.5, 1) by an exact power of two
+      // and fold the factor into the score scale; hi + lo keeps ~22 bits.
+      int e = 0;
+      if (qmax > 0.f) frexpf(qmax, &e);
+      float qsum = 0.f;  // sum of the operand values exactly as the MMA sees them
 #pragma unroll
-    for (int blk = 0; blk < KB; ++blk)
+      for (int ks = 0; ks < KS; ++ks) {
+        const float x[4] = {ldexpf(qv[ks].x, -e), ldexpf(qv[ks].y, -e), ldexpf(qv[ks].z, -e),
+                            ldexpf(qv[ks].w, -e)};
+        uint4 f;
+        split_h2(x[0], x[1], f.x, f.y);
+        split_h2(x[2], x[3], f.z, f.w);
+        frag[ks * 32 + lane] = f;
+        const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float t = qv[blk][8 * h + e] * inv;
-          const float hi = rintf(t);
-          const float lo = rintf((t - hi) * 254.f);
-          const uint32_t hb = static_cast<uint32_t>(static_cast<int>(hi)) & 0xffu;
-          const uint32_t lb = static_cast<uint32_t>(static_cast<int>(lo)) & 0xffu;
-          hw[e >> 2] |= hb << (8 * (e & 3));
-          lw[e >> 2] |= lb << (8 * (e & 3));
+        for (int h = 0; h < 4; ++h) {
+          const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&fw[h]));
+          qsum += v.x + v.y;
         }
-        qa[2 * blk + h][0] = hw[0];  // row r,   k-slots 4c..4c+3
-        qa[2 * blk + h][1] = lw[0];  // row r+8
-        qa[2 * blk + h][2] = hw[1];  // row r,   k-slots 16+4c..
-        qa[2 * blk + h][3] = lw[1];  // row r+8
       }
-    row_scale = p.scale_log2 * (qmax * (1.f / 127.f));
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+      if (c == 0) {
+        rowc[r] = ldexpf(p.scale_log2, e);
+        rowc[kMaxHeads + r] = 1152.f * qsum;  // K entered the MMA as 1152 + code
+      }
+    }
     m = -CUDART_INF_F;
     l = 0.f;
     sp = 0.f;
 #pragma unroll
     for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  }
+  __device__ void finish(const uint8_t* aux, int lane) {
+    const float* rowc = reinterpret_cast<const float*>(aux + KS * 32 * 16);
+    row_scale = rowc[lane >> 2];
+    kbias = rowc[kMaxHeads + (lane >> 2)];
   }
 
   // PPI consecutive pages at st + pg * pageBytes; valid[pg] tokens each (a page with
@@ -486,26 +492,33 @@ struct Int8Warp {
       const float4 v4 = *reinterpret_cast<const float4*>(Ks + 2 * Lo::kBytes + Lo::sBytes + c * 16);
       ksc[pg][0] = k4.x; ksc[pg][1] = k4.y; ksc[pg][2] = k4.z; ksc[pg][3] = k4.w;
       vsc[pg][0] = v4.x; vsc[pg][1] = v4.y; vsc[pg][2] = v4.z; vsc[pg][3] = v4.w;
-      int sacc[2][4];
+      // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
+      // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3.
+      float sacc[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0;
+        sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
         const int tok = 4 * (r >> 1) + (r & 1) + 2 * j;
         const uint8_t* krow = Ks + tok * D;
 #pragma unroll
-        for (int blk = 0; blk < KB; ++blk) {
+        for (int blk = 0; blk < D / 64; ++blk) {
           const uint4 w = *reinterpret_cast<const uint4*>(krow + blk * 64 + c * 16);
-          mma_s8(sacc[j], qa[2 * blk + 0], w.x, w.y);
-          mma_s8(sacc[j], qa[2 * blk + 1], w.z, w.w);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            uint32_t b0, b1;
+            s8x4_to_f16x4_biased(ws[s], b0, b1);
+            const uint4 f = qs[(4 * blk + s) * 32 + lane];
+            const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+            mma_f16(sacc[j], a, b0, b1);
+          }
         }
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e)
-          x[pg][2 * j + e] =
-              fmaf(static_cast<float>(sacc[j][2 + e]), 1.f / 254.f, static_cast<float>(sacc[j][e])) *
-              (row_scale * ksc[pg][2 * j + e]);
+          x[pg][2 * j + e] = ((sacc[j][e] + sacc[j][2 + e]) - kbias) * (row_scale * ksc[pg][2 * j + e]);
     }
     bool partial = false;
 #pragma unroll
@@ -611,7 +624,8 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   float* probs_all = reinterpret_cast<float*>(smem + Sm::big);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::big + Sm::probs + Sm::flags);
+  uint8_t* aux = smem + Sm::big + Sm::probs;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::big + Sm::probs + Sm::aux);
   __shared__ int s_flag, s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -699,7 +713,9 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   }
 
   typename WarpOf<KVT, D>::type st;
-  st.init(p, b, h0, nh, lane);
+  st.init(p, b, h0, nh, lane, aux, w);
+  if constexpr (KVT == kINT8) __syncthreads();  // warp 0 built the shared query fragments
+  st.finish(aux, lane);
   __syncwarp();
 
   int werr = 0;
