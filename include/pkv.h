@@ -34,9 +34,15 @@
  *   - There is no fallback: an unsupported combination returns PKV_ERR_UNSUPPORTED.
  *   - Only page_size 16 and head_dim 64 or 128 are supported.
  *
- * Cache layout (struct pkv_cache)
- *   k_cache  [num_pages][num_kv_heads][page_size][head_dim]   row per token
- *   v_cache  [num_pages][num_kv_heads][head_dim][page_size]   each page block transposed
+ * Cache layout (struct pkv_cache).  Each (page, kv head) pair owns one K block and one
+ * V block of page_size * head_dim elements; block (page, h) starts at element
+ * (page * num_kv_heads + h) * page_size * head_dim of k_cache / v_cache.
+ *   FP32, INT8:  K element (token t, column d) at t * head_dim + d        (row per token)
+ *                V element (token t, column d) at d * page_size + t       (transposed)
+ *   BF16 (tensor-core tiles: 8 x 8 core matrices of 64 contiguous elements, so a block
+ *         is directly an MMA operand tile):
+ *                K element (t, d) at ((t/8) * (head_dim/8) + d/8) * 64 + (t%8) * 8 + d%8
+ *                V element (t, d) at ((d/8) * 2 + t/8) * 64 + (d%8) * 8 + t%8
  *   k_scale, v_scale  float32 [num_pages][num_kv_heads][page_size]   INT8 only
  *   Token t of a sequence lives in page block_tables[b][t / page_size] at offset
  *   t % page_size; its slot number is page * page_size + offset.

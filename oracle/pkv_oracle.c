@@ -22,11 +22,15 @@
  * values as stored (FP32 as is, BF16 widened exactly, INT8 as code * scale in double).
  *
  * Physical layout (the library's documented layout, restated here from its
- * specification and not from its code):
- *   K cache  [num_pages][Hkv][P][D]           element (page,h,off,d)
- *   V cache  [num_pages][Hkv][D][P]           (each page's V block is transposed)
- *   scales   [num_pages][Hkv][P]  float32     (INT8 only; one per token and kv head)
- *   slot = page * P + off
+ * specification and not from its code).  Each (page, kv head) pair owns one K block and
+ * one V block of 16*D elements; block (page, h) starts at element (page*Hkv + h)*16*D.
+ *   FP32 / INT8:  K block [16 tokens][D]     element (t, d) at t*D + d
+ *                 V block [D][16 tokens]     element (d, t) at d*16 + t
+ *   BF16 (tensor-core tiles of 8x8 "core matrices", each 64 contiguous elements):
+ *                 K element (t, d) at ((t/8)*(D/8) + d/8)*64 + (t%8)*8 + d%8
+ *                 V element (d, t) at ((d/8)*2  + t/8)*64 + (d%8)*8 + t%8
+ *   scales   [num_pages][Hkv][16]  float32     (INT8 only; one per token and kv head)
+ *   slot = page * 16 + offset
  *
  * The INT8 quantiser and the BF16 rounding run in C `float` exactly as specified
  * (IEEE division, round-half-to-even), compiled with -ffp-contract=off and without
@@ -115,14 +119,21 @@ void oracle_quantize_row_int8(const float* x, int n, int8_t* codes, float* scale
 
 /* ---------------------------------------------------------------- cache addressing */
 
-static size_t k_index(int page, int h, int off, int d, int Hkv, int P, int D) {
-  return (((size_t)page * Hkv + h) * P + off) * D + d;
+static size_t k_index(int kv_dtype, int page, int h, int off, int d, int Hkv, int P, int D) {
+  size_t blk = ((size_t)page * Hkv + h) * (size_t)P * D;
+  if (kv_dtype == ODT_BF16)
+    return blk + ((size_t)(off / 8) * (D / 8) + d / 8) * 64 + (off % 8) * 8 + d % 8;
+  return blk + (size_t)off * D + d;
 }
-static size_t v_index(int page, int h, int off, int d, int Hkv, int P, int D) {
+static size_t v_index(int kv_dtype, int page, int h, int off, int d, int Hkv, int P, int D) {
+  size_t blk = ((size_t)page * Hkv + h) * (size_t)P * D;
 #if ORACLE_MUTANT == 3 /* V block not transposed */
-  return (((size_t)page * Hkv + h) * P + off) * D + d;
+  (void)kv_dtype;
+  return blk + (size_t)off * D + d;
 #else
-  return (((size_t)page * Hkv + h) * D + d) * P + off;
+  if (kv_dtype == ODT_BF16)
+    return blk + ((size_t)(d / 8) * (P / 8) + off / 8) * 64 + (d % 8) * 8 + off % 8;
+  return blk + (size_t)d * P + off;
 #endif
 }
 static size_t s_index(int page, int h, int off, int Hkv, int P) {
@@ -132,7 +143,8 @@ static size_t s_index(int page, int h, int off, int Hkv, int P) {
 /* Stored K or V element as a double (after dequantisation). */
 static double cache_value(const void* cache, const float* scales, int kv_dtype, int is_v,
                           int page, int h, int off, int d, int Hkv, int P, int D) {
-  size_t i = is_v ? v_index(page, h, off, d, Hkv, P, D) : k_index(page, h, off, d, Hkv, P, D);
+  size_t i = is_v ? v_index(kv_dtype, page, h, off, d, Hkv, P, D)
+                  : k_index(kv_dtype, page, h, off, d, Hkv, P, D);
   if (kv_dtype == ODT_INT8) {
     int8_t c = ((const int8_t*)cache)[i];
     return (double)c * (double)scales[s_index(page, h, off, Hkv, P)];
@@ -171,13 +183,15 @@ int oracle_append(int kv_dtype, int num_pages, int P, int Hkv, int D, void* k_ca
           float s;
           oracle_quantize_row_int8(row, D, codes, &s);
           for (int d = 0; d < D; ++d) {
-            size_t j = is_v ? v_index(page, h, off, d, Hkv, P, D) : k_index(page, h, off, d, Hkv, P, D);
+            size_t j = is_v ? v_index(kv_dtype, page, h, off, d, Hkv, P, D)
+                            : k_index(kv_dtype, page, h, off, d, Hkv, P, D);
             ((int8_t*)dst)[j] = codes[d];
           }
           (is_v ? v_scale : k_scale)[s_index(page, h, off, Hkv, P)] = s;
         } else {
           for (int d = 0; d < D; ++d) {
-            size_t j = is_v ? v_index(page, h, off, d, Hkv, P, D) : k_index(page, h, off, d, Hkv, P, D);
+            size_t j = is_v ? v_index(kv_dtype, page, h, off, d, Hkv, P, D)
+                            : k_index(kv_dtype, page, h, off, d, Hkv, P, D);
             if (kv_dtype == ODT_BF16) ((uint16_t*)dst)[j] = oracle_f32_to_bf16(row[d]);
             else ((float*)dst)[j] = row[d];
           }

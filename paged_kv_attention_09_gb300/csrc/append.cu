@@ -79,12 +79,14 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
       if (lane == 0) (which ? v_scale : k_scale)[blk * kPage + off] = s;
     } else if constexpr (KV_DT == kBF16) {
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? v_cache : k_cache);
+      // tensor-core tile order inside the block (see bf16_k_off / bf16_v_off)
+      uint8_t* blkp = static_cast<uint8_t*>(which ? v_cache : k_cache) + blk * kPage * D * 2;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const __nv_bfloat16 b = __float2bfloat16_rn(x[e]);
-        if (which == 0) dst[k_row + lane * E + e] = b;
-        else dst[v_base + static_cast<size_t>(lane * E + e) * kPage] = b;
+        const int d = lane * E + e;
+        const int off_b = which == 0 ? bf16_k_off(off, d, D) : bf16_v_off(d, off);
+        *reinterpret_cast<__nv_bfloat16*>(blkp + off_b) = b;
       }
     } else {
       float* dst = static_cast<float*>(which ? v_cache : k_cache);

@@ -307,15 +307,19 @@ struct Bf16Warp {
   __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t*, int) {
     const int r = lane >> 2, c = lane & 3;
     const bool has = r < nh;
+    const size_t row = (static_cast<size_t>(b) * p.Hq + h0 + r) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      // k-slot pair {2c, 2c+1} of k-step ks <-> head_dim 32(ks/2) + 8c + 4(ks%2): each
-      // lane's K operand is then one contiguous 16-byte shared-memory load.
-      const int d0 = 32 * (ks >> 1) + 8 * c + 4 * (ks & 1);
-      const float4 v = has ? load_q4(p.q, p.q_dtype, (static_cast<size_t>(b) * p.Hq + h0 + r) * D + d0)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-      split_b2(v.x, v.y, qa[ks][0], qa[ks][1]);
-      split_b2(v.z, v.w, qa[ks][2], qa[ks][3]);
+      // standard fragment order: k-slots {2c, 2c+1} and {2c+8, 2c+9} of k-step ks
+      float2 lo2 = make_float2(0.f, 0.f), hi2 = make_float2(0.f, 0.f);
+      if (has) {
+        const float4 a = load_q4(p.q, p.q_dtype, row + 16 * ks + (2 * c & ~3));
+        const float4 e = load_q4(p.q, p.q_dtype, row + 16 * ks + 8 + (2 * c & ~3));
+        lo2 = (c & 1) ? make_float2(a.z, a.w) : make_float2(a.x, a.y);
+        hi2 = (c & 1) ? make_float2(e.z, e.w) : make_float2(e.x, e.y);
+      }
+      split_b2(lo2.x, lo2.y, qa[ks][0], qa[ks][1]);
+      split_b2(hi2.x, hi2.y, qa[ks][2], qa[ks][3]);
     }
     row_scale = p.scale_log2;
     m = -CUDART_INF_F;
@@ -324,26 +328,26 @@ struct Bf16Warp {
     for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   }
 
+  // One page.  K and V arrive as tensor-core tiles, so ldmatrix builds every B fragment
+  // from whole 16-byte core-matrix rows without bank conflicts.  n-tile j holds tokens
+  // 8j .. 8j+7; lane (r, c) ends up with tokens 2c, 2c+1, 8+2c, 9+2c.
   __device__ void page(const uint8_t* st, int valid, int lane) {
     using Lo = Layout<kBF16, D>;
-    const int r = lane >> 2, c = lane & 3;
-    const uint8_t* Ks = st;
-    const uint8_t* Vs = st + Lo::kBytes;
-    // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
-    // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3.
-    // two accumulator chains per n-tile (even / odd k-steps) halve the MMA latency chain
+    const int c = lane & 3;
+    const uint32_t Ks = smem_u32(st);
+    const uint32_t Vs = Ks + Lo::kBytes;
     float sacc[2][2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) sacc[j][h][0] = sacc[j][h][1] = sacc[j][h][2] = sacc[j][h][3] = 0.f;
-      const int tok = 4 * (r >> 1) + (r & 1) + 2 * j;
-      const uint8_t* krow = Ks + tok * D * 2;
 #pragma unroll
-      for (int blk = 0; blk < D / 32; ++blk) {
-        const uint4 w = *reinterpret_cast<const uint4*>(krow + (blk * 32 + c * 8) * 2);
-        mma_bf16(sacc[j][0], qa[2 * blk + 0], w.x, w.y);
-        mma_bf16(sacc[j][1], qa[2 * blk + 1], w.z, w.w);
+      for (int s = 0; s < KS / 2; ++s) {
+        // matrices: chunks 4s .. 4s+3 of key group j -> b0/b1 of k-steps 2s and 2s+1
+        uint32_t f[4];
+        ldsm_x4(f, Ks + ((j * (D / 8) + 4 * s + (lane >> 3)) << 7) + ((lane & 7) << 4));
+        mma_bf16(sacc[j][0], qa[2 * s + 0], f[0], f[1]);
+        mma_bf16(sacc[j][1], qa[2 * s + 1], f[2], f[3]);
       }
     }
     float x[4];
@@ -356,9 +360,9 @@ struct Bf16Warp {
     uint32_t vmask0 = 0xffffffffu, vmask1 = 0xffffffffu;
     if (valid < kPage) {  // padding tokens may hold NaN: mask scores, zero their V entries
 #pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = (4 * c + i) < valid ? x[i] : -CUDART_INF_F;
-      vmask0 = (4 * c + 0 < valid ? 0x0000ffffu : 0u) | (4 * c + 1 < valid ? 0xffff0000u : 0u);
-      vmask1 = (4 * c + 2 < valid ? 0x0000ffffu : 0u) | (4 * c + 3 < valid ? 0xffff0000u : 0u);
+      for (int i = 0; i < 4; ++i) x[i] = (8 * (i >> 1) + 2 * c + (i & 1)) < valid ? x[i] : -CUDART_INF_F;
+      vmask0 = (2 * c + 0 < valid ? 0x0000ffffu : 0u) | (2 * c + 1 < valid ? 0xffff0000u : 0u);
+      vmask1 = (2 * c + 8 < valid ? 0x0000ffffu : 0u) | (2 * c + 9 < valid ? 0xffff0000u : 0u);
     }
     float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -380,10 +384,12 @@ struct Bf16Warp {
     split_b2(pr[0], pr[1], pa[0], pa[1]);
     split_b2(pr[2], pr[3], pa[2], pa[3]);
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int d = 8 * j + r;
-      const uint2 w = *reinterpret_cast<const uint2*>(Vs + (d * kPage + 4 * c) * 2);
-      mma_bf16(o[j], pa, w.x & vmask0, w.y & vmask1);
+    for (int j = 0; j < NT; j += 2) {
+      // matrices: (d-group j, tokens 0-7), (j, 8-15), (j+1, 0-7), (j+1, 8-15): contiguous
+      uint32_t f[4];
+      ldsm_x4(f, Vs + (j << 8) + (lane << 4));
+      mma_bf16(o[j], pa, f[0] & vmask0, f[1] & vmask1);
+      mma_bf16(o[j + 1], pa, f[2] & vmask0, f[3] & vmask1);
     }
   }
 

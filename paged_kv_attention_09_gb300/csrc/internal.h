@@ -10,6 +10,18 @@ constexpr int kPage = 16;  // tokens per page (the only supported page size)
 
 enum : int { kF32 = 0, kBF16 = 1, kINT8 = 2 };
 
+// BF16 page blocks are stored as tensor-core tiles: 8 x 8 "core matrices" of 16-byte
+// rows, each matrix 128 contiguous bytes, so one bulk copy of a block lands a valid
+// MMA operand tile in shared memory.  Byte offsets inside one (page, kv head) block:
+//   K (token t, column d): core matrix (t/8, d/8), row t%8, element d%8
+//   V (column d, token t): core matrix (d/8, t/8), row d%8, element t%8
+__host__ __device__ constexpr int bf16_k_off(int t, int d, int D) {
+  return (((t >> 3) * (D >> 3) + (d >> 3)) << 7) + ((t & 7) << 4) + ((d & 7) << 1);
+}
+__host__ __device__ constexpr int bf16_v_off(int d, int t) {
+  return ((((d >> 3) << 1) + (t >> 3)) << 7) + ((d & 7) << 4) + ((t & 7) << 1);
+}
+
 struct CacheView {
   const void* k;
   const void* v;

@@ -191,11 +191,11 @@ __global__ void __launch_bounds__(kPThreads)
 #pragma unroll
       for (int nt = 0; nt < 2 * kTilePages; ++nt) {
         sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-        const int key = 16 * (nt >> 1) + 4 * (r >> 1) + (r & 1) + 2 * (nt & 1);
-        const uint8_t* krow = Ks + key * D * 2;
+        const int t = 4 * (r >> 1) + (r & 1) + 2 * (nt & 1);  // token inside page nt/2
+        const uint8_t* kpage = Ks + (nt >> 1) * Sm::kBlk;
 #pragma unroll
         for (int blk = 0; blk < D / 32; ++blk) {
-          const uint4 kw = *reinterpret_cast<const uint4*>(krow + (blk * 32 + c * 8) * 2);
+          const uint4 kw = *reinterpret_cast<const uint4*>(kpage + bf16_k_off(t, blk * 32 + c * 8, D));
 #pragma unroll
           for (int part = 0; part < NQ; ++part) {
             mma_bf16(sacc[nt], qa[part][2 * blk + 0], kw.x, kw.y);
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kPThreads)
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           const int d = 8 * j + r;
-          const uint2 vw = *reinterpret_cast<const uint2*>(vblk + (d * kPage + 4 * c) * 2);
+          const uint2 vw = *reinterpret_cast<const uint2*>(vblk + bf16_v_off(d, 4 * c));
           mma_bf16(o[j], ahi, vw.x & vm0, vw.y & vm1);
           mma_bf16(o[j], alo, vw.x & vm0, vw.y & vm1);
         }

@@ -95,7 +95,9 @@ class KVCache:
     """Device tensors of one paged cache in the library's layout.
 
     k: [num_pages, Hkv, 16, D]; v: [num_pages, Hkv, D, 16] (page blocks transposed);
-    k_scale, v_scale: float32 [num_pages, Hkv, 16] for INT8 caches.
+    k_scale, v_scale: float32 [num_pages, Hkv, 16] for INT8 caches.  For BF16 caches the
+    elements inside each (page, kv head) block are in tensor-core tile order (see
+    include/pkv.h); the tensor shapes are containers of the right size.
     """
 
     def __init__(self, k, v, k_scale=None, v_scale=None):

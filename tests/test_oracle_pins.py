@@ -31,12 +31,30 @@ def bf16_to_f32(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def k_elem(dtype, t, d, D):
+    """Element index of K (token t, column d) inside one (page, kv head) block."""
+    if dtype == BF16:  # tensor-core tiles: 8x8 core matrices of 64 contiguous elements
+        return ((t // 8) * (D // 8) + d // 8) * 64 + (t % 8) * 8 + d % 8
+    return t * D + d
+
+
+def v_elem(dtype, t, d, D):
+    """Element index of V (token t, column d) inside one (page, kv head) block."""
+    if dtype == BF16:
+        return ((d // 8) * (P // 8) + t // 8) * 64 + (d % 8) * 8 + t % 8
+    return d * P + t
+
+
 def logical_kv(cache: HostCache, bt_row, L, g):
     """Reassemble logical K/V [L, D] (float64, dequantised) from the documented layout."""
     t = np.arange(L)
     pages, offs = bt_row[t // P], t % P
-    k = cache.k[pages, g, offs, :]
-    v = cache.v[pages, g, :, offs]  # fancy indices first -> [L, D]
+    D = cache.head_dim
+    dd = np.arange(D)[None, :]
+    kf = cache.k.reshape(cache.num_pages, cache.num_kv_heads, -1)
+    vf = cache.v.reshape(cache.num_pages, cache.num_kv_heads, -1)
+    k = kf[pages[:, None], g, k_elem(cache.kv_dtype, offs[:, None], dd, D)]
+    v = vf[pages[:, None], g, v_elem(cache.kv_dtype, offs[:, None], dd, D)]
     if cache.kv_dtype == BF16:
         k, v = bf16_to_f32(k), bf16_to_f32(v)
     k = k.astype(np.float64)
@@ -204,7 +222,13 @@ def test_append_bf16_and_int8_stored_values():
             codes, s = oracle.quantize_row_int8(wl.v_src[i, h])
             assert np.array_equal(ci.v[pg, h, :, off], codes) and ci.v_scale[pg, h, off] == s
             ref = torch.from_numpy(wl.k_src[i, h]).to(torch.bfloat16).view(torch.int16)
-            assert np.array_equal(cb.k[pg, h, off], ref.numpy().view(np.uint16))
+            idx = k_elem(BF16, off, np.arange(64), 64)
+            assert np.array_equal(cb.k.reshape(wl.num_pages, 2, -1)[pg, h, idx],
+                                  ref.numpy().view(np.uint16))
+            ref = torch.from_numpy(wl.v_src[i, h]).to(torch.bfloat16).view(torch.int16)
+            idx = v_elem(BF16, off, np.arange(64), 64)
+            assert np.array_equal(cb.v.reshape(wl.num_pages, 2, -1)[pg, h, idx],
+                                  ref.numpy().view(np.uint16))
 
 
 # --------------------------------------------------------------------------- dense brute force
