@@ -86,5 +86,8 @@ struct PrefillArgs {
 bool plan_prefill(const CacheView& c, int B, int Hq, int max_q_len, int MB, int q_dtype,
                   int device, PrefillPlan* plan);
 cudaError_t launch_prefill(const PrefillArgs& a, const PrefillPlan& plan, cudaStream_t st);
+// tcgen05 path (BF16 KV): query rows per block, and the launch over n_row_tiles blocks.
+int prefill_tc_rows();
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, cudaStream_t st);
 
 }  // namespace pkv

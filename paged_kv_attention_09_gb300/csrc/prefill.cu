@@ -22,6 +22,11 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+// 1: tcgen05 kernel (prefill_tc.cu); 0: the warp-level MMA kernel below.
+#ifndef PKV_PREFILL_TC
+#define PKV_PREFILL_TC 1
+#endif
+
 namespace pkv {
 namespace {
 
@@ -326,20 +331,34 @@ bool raise_smem_limit(int device, int slot, const void* fn, int smem) {
 
 }  // namespace
 
+cudaError_t launch_prefill_mma(const PrefillArgs& a, const PrefillPlan& plan, cudaStream_t st);
+
 bool plan_prefill(const CacheView& c, int B, int Hq, int max_q_len, int MB, int q_dtype,
                   int device, PrefillPlan* plan) {
   (void)B; (void)MB; (void)device; (void)q_dtype;
   if (c.dtype != kBF16) return false;
   if (c.D != 64 && c.D != 128) return false;
   const int G = Hq / c.Hkv;
+#if PKV_PREFILL_TC
+  plan->rows_per_cta = prefill_tc_rows();
+#else
   plan->rows_per_cta = kRows;
+#endif
   const long long rows = static_cast<long long>(max_q_len) * G;
-  plan->n_row_tiles = static_cast<int>((rows + kRows - 1) / kRows);
+  plan->n_row_tiles = static_cast<int>((rows + plan->rows_per_cta - 1) / plan->rows_per_cta);
   plan->ws_bytes = 0;
   return true;
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const PrefillPlan& plan, cudaStream_t st) {
+#if PKV_PREFILL_TC
+  return launch_prefill_tc(a, plan.n_row_tiles, st);
+#else
+  return launch_prefill_mma(a, plan, st);
+#endif
+}
+
+cudaError_t launch_prefill_mma(const PrefillArgs& a, const PrefillPlan& plan, cudaStream_t st) {
   PParams p{};
   p.k = static_cast<const __nv_bfloat16*>(a.c.k);
   p.v = static_cast<const __nv_bfloat16*>(a.c.v);
