@@ -410,16 +410,18 @@ struct Bf16Warp {
   }
 };
 
-// ------------------------------------------------------------------ INT8 (s8 + f16 MMA)
+// ------------------------------------------------------------------ INT8 (f16 MMA)
 
 template <int D>
 struct Int8Warp {
   static constexpr int KS = D / 16;  // k-steps of the q.k product
-  static constexpr int NT = D / 8;   // n-tiles of the P.V product
+  static constexpr int MT = D / 16;  // m-tiles (16 head-dim rows) of O^T = V^T P^T
   static constexpr int PPI = Tune<kINT8, D>::PPI;  // pages per iteration
-  const uint4* qs;                   // [k-step][lane] f16 A fragments in shared memory
-  float o[NT][4];
-  float m, l, sp, row_scale, kbias;
+  uint32_t qf[KS][4];                // f16 A fragments of the query rows (hi 0-7, lo 8-15)
+  // O^T accumulators: lane (r, c) holds head-dim rows 16 mt + r and 16 mt + r + 8 of
+  // heads 2c and 2c + 1 (the C layout of the transposed product)
+  float o[MT][4];
+  float m, l, sp, row_scale, kbias;  // per query head r = lane / 4
 
   // k-slot pair {2c, 2c+1} of k-step ks <-> head_dim 64(ks/4) + 16c + 4(ks%4): each lane's
   // K operand is then one contiguous 16-byte shared-memory load per n-tile.
@@ -430,7 +432,6 @@ struct Int8Warp {
   __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t* aux, int w) {
     uint4* frag = reinterpret_cast<uint4*>(aux);
     float* rowc = reinterpret_cast<float*>(aux + KS * 32 * 16);
-    qs = frag;
     if (w == 0) {
       const int r = lane >> 2, c = lane & 3;
       const bool has = r < nh;
@@ -476,9 +477,15 @@ struct Int8Warp {
     l = 0.f;
     sp = 0.f;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    for (int j = 0; j < MT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   }
   __device__ void finish(const uint8_t* aux, int lane) {
+    const uint4* frag = reinterpret_cast<const uint4*>(aux);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint4 f = frag[ks * 32 + lane];
+      qf[ks][0] = f.x; qf[ks][1] = f.y; qf[ks][2] = f.z; qf[ks][3] = f.w;
+    }
     const float* rowc = reinterpret_cast<const float*>(aux + KS * 32 * 16);
     row_scale = rowc[lane >> 2];
     kbias = rowc[kMaxHeads + (lane >> 2)];
@@ -499,7 +506,7 @@ struct Int8Warp {
       ksc[pg][0] = k4.x; ksc[pg][1] = k4.y; ksc[pg][2] = k4.z; ksc[pg][3] = k4.w;
       vsc[pg][0] = v4.x; vsc[pg][1] = v4.y; vsc[pg][2] = v4.z; vsc[pg][3] = v4.w;
       // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
-      // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3.
+      // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3 of head r.
       float sacc[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -514,9 +521,7 @@ struct Int8Warp {
           for (int s = 0; s < 4; ++s) {
             uint32_t b0, b1;
             s8x4_to_f16x4_biased(ws[s], b0, b1);
-            const uint4 f = qs[(4 * blk + s) * 32 + lane];
-            const uint32_t a[4] = {f.x, f.y, f.z, f.w};
-            mma_f16(sacc[j], a, b0, b1);
+            mma_f16(sacc[j], qf[4 * blk + s], b0, b1);
           }
         }
       }
@@ -548,38 +553,47 @@ struct Int8Warp {
     const float mn = fmaxf(m, mx);
     const float corr = fast_exp2(m - mn);
     m = mn;
-    float pr[PPI][4], pv[PPI][4];
+    float pv[PPI][4];
     float ls = 0.f, ps = 0.f;
 #pragma unroll
     for (int pg = 0; pg < PPI; ++pg)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        pr[pg][i] = fast_exp2(x[pg][i] - mn);
-        pv[pg][i] = pr[pg][i] * vsc[pg][i];
-        ls += pr[pg][i];
+        const float pr = fast_exp2(x[pg][i] - mn);
+        pv[pg][i] = pr * vsc[pg][i];
+        ls += pr;
         ps += pv[pg][i];
       }
     l = l * corr + ls;
     sp = sp * corr + ps;
     if (__any_sync(0xffffffffu, corr != 1.f)) {
+      // this lane's accumulators belong to heads 2c and 2c + 1
+      const float ca = __shfl_sync(0xffffffffu, corr, 8 * c);
+      const float cb = __shfl_sync(0xffffffffu, corr, 8 * c + 4);
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        o[j][0] *= corr; o[j][1] *= corr; o[j][2] *= corr; o[j][3] *= corr;
+      for (int j = 0; j < MT; ++j) {
+        o[j][0] *= ca; o[j][1] *= cb; o[j][2] *= ca; o[j][3] *= cb;
       }
     }
 #pragma unroll
     for (int pg = 0; pg < PPI; ++pg) {
-      uint32_t pa[4];
-      split_h2(pv[pg][0], pv[pg][1], pa[0], pa[1]);
-      split_h2(pv[pg][2], pv[pg][3], pa[2], pa[3]);
+      // B = P^T (tokens x heads): lane (r, c) holds head r, tokens 4c .. 4c+3, which the
+      // k-slot order {2c, 2c+1 | 2c+8, 2c+9} -> tokens {4c, 4c+1 | 4c+2, 4c+3} makes a
+      // ready-made fragment; the hi and lo parts accumulate into the same C.
+      uint32_t bh[2], bl[2];
+      split_h2(pv[pg][0], pv[pg][1], bh[0], bl[0]);
+      split_h2(pv[pg][2], pv[pg][3], bh[1], bl[1]);
       const uint8_t* Vs = st + pg * Lo::pageBytes + Lo::kBytes;
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const int d = 8 * j + r;
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + d * kPage + 4 * c);
-        uint32_t b0, b1;
-        s8x4_to_f16x4_biased(w, b0, b1);
-        mma_f16(o[j], pa, b0, b1);
+      for (int j = 0; j < MT; ++j) {
+        // A = V^T rows 16 j + r and 16 j + r + 8, tokens 4c .. 4c+3 (same k-slot order)
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r) * kPage + 4 * c);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r + 8) * kPage + 4 * c);
+        uint32_t a[4];
+        s8x4_to_f16x4_biased(w0, a[0], a[2]);
+        s8x4_to_f16x4_biased(w1, a[1], a[3]);
+        mma_f16(o[j], a, bh[0], bh[1]);
+        mma_f16(o[j], a, bl[0], bl[1]);
       }
     }
   }
@@ -595,11 +609,17 @@ struct Int8Warp {
       cm[r] = m;
       cl[r] = lt;
     }
-    const float bias = 1152.f * st;  // V entered the MMA as 1152 + code
+    // V entered the MMA as 1152 + code: remove 1152 * sum(P) of heads 2c and 2c + 1
+    const float ba = 1152.f * __shfl_sync(0xffffffffu, st, 8 * c);
+    const float bb = 1152.f * __shfl_sync(0xffffffffu, st, 8 * c + 4);
+    float* oa = cO + (2 * c) * (D + 2);
+    float* ob = oa + (D + 2);
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      cO[r * (D + 2) + 8 * j + 2 * c + 0] = (o[j][0] + o[j][2]) - bias;
-      cO[r * (D + 2) + 8 * j + 2 * c + 1] = (o[j][1] + o[j][3]) - bias;
+    for (int j = 0; j < MT; ++j) {
+      oa[16 * j + r] = o[j][0] - ba;
+      ob[16 * j + r] = o[j][1] - bb;
+      oa[16 * j + r + 8] = o[j][2] - ba;
+      ob[16 * j + r + 8] = o[j][3] - bb;
     }
   }
 };
@@ -656,64 +676,55 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   const int ngroups = (pe - pb + PPI - 1) / PPI;
   const int n_my = ngroups > w ? (ngroups - w + kW - 1) / kW : 0;
 
-  // ---- page ids: lane l holds those of this warp's iteration 32 k + l (batch k), for
-  // the current and the next batch, so the copies never wait on the block table.
-  // -1 marks an id outside the pool, -2 a page past the block's range.
-  auto load_ids = [&](int batch, int (&ids)[PPI]) {
-    const int it = 32 * batch + lane;
-#pragma unroll
-    for (int q = 0; q < PPI; ++q) {
-      const int j = pb + (w + it * kW) * PPI + q;
-      int id = -2;
-      if (it < n_my && j < pe) {
-        id = bt[j];
-        if (id < 0 || id >= p.num_pages) id = -1;
+  // ---- page ids: lane l holds the id of this warp's page m = 32 k + l (batch k) for the
+  // current and the next batch; the warp's page m is the block's logical page
+  // pb + (w + (m / PPI) kW) PPI + m % PPI.  -2 marks a page past the block's range.  An
+  // id outside the pool is replaced by page 0 (so every copy stays inside the cache) and
+  // flagged: the block's outputs then become NaN.
+  int werr = 0;
+  auto load_ids = [&](int batch) -> int {
+    const int m = 32 * batch + lane;
+    const int it = m / PPI;
+    const int j = pb + (w + it * kW) * PPI + m % PPI;
+    int id = -2;
+    if (it < n_my && j < pe) {
+      id = bt[j];
+      if (id < 0 || id >= p.num_pages) {
+        werr |= 0x1;  // PKV_DEV_BAD_PAGE
+        id = 0;
       }
-      ids[q] = id;
     }
+    return id;
   };
-  int ids_cur[PPI], ids_nxt[PPI];
-  load_ids(0, ids_cur);
-  load_ids(1, ids_nxt);
+  int ids_cur = load_ids(0), ids_nxt = load_ids(1);
 
-  // ---- copy issue: every lane computes the same (warp-uniform) addresses and only
-  // lane 0's predicate is set, so there is no divergent branch.  Bit (i & 31) of
-  // `badmask` records whether iteration i met an invalid page id.
-  uint64_t pol = 0;
-  uint32_t badmask = 0;
-  const bool leader = lane == 0;
+  // ---- copy issue: lane l < NK PPI issues one copy (kind l % NK of page l / NK of the
+  // iteration), so a whole stage costs one warp instruction; lane 0 posts the byte count.
+  constexpr int NK = KVT == kINT8 ? 4 : 2;  // K, V (and the two scale vectors)
+  const int cq = lane / NK, ck = lane % NK;
+  // this lane's copy: size, and destination inside stage 0 (the source is selected per
+  // issue from the kernel parameters, which costs no registers across the loop)
+  const uint32_t c_bytes = ck < 2 ? static_cast<uint32_t>(Lo::kBytes) : static_cast<uint32_t>(Lo::sBytes);
+  const uint32_t c_dst = smem_u32(my_stages) + cq * Lo::pageBytes +
+                         (ck == 0 ? 0 : ck == 1 ? Lo::kBytes : 2 * Lo::kBytes + (ck - 2) * Lo::sBytes);
   auto issue = [&](int i, int stage) {
-    uint8_t* dst = my_stages + stage * Lo::stageBytes;
-    uint64_t* bar = &my_bars[stage];
-    int pid[PPI];
-    int bad = 0, bytes = 0;
-#pragma unroll
-    for (int q = 0; q < PPI; ++q) {
-      pid[q] = __shfl_sync(0xffffffffu, ids_cur[q], i & 31);
-      bad |= pid[q] == -1;
-      bytes += pid[q] >= 0 ? Lo::pageBytes : 0;
-    }
-    badmask = (badmask & ~(1u << (i & 31))) | (static_cast<uint32_t>(bad) << (i & 31));
-    mbar_arrive_expect_tx_if(leader, bar, bytes);
-#pragma unroll
-    for (int q = 0; q < PPI; ++q) {
-      const bool go = leader && pid[q] >= 0;
-      const size_t blk = static_cast<size_t>(pid[q] >= 0 ? pid[q] : 0) * p.Hkv + g;
-      uint8_t* d = dst + q * Lo::pageBytes;
-      bulk_g2s_if(go, d, p.k + blk * Lo::kBytes, Lo::kBytes, bar, pol);
-      bulk_g2s_if(go, d + Lo::kBytes, p.v + blk * Lo::vBytes, Lo::vBytes, bar, pol);
-      if constexpr (KVT == kINT8) {
-        bulk_g2s_if(go, d + 2 * Lo::kBytes, p.ks + blk * kPage, Lo::sBytes, bar, pol);
-        bulk_g2s_if(go, d + 2 * Lo::kBytes + Lo::sBytes, p.vs + blk * kPage, Lo::sBytes, bar, pol);
-      }
-    }
+    const uint64_t pol = l2_evict_first_policy();  // streamed once: keep L2 for others
+    const int j0 = pb + (w + i * kW) * PPI;
+    const int cnt = min(PPI, pe - j0);  // pages of this iteration (>= 1)
+    const int pid = __shfl_sync(0xffffffffu, ids_cur, (i * PPI + cq) & 31);
+    const uint32_t bar = smem_u32(&my_bars[stage]);
+    mbar_arrive_expect_tx_if(lane == 0, bar, static_cast<uint32_t>(cnt * Lo::pageBytes));
+    const uint8_t* base = ck == 0 ? p.k : ck == 1 ? p.v
+                        : reinterpret_cast<const uint8_t*>(NK == 4 && ck == 2 ? p.ks : p.vs);
+    const size_t blk = static_cast<size_t>(max(pid, 0) * p.Hkv + g);
+    bulk_g2s_if(lane < NK * PPI && cq < cnt, c_dst + stage * Lo::stageBytes, base + blk * c_bytes,
+                c_bytes, bar, pol);
   };
   if (n_my > 0) {
-    if (leader) {
+    if (lane == 0) {
       for (int i = 0; i < S; ++i) mbar_init(&my_bars[i], 1);
       fence_barrier_init();
     }
-    pol = l2_evict_first_policy();
     __syncwarp();
     for (int i = 0; i < min(S, n_my); ++i) issue(i, i);
   }
@@ -724,7 +735,6 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   st.finish(aux, lane);
   __syncwarp();
 
-  int werr = 0;
   int i = 0, stage = 0;
   uint32_t phase = 0;
   for (; i < n_my; ++i) {
@@ -734,36 +744,31 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
       break;
     }
     const uint8_t* sp = my_stages + stage * Lo::stageBytes;
-    if ((badmask >> (i & 31)) & 1u) {
-      werr |= 0x1;  // PKV_DEV_BAD_PAGE
-    } else {
-      const int j0 = pb + (w + i * kW) * PPI;
-      if constexpr (KVT == kF32) {
-        const int valid = min(kPage, L - j0 * kPage);
-        constexpr int HM = f32_head_cap<D>();
-        switch (nh) {  // the FP32 path unrolls over the block's head count
-          case 1: st.template page<1>(sp, probs, valid, p.scale_log2, lane); break;
-          case 2: st.template page<2>(sp, probs, valid, p.scale_log2, lane); break;
-          case 3: st.template page<3>(sp, probs, valid, p.scale_log2, lane); break;
-          case 4: st.template page<4>(sp, probs, valid, p.scale_log2, lane); break;
-          default: st.template page<HM>(sp, probs, valid, p.scale_log2, lane); break;
-        }
-      } else if constexpr (KVT == kBF16) {
-        st.page(sp, min(kPage, L - j0 * kPage), lane);
-      } else {
-        int valid[PPI];
-#pragma unroll
-        for (int q = 0; q < PPI; ++q) valid[q] = j0 + q < pe ? min(kPage, L - (j0 + q) * kPage) : 0;
-        st.pages(sp, valid, lane);
+    const int j0 = pb + (w + i * kW) * PPI;
+    if constexpr (KVT == kF32) {
+      const int valid = min(kPage, L - j0 * kPage);
+      constexpr int HM = f32_head_cap<D>();
+      switch (nh) {  // the FP32 path unrolls over the block's head count
+        case 1: st.template page<1>(sp, probs, valid, p.scale_log2, lane); break;
+        case 2: st.template page<2>(sp, probs, valid, p.scale_log2, lane); break;
+        case 3: st.template page<3>(sp, probs, valid, p.scale_log2, lane); break;
+        case 4: st.template page<4>(sp, probs, valid, p.scale_log2, lane); break;
+        default: st.template page<HM>(sp, probs, valid, p.scale_log2, lane); break;
       }
+    } else if constexpr (KVT == kBF16) {
+      st.page(sp, min(kPage, L - j0 * kPage), lane);
+    } else {
+      int valid[PPI];
+#pragma unroll
+      for (int q = 0; q < PPI; ++q) valid[q] = j0 + q < pe ? min(kPage, L - (j0 + q) * kPage) : 0;
+      st.pages(sp, valid, lane);
     }
     const int nxt = i + S;
     if (nxt < n_my) {
-      if ((nxt & 31) == 0) {
+      if (((nxt * PPI) & 31) == 0) {
         // the issue index enters a new batch of ids: it becomes the current one
-#pragma unroll
-        for (int q = 0; q < PPI; ++q) ids_cur[q] = ids_nxt[q];
-        load_ids((nxt >> 5) + 1, ids_nxt);
+        ids_cur = ids_nxt;
+        ids_nxt = load_ids(((nxt * PPI) >> 5) + 1);
       }
       __syncwarp();
       issue(nxt, stage);
@@ -782,6 +787,7 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
       if (++s2 == S) { s2 = 0; ph2 ^= 1u; }
     }
   }
+  werr = __reduce_or_sync(0xffffffffu, werr);
   if (werr && lane == 0) atomicOr(&s_flag, werr);
 
   // ---- merge the warps' states (the stage memory is reused once every warp is done)

@@ -102,6 +102,25 @@ __device__ __forceinline__ void bulk_g2s_if(bool pred, void* dst, const void* sr
       : "memory");
 }
 
+// The same two operations on shared-window addresses (32-bit), for hot loops that keep
+// their stage and barrier addresses in registers.
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(bool pred, uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t"
+      "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_if(bool pred, uint32_t dst, const void* src,
+                                            uint32_t bytes, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t"
+      "@q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;\n\t}" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+
 // One-dimensional bulk copy global -> shared, completing on `bar` (TMA engine).
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
