@@ -111,8 +111,8 @@ template <int KVT, int D>
 struct Smem {
   using Lo = Layout<KVT, D>;
   static constexpr int stages = kW * Lo::S * Lo::stageBytes;
-  // merge area: per-warp max[8], sum[8], acc[8][D+2] floats
-  static constexpr int combine = (2 * kW * kMaxHeads + kW * kMaxHeads * (D + 2)) * 4;
+  // merge area: per-warp max[8], sum[8], acc[8][D+2], then weights [warp][8] (floats)
+  static constexpr int combine = (3 * kW * kMaxHeads + kW * kMaxHeads * (D + 2)) * 4;
   static constexpr int big = stages > combine ? stages : combine;
   static constexpr int probs = KVT == kF32 ? kW * kMaxHeads * kPage * 4 : 0;
   // INT8: the query fragments (one uint4 per k-step and lane) and per-row constants,
@@ -507,10 +507,13 @@ struct Int8Warp {
       vsc[pg][0] = v4.x; vsc[pg][1] = v4.y; vsc[pg][2] = v4.z; vsc[pg][3] = v4.w;
       // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
       // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3 of head r.
+      // The accumulators of the hi rows start at -1152 sum(q): the code bias cancels
+      // inside the FP32 accumulation.
       float sacc[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+        sacc[j][0] = sacc[j][1] = -kbias;
+        sacc[j][2] = sacc[j][3] = 0.f;
         const int tok = 4 * (r >> 1) + (r & 1) + 2 * j;
         const uint8_t* krow = Ks + tok * D;
 #pragma unroll
@@ -529,7 +532,7 @@ struct Int8Warp {
       for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e)
-          x[pg][2 * j + e] = ((sacc[j][e] + sacc[j][2 + e]) - kbias) * (row_scale * ksc[pg][2 * j + e]);
+          x[pg][2 * j + e] = (sacc[j][e] + sacc[j][2 + e]) * (row_scale * ksc[pg][2 * j + e]);
     }
     bool partial = false;
 #pragma unroll
@@ -583,10 +586,10 @@ struct Int8Warp {
       uint32_t bh[2], bl[2];
       split_h2(pv[pg][0], pv[pg][1], bh[0], bl[0]);
       split_h2(pv[pg][2], pv[pg][3], bh[1], bl[1]);
+      // A = V^T rows 16 j + r and 16 j + r + 8, tokens 4c .. 4c+3 (same k-slot order)
       const uint8_t* Vs = st + pg * Lo::pageBytes + Lo::kBytes;
 #pragma unroll
       for (int j = 0; j < MT; ++j) {
-        // A = V^T rows 16 j + r and 16 j + r + 8, tokens 4c .. 4c+3 (same k-slot order)
         const uint32_t w0 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r) * kPage + 4 * c);
         const uint32_t w1 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r + 8) * kPage + 4 * c);
         uint32_t a[4];
@@ -660,13 +663,20 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   const int h0 = g * p.G + hg * p.hpc;
   const int nh = min(p.hpc, p.G - hg * p.hpc);
 
+  // The block-table entries of this warp's first 32 pages do not depend on the context
+  // length: read them together with it (validated below), so that the first copies wait
+  // for one global round trip instead of two.  The warp's page m is the block's logical
+  // page pb + (w + (m / PPI) kW) PPI + m % PPI.
+  const int pb = split * p.chunk;
+  const int32_t* bt = p.bt + static_cast<size_t>(b) * p.MB;
+  const int j_first = pb + (w + (lane / PPI) * kW) * PPI + lane % PPI;
+  const int raw_first = j_first < min(p.MB, pb + p.chunk) ? bt[j_first] : -1;
   const int L = p.lens[b];
   const bool len_ok = L >= 0 && L <= p.MB * kPage;
   const int np = len_ok ? (L + kPage - 1) / kPage : 0;
   const int nsplit = len_ok ? max(1, (np + p.chunk - 1) / p.chunk) : 1;
   if (split >= nsplit) return;
-  const int pb = split * p.chunk, pe = min(np, pb + p.chunk);
-  const int32_t* bt = p.bt + static_cast<size_t>(b) * p.MB;
+  const int pe = min(np, pb + p.chunk);
   if (tid == 0) s_flag = len_ok ? 0 : 0x2 /*PKV_DEV_BAD_LEN*/;
 
   uint8_t* my_stages = stages + static_cast<size_t>(w) * S * Lo::stageBytes;
@@ -677,26 +687,27 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   const int n_my = ngroups > w ? (ngroups - w + kW - 1) / kW : 0;
 
   // ---- page ids: lane l holds the id of this warp's page m = 32 k + l (batch k) for the
-  // current and the next batch; the warp's page m is the block's logical page
-  // pb + (w + (m / PPI) kW) PPI + m % PPI.  -2 marks a page past the block's range.  An
-  // id outside the pool is replaced by page 0 (so every copy stays inside the cache) and
-  // flagged: the block's outputs then become NaN.
+  // current and the next batch.  -2 marks a page past the block's range.  An id outside
+  // the pool is replaced by page 0 (so every copy stays inside the cache) and flagged:
+  // the block's outputs then become NaN.
   int werr = 0;
+  auto check_id = [&](int m, int raw) -> int {
+    const int it = m / PPI;
+    const int j = pb + (w + it * kW) * PPI + m % PPI;
+    if (it >= n_my || j >= pe) return -2;
+    if (raw < 0 || raw >= p.num_pages) {
+      werr |= 0x1;  // PKV_DEV_BAD_PAGE
+      return 0;
+    }
+    return raw;
+  };
   auto load_ids = [&](int batch) -> int {
     const int m = 32 * batch + lane;
     const int it = m / PPI;
     const int j = pb + (w + it * kW) * PPI + m % PPI;
-    int id = -2;
-    if (it < n_my && j < pe) {
-      id = bt[j];
-      if (id < 0 || id >= p.num_pages) {
-        werr |= 0x1;  // PKV_DEV_BAD_PAGE
-        id = 0;
-      }
-    }
-    return id;
+    return check_id(m, it < n_my && j < pe ? bt[j] : -1);
   };
-  int ids_cur = load_ids(0), ids_nxt = load_ids(1);
+  int ids_cur = check_id(lane, raw_first), ids_nxt = load_ids(1);
 
   // ---- copy issue: lane l < NK PPI issues one copy (kind l % NK of page l / NK of the
   // iteration), so a whole stage costs one warp instruction; lane 0 posts the byte count.
@@ -726,7 +737,9 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
       fence_barrier_init();
     }
     __syncwarp();
-    for (int i = 0; i < min(S, n_my); ++i) issue(i, i);
+    // Only the first stage is requested up front: a launch-wide burst of every stage
+    // would delay every warp's first page; the other stages follow its arrival.
+    issue(0, 0);
   }
 
   typename WarpOf<KVT, D>::type st;
@@ -735,13 +748,14 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   st.finish(aux, lane);
   __syncwarp();
 
-  int i = 0, stage = 0;
-  uint32_t phase = 0;
-  for (; i < n_my; ++i) {
+  // One ring step: wait for stage `stage`, consume its pages, refill it with iteration
+  // i + S.  For the tensor-core paths the loop below unrolls the ring, so every stage
+  // address is a constant.
+  auto step = [&](int i, int stage, uint32_t phase) -> bool {
     const bool ok = mbar_wait(&my_bars[stage], phase);
-    if (!__all_sync(0xffffffffu, ok)) {
-      werr |= 0x10;  // PKV_DEV_TIMEOUT
-      break;
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    if (i == 0) {
+      for (int k = 1; k < min(S, n_my); ++k) issue(k, k);
     }
     const uint8_t* sp = my_stages + stage * Lo::stageBytes;
     const int j0 = pb + (w + i * kW) * PPI;
@@ -773,16 +787,46 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
       __syncwarp();
       issue(nxt, stage);
     }
-    if (++stage == S) {
-      stage = 0;
-      phase ^= 1u;
+    return true;
+  };
+  int i = 0, stage = 0;  // where a timed-out wait stopped
+  uint32_t phase = 0;
+  if constexpr (KVT == kF32) {
+    // (the FP32 page code is large: a rolled ring keeps it in the instruction cache)
+    for (; i < n_my; ++i) {
+      if (!step(i, stage, phase)) {
+        werr |= 0x10;  // PKV_DEV_TIMEOUT
+        break;
+      }
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  } else {
+    uint32_t ph = 0;
+    bool going = true;
+    for (int base = 0; going && base < n_my; base += S, ph ^= 1u) {
+#pragma unroll
+      for (int k = 0; k < S; ++k) {
+        if (base + k >= n_my) break;
+        if (!step(base + k, k, ph)) {
+          werr |= 0x10;  // PKV_DEV_TIMEOUT
+          i = base + k;
+          stage = k;
+          phase = ph;
+          going = false;
+          break;
+        }
+      }
     }
   }
   if (werr & 0x10) {
-    // Drain (bounded) whatever this warp still has in flight before leaving.
+    // Drain (bounded) whatever this warp still has in flight before leaving: iterations
+    // i .. i + S - 1 (only iteration 0 when the very first wait gave up).
     int s2 = stage;
     uint32_t ph2 = phase;
-    for (int k = i; k < min(n_my, i + S); ++k) {
+    for (int k = i; k < (i == 0 ? 1 : min(n_my, i + S)); ++k) {
       if (k > i) (void)mbar_wait(&my_bars[s2], ph2);
       if (++s2 == S) { s2 = 0; ph2 ^= 1u; }
     }
@@ -800,30 +844,46 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   const int err = s_flag;
   if (tid == 0 && err && p.dev_status) atomicOr(p.dev_status, err);
 
+  // Merge weights, once per (warp, head): exp2(m_w - M), divided by the total sum when
+  // this block holds the whole sequence (NaN when the block met an error).
+  float* fw = cO + kW * kMaxHeads * (D + 2);
   const bool single = nsplit == 1;
-  for (int idx = tid; idx < nh * D; idx += kThreads) {
-    const int r = idx / D, d = idx % D;
+  if (tid < nh) {
+    const int r = tid;
     float M = -CUDART_INF_F;
 #pragma unroll
     for (int ww = 0; ww < kW; ++ww) M = fmaxf(M, cm[ww * kMaxHeads + r]);
-    float Ls = 0.f, O = 0.f;
+    float f[kW], Ls = 0.f;
 #pragma unroll
     for (int ww = 0; ww < kW; ++ww) {
       const float mw = cm[ww * kMaxHeads + r];
-      const float f = mw == -CUDART_INF_F ? 0.f : fast_exp2(mw - M);
-      Ls += cl[ww * kMaxHeads + r] * f;
-      O += cO[(ww * kMaxHeads + r) * (D + 2) + d] * f;
+      f[ww] = mw == -CUDART_INF_F ? 0.f : fast_exp2(mw - M);
+      Ls += cl[ww * kMaxHeads + r] * f[ww];
     }
     const size_t row = static_cast<size_t>(b) * p.Hq + h0 + r;
     if (single) {
-      p.out[row * D + d] = err ? CUDART_NAN_F : (Ls > 0.f ? O / Ls : 0.f);
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+      for (int ww = 0; ww < kW; ++ww) fw[ww * kMaxHeads + r] = err ? CUDART_NAN_F : f[ww] * inv;
     } else {
+#pragma unroll
+      for (int ww = 0; ww < kW; ++ww) fw[ww * kMaxHeads + r] = f[ww];
       const size_t prow = static_cast<size_t>(split) * p.B * p.Hq + row;
-      p.ws_o[prow * D + d] = O;
-      if (d == 0) {
-        p.ws_m[prow] = err ? CUDART_NAN_F : M;
-        p.ws_l[prow] = Ls;
-      }
+      p.ws_m[prow] = err ? CUDART_NAN_F : M;
+      p.ws_l[prow] = Ls;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < nh * D; idx += kThreads) {
+    const int r = idx / D, d = idx % D;
+    float O = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < kW; ++ww) O += cO[(ww * kMaxHeads + r) * (D + 2) + d] * fw[ww * kMaxHeads + r];
+    const size_t row = static_cast<size_t>(b) * p.Hq + h0 + r;
+    if (single) {
+      p.out[row * D + d] = O;
+    } else {
+      p.ws_o[(static_cast<size_t>(split) * p.B * p.Hq + row) * D + d] = O;
     }
   }
   if (single) return;
@@ -836,11 +896,14 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // The merge: warp w handles heads w and w + 4; its lanes stride over the splits, so
-  // the max and the weighted sum are shuffle reductions and every load is independent.
-  // The weights go to shared memory, then all threads accumulate the partial outputs.
+  // The merge.  Warp w handles heads w and w + 4: its lanes read the (max, sum) of every
+  // split in one round trip and reduce them by shuffles; the weights go to shared memory.
+  // Then each thread owns 4 consecutive outputs of one or two heads and reads the
+  // partial outputs of 8 or 16 splits at a time as 16-byte loads, all in flight together,
+  // adding them in split order.
   {
     float* wts = reinterpret_cast<float*>(stages);  // [nsplit][8] weights, then [8] 1/L
+    float* lsm = wts + (nsplit + 1) * kMaxHeads;    // [nsplit][8] partial sums
     const size_t stride = static_cast<size_t>(p.B) * p.Hq;
     const size_t row0 = static_cast<size_t>(b) * p.Hq + h0;
     __syncthreads();
@@ -849,9 +912,11 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
       bool poisoned = false;
       for (int s = lane; s < nsplit; s += 32) {
         const float ms = __ldcg(p.ws_m + s * stride + row0 + r);
+        const float ls = __ldcg(p.ws_l + s * stride + row0 + r);
         poisoned |= isnan(ms);
         M = fmaxf(M, ms);
         wts[s * kMaxHeads + r] = ms;
+        lsm[s * kMaxHeads + r] = ls;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -861,26 +926,60 @@ __global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
         const float ms = wts[s * kMaxHeads + r];
         const float f = ms == -CUDART_INF_F ? 0.f : fast_exp2(ms - M);
         wts[s * kMaxHeads + r] = f;
-        Ls += __ldcg(p.ws_l + s * stride + row0 + r) * f;
+        Ls += lsm[s * kMaxHeads + r] * f;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
       if (lane == 0) wts[nsplit * kMaxHeads + r] = poisoned ? CUDART_NAN_F : (Ls > 0.f ? 1.f / Ls : 0.f);
     }
     __syncthreads();
-    for (int idx = tid; idx < nh * D; idx += kThreads) {
-      const int r = idx / D, d = idx % D;
-      const float* src = p.ws_o + (row0 + r) * D + d;
-      float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
-      int s = 0;
-      for (; s + 4 <= nsplit; s += 4) {
-        O0 += __ldcg(src + (s + 0) * stride * D) * wts[(s + 0) * kMaxHeads + r];
-        O1 += __ldcg(src + (s + 1) * stride * D) * wts[(s + 1) * kMaxHeads + r];
-        O2 += __ldcg(src + (s + 2) * stride * D) * wts[(s + 2) * kMaxHeads + r];
-        O3 += __ldcg(src + (s + 3) * stride * D) * wts[(s + 3) * kMaxHeads + r];
-      }
-      for (; s < nsplit; ++s) O0 += __ldcg(src + s * stride * D) * wts[s * kMaxHeads + r];
-      p.out[(row0 + r) * D + d] = ((O0 + O1) + (O2 + O3)) * wts[nsplit * kMaxHeads + r];
+    constexpr int D4 = D / 4;
+    constexpr int CPT = (kMaxHeads * D4 + kThreads - 1) / kThreads;  // chunks per thread
+    constexpr int SB = 8;                                             // splits per batch
+    const size_t sstride = stride * D4;  // float4s from one split's partial to the next
+    const float4* src[CPT];
+    int rr[CPT];
+    bool act[CPT];
+    float4 acc[CPT];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+      const int cidx = tid + c * kThreads;
+      act[c] = cidx < nh * D4;
+      rr[c] = act[c] ? cidx / D4 : 0;
+      src[c] = reinterpret_cast<const float4*>(p.ws_o + (row0 + rr[c]) * D) + (act[c] ? cidx % D4 : 0);
+      acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int s0 = 0; s0 < nsplit; s0 += SB) {
+      float4 v[CPT][SB];
+#pragma unroll
+      for (int c = 0; c < CPT; ++c)
+#pragma unroll
+        for (int k = 0; k < SB; ++k)
+          v[c][k] = act[c] && s0 + k < nsplit ? __ldcg(src[c] + (s0 + k) * sstride)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c)
+#pragma unroll
+        for (int k = 0; k < SB; ++k) {
+          if (s0 + k < nsplit) {
+            const float wt = wts[(s0 + k) * kMaxHeads + rr[c]];
+            acc[c].x += v[c][k].x * wt;
+            acc[c].y += v[c][k].y * wt;
+            acc[c].z += v[c][k].z * wt;
+            acc[c].w += v[c][k].w * wt;
+          }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+      if (!act[c]) continue;
+      const int cidx = tid + c * kThreads;
+      const float inv = wts[nsplit * kMaxHeads + rr[c]];
+      float* dst = p.out + (row0 + rr[c]) * D + 4 * (cidx % D4);
+      dst[0] = acc[c].x * inv;
+      dst[1] = acc[c].y * inv;
+      dst[2] = acc[c].z * inv;
+      dst[3] = acc[c].w * inv;
     }
   }
   if (tid == 0) *ticket = 0;  // leave the counter ready for the next call
@@ -896,12 +995,12 @@ struct Variant {
   int smem;
   int index;
   int ppi;
-  int max_splits;  // the last block's merge keeps (splits + 1) x 8 weights in shared memory
+  int max_splits;  // the last block's merge keeps (2 splits + 1) x 8 floats in shared memory
 };
 
 template <int KVT, int D>
 constexpr int max_splits_of() {
-  return Smem<KVT, D>::big / (kMaxHeads * 4) - 1;
+  return Smem<KVT, D>::big / (2 * kMaxHeads * 4) - 1;
 }
 
 #define PKV_VARIANT(T, D, I) \
@@ -1028,9 +1127,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
     p.ws_ticket = reinterpret_cast<int*>(base);
     const size_t rows = static_cast<size_t>(plan.n_splits) * a.B * a.Hq;
     float* f = reinterpret_cast<float*>(base + ((tickets * 4 + 255) / 256) * 256);
-    p.ws_m = f;
-    p.ws_l = f + rows;
-    p.ws_o = f + 2 * rows;
+    p.ws_o = f;  // [split][seq][head][D]: 16-byte aligned rows for the merge's loads
+    p.ws_m = f + rows * a.c.D;
+    p.ws_l = p.ws_m + rows;
   }
   // (the shared-memory limit was raised by plan_decode on this device)
   const dim3 grid(plan.n_splits, a.B, a.c.Hkv * plan.head_groups);

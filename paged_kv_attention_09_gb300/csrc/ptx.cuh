@@ -134,6 +134,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 // Four 8x8 b16 matrices from shared memory (lanes 8i..8i+7 give matrix i's row
 // addresses); lane t receives row t/4, elements 2(t%4), 2(t%4)+1 of each matrix.
+__device__ __forceinline__ void ldsm_x2(uint32_t (&f)[2], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(f[0]), "=r"(f[1])
+               : "r"(addr));
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t (&f)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
