@@ -46,8 +46,6 @@
 namespace pkv {
 namespace {
 
-constexpr int kW = 4;            // warps per block
-constexpr int kThreads = kW * 32;
 constexpr int kMaxHeads = 8;     // query heads per block
 
 struct DParams {
@@ -92,6 +90,9 @@ struct Tune {
   static constexpr int S = KVT == kINT8 ? PKV_INT8_STAGES
                          : KVT == kBF16 ? (D == 64 ? 3 : PKV_BF16_STAGES)
                                         : (D == 64 ? 3 : 2);
+  // Warps per block.  (Three-warp INT8 blocks, which leave 96 registers at 7 blocks per
+  // SM, measured slower than four warps at 72 registers.)
+  static constexpr int W = 4;
   static constexpr int minBlocks = (KVT == kINT8 && D == 64) ? 7 : (KVT == kBF16 && D == 128) ? 3 : 1;
 };
 
@@ -110,6 +111,7 @@ struct Layout {
 template <int KVT, int D>
 struct Smem {
   using Lo = Layout<KVT, D>;
+  static constexpr int kW = Tune<KVT, D>::W;
   static constexpr int stages = kW * Lo::S * Lo::stageBytes;
   // merge area: per-warp max[8], sum[8], acc[8][D+2], then weights [warp][8] (floats)
   static constexpr int combine = (3 * kW * kMaxHeads + kW * kMaxHeads * (D + 2)) * 4;
@@ -417,7 +419,8 @@ struct Int8Warp {
   static constexpr int KS = D / 16;  // k-steps of the q.k product
   static constexpr int MT = D / 16;  // m-tiles (16 head-dim rows) of O^T = V^T P^T
   static constexpr int PPI = Tune<kINT8, D>::PPI;  // pages per iteration
-  uint32_t qf[KS][4];                // f16 A fragments of the query rows (hi 0-7, lo 8-15)
+  const uint4* qs;                   // [k-step][lane] f16 A fragments of the query rows
+                                     // (hi 0-7, lo 8-15), in shared memory
   // O^T accumulators: lane (r, c) holds head-dim rows 16 mt + r and 16 mt + r + 8 of
   // heads 2c and 2c + 1 (the C layout of the transposed product)
   float o[MT][4];
@@ -480,12 +483,7 @@ struct Int8Warp {
     for (int j = 0; j < MT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   }
   __device__ void finish(const uint8_t* aux, int lane) {
-    const uint4* frag = reinterpret_cast<const uint4*>(aux);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const uint4 f = frag[ks * 32 + lane];
-      qf[ks][0] = f.x; qf[ks][1] = f.y; qf[ks][2] = f.z; qf[ks][3] = f.w;
-    }
+    qs = reinterpret_cast<const uint4*>(aux);
     const float* rowc = reinterpret_cast<const float*>(aux + KS * 32 * 16);
     row_scale = rowc[lane >> 2];
     kbias = rowc[kMaxHeads + (lane >> 2)];
@@ -509,22 +507,29 @@ struct Int8Warp {
       // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3 of head r.
       // The accumulators of the hi rows start at -1152 sum(q): the code bias cancels
       // inside the FP32 accumulation.
+      // Each query fragment is read once per page and serves both n-tiles.
       float sacc[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         sacc[j][0] = sacc[j][1] = -kbias;
         sacc[j][2] = sacc[j][3] = 0.f;
-        const int tok = 4 * (r >> 1) + (r & 1) + 2 * j;
-        const uint8_t* krow = Ks + tok * D;
+      }
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk) {
-          const uint4 w = *reinterpret_cast<const uint4*>(krow + blk * 64 + c * 16);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      for (int blk = 0; blk < D / 64; ++blk) {
+        uint4 kw[2];
 #pragma unroll
-          for (int s = 0; s < 4; ++s) {
+        for (int j = 0; j < 2; ++j)
+          kw[j] = *reinterpret_cast<const uint4*>(Ks + (4 * (r >> 1) + (r & 1) + 2 * j) * D + blk * 64 + c * 16);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint4 f = qs[(4 * blk + s) * 32 + lane];
+          const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t wsj = s == 0 ? kw[j].x : s == 1 ? kw[j].y : s == 2 ? kw[j].z : kw[j].w;
             uint32_t b0, b1;
-            s8x4_to_f16x4_biased(ws[s], b0, b1);
-            mma_f16(sacc[j], qf[4 * blk + s], b0, b1);
+            s8x4_to_f16x4_biased(wsj, b0, b1);
+            mma_f16(sacc[j], a, b0, b1);
           }
         }
       }
@@ -645,11 +650,12 @@ struct WarpOf<kINT8, D> {
 // ------------------------------------------------------------------ the kernel
 
 template <int KVT, int D>
-__global__ void __launch_bounds__(kThreads, Tune<KVT, D>::minBlocks)
+__global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     decode_kernel(const __grid_constant__ DParams p) {
   using Lo = Layout<KVT, D>;
   using Sm = Smem<KVT, D>;
   constexpr int S = Lo::S, PPI = Lo::PPI;
+  constexpr int kW = Tune<KVT, D>::W, kThreads = kW * 32;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   float* probs_all = reinterpret_cast<float*>(smem + Sm::big);
@@ -996,6 +1002,7 @@ struct Variant {
   int index;
   int ppi;
   int max_splits;  // the last block's merge keeps (2 splits + 1) x 8 floats in shared memory
+  int warps;       // warps per block
 };
 
 template <int KVT, int D>
@@ -1004,7 +1011,7 @@ constexpr int max_splits_of() {
 }
 
 #define PKV_VARIANT(T, D, I) \
-  {kernel_ptr<T, D>(), Smem<T, D>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>()}
+  {kernel_ptr<T, D>(), Smem<T, D>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>(), Tune<T, D>::W}
 Variant variant(int dtype, int D) {
   switch (dtype * 1000 + D) {
     case kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, 0);
@@ -1013,7 +1020,7 @@ Variant variant(int dtype, int D) {
     case kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, 3);
     case kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, 4);
     case kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, 5);
-    default: return {nullptr, 0, -1, 1, 1};
+    default: return {nullptr, 0, -1, 1, 1, 4};
   }
 }
 #undef PKV_VARIANT
@@ -1039,7 +1046,7 @@ bool device_facts(int device, const Variant& v, int* sms, int* occ) {
     int o = 0;
     if (cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.fn, kThreads, v.smem) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.fn, v.warps * 32, v.smem) !=
             cudaSuccess)
       return false;
     d.occ[v.index] = o > 0 ? o : 1;
@@ -1076,7 +1083,7 @@ bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int dev
     long long splits = 1;
     if (units > 0 && 4 * units < 3 * slots) {
       splits = (2 * slots + units - 1) / units;
-      const long long by_len = mb / (8 * kW * v.ppi);
+      const long long by_len = mb / (8 * v.warps * v.ppi);
       if (splits > by_len) splits = by_len;
       if (splits > 32) splits = 32;
       if (splits < 1) splits = 1;
@@ -1134,7 +1141,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   // (the shared-memory limit was raised by plan_decode on this device)
   const dim3 grid(plan.n_splits, a.B, a.c.Hkv * plan.head_groups);
   void* args[] = {&p};
-  return cudaLaunchKernel(v.fn, grid, dim3(kThreads), args, v.smem, st);
+  return cudaLaunchKernel(v.fn, grid, dim3(v.warps * 32), args, v.smem, st);
 }
 
 }  // namespace pkv
