@@ -176,6 +176,9 @@ struct F32Warp {
   float o[HM][NC];
 
   __device__ void finish(const uint8_t*, int) {}
+  // (loading the queries before the first copy measured slower here: they are only
+  // consumed by the first page anyway)
+  __device__ void prefetch(const DParams&, int, int, int, int, int) {}
   __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t*, int) {
     const int c8 = lane & 7;
 #pragma unroll
@@ -301,27 +304,53 @@ template <int D>
 struct Bf16Warp {
   static constexpr int KS = D / 16;  // k-steps of the q.k product
   static constexpr int NT = D / 8;   // n-tiles of the P.V product
-  uint32_t qa[KS][4];
+  uint32_t qa[KS][4];  // raw query bits from prefetch(), then the A fragments
   float o[NT][4];
   float m, l, row_scale;
 
   __device__ void finish(const uint8_t*, int) {}
-  __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t*, int) {
+  // Query elements of k-slots {2c, 2c+1} and {2c+8, 2c+9} of every k-step (the standard
+  // fragment order), loaded as raw bits: two BF16 or two FP32 values per slot pair.
+  __device__ void prefetch(const DParams& p, int b, int h0, int nh, int lane, int) {
     const int r = lane >> 2, c = lane & 3;
     const bool has = r < nh;
     const size_t row = (static_cast<size_t>(b) * p.Hq + h0 + r) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      // standard fragment order: k-slots {2c, 2c+1} and {2c+8, 2c+9} of k-step ks
-      float2 lo2 = make_float2(0.f, 0.f), hi2 = make_float2(0.f, 0.f);
-      if (has) {
-        const float4 a = load_q4(p.q, p.q_dtype, row + 16 * ks + (2 * c & ~3));
-        const float4 e = load_q4(p.q, p.q_dtype, row + 16 * ks + 8 + (2 * c & ~3));
-        lo2 = (c & 1) ? make_float2(a.z, a.w) : make_float2(a.x, a.y);
-        hi2 = (c & 1) ? make_float2(e.z, e.w) : make_float2(e.x, e.y);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const size_t i = row + 16 * ks + 8 * half + 2 * c;
+        uint32_t w0 = 0u, w1 = 0u;
+        if (has) {
+          if (p.q_dtype == kBF16) {
+            w0 = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.q) + i);
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const float*>(p.q) + i);
+            w0 = v.x;
+            w1 = v.y;
+          }
+        }
+        qa[ks][2 * half] = w0;
+        qa[ks][2 * half + 1] = w1;
       }
-      split_b2(lo2.x, lo2.y, qa[ks][0], qa[ks][1]);
-      split_b2(hi2.x, hi2.y, qa[ks][2], qa[ks][3]);
+    }
+  }
+  __device__ void init(const DParams& p, int, int, int, int, uint8_t*, int) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float2 v;
+        if (p.q_dtype == kBF16) {
+          v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qa[ks][2 * half]));
+        } else {
+          v = make_float2(__uint_as_float(qa[ks][2 * half]), __uint_as_float(qa[ks][2 * half + 1]));
+        }
+        uint32_t hi, lo;
+        split_b2(v.x, v.y, hi, lo);
+        qa[ks][2 * half] = hi;      // rows 0-7 (a0 / a2): the BF16 high part
+        qa[ks][2 * half + 1] = lo;  // rows 8-15 (a1 / a3): the remainder
+      }
     }
     row_scale = p.scale_log2;
     m = -CUDART_INF_F;
@@ -429,6 +458,10 @@ struct Int8Warp {
   // k-slot pair {2c, 2c+1} of k-step ks <-> head_dim 64(ks/4) + 16c + 4(ks%4): each lane's
   // K operand is then one contiguous 16-byte shared-memory load per n-tile.
   __device__ static int kslot_d(int ks, int c) { return 64 * (ks >> 2) + 16 * c + 4 * (ks & 3); }
+
+  // (loading the queries ahead of the first copy, into registers or by a bulk copy into
+  // shared memory, measured slower for this register-bound kernel)
+  __device__ void prefetch(const DParams&, int, int, int, int, int) {}
 
   // Warp 0 builds the fragments and the per-row constants; the caller synchronises the
   // block before any warp reads them (finish()).
@@ -677,6 +710,8 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   const int32_t* bt = p.bt + static_cast<size_t>(b) * p.MB;
   const int j_first = pb + (w + (lane / PPI) * kW) * PPI + lane % PPI;
   const int raw_first = j_first < min(p.MB, pb + p.chunk) ? bt[j_first] : -1;
+  typename WarpOf<KVT, D>::type st;
+  st.prefetch(p, b, h0, nh, lane, w);  // query loads, in flight with the length and table reads
   const int L = p.lens[b];
   const bool len_ok = L >= 0 && L <= p.MB * kPage;
   const int np = len_ok ? (L + kPage - 1) / kPage : 0;
@@ -748,7 +783,6 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     issue(0, 0);
   }
 
-  typename WarpOf<KVT, D>::type st;
   st.init(p, b, h0, nh, lane, aux, w);
   if constexpr (KVT == kINT8) __syncthreads();  // warp 0 built the shared query fragments
   st.finish(aux, lane);
