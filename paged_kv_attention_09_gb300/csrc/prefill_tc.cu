@@ -8,18 +8,24 @@
 //
 // One block computes 128 query rows — (chunk token, query head) pairs of one GQA group,
 // token-major — against the group's paged K/V in tiles of 64 keys (4 pages):
-//   warp 9    producer: one bulk copy per BF16 page block (K and V, already stored as
-//             tensor-core tiles) into a two-stage ring;
-//   warp 8    MMA issuer: S = Q K^T (M=128, N=64) into a double-buffered TMEM region and
-//             O += P V (M=128, N=head_dim) into a TMEM accumulator, one thread issuing
-//             tcgen05.mma and tracking completion with tcgen05.commit on mbarriers;
-//   warps 0-7 softmax: two threads per row (one TMEM lane, 32 keys each; the row max is
-//             exchanged through shared memory): they read S from TMEM, apply the causal
-//             mask and the online softmax in FP32, and write P into shared memory as a
-//             BF16 high part and a BF16 remainder (two MMAs per page) so that the product
-//             keeps ~16 bits.  The running max is only raised when it
-//             grows by more than 2^8 (the accumulator in TMEM is rescaled then), so the
-//             P.V MMAs accumulate without a per-tile round trip through registers.
+//   warps 9, 10  producers of K and of V: one bulk copy per BF16 page block (already
+//             stored as tensor-core tiles) into a ring each; two threads, so that K runs
+//             ahead of V (the V ring is paced by the P.V products, late in each tile);
+//   warp 8    score MMAs: S = Q K^T (M=128, N=64) into one of two TMEM score buffers;
+//   warp 11   P.V MMAs: O += P V (M=128, N=head_dim) into one of two TMEM accumulators;
+//             one thread each issues tcgen05.mma and tracks completion with
+//             tcgen05.commit on mbarriers: two issuers, so that one waits on its barriers
+//             while the other keeps the tensor pipe fed;
+//   warps 0-7 softmax, two groups of four warps: group g takes key tiles g, g+2, g+4, ...
+//             with its own running max and sum, its own score buffer, P buffer and O
+//             accumulator, one thread per row (one TMEM lane, 64 keys).  The groups work on
+//             two tiles at once and never wait for each other; their (max, sum, O) are
+//             merged once at the end.  A thread reads S from TMEM, applies the causal mask
+//             and the online softmax in FP32, and writes P back into TMEM as a BF16 high
+//             part and a BF16 remainder (two MMAs per page, A operand read from TMEM) so
+//             that the product keeps ~16 bits and P never crosses shared memory.  The running max is only raised when it grows by more than 2^8
+//             (the group's accumulator in TMEM is rescaled then), so the P.V MMAs
+//             accumulate without a per-tile round trip through registers.
 // FP32 queries are split the same way into two BF16 tiles (two Q.K^T MMAs per k-step).
 // Every operand tile uses the no-swizzle K-major canonical layout of 8 x 16-byte core
 // matrices; every wait is bounded.
@@ -38,9 +44,9 @@ namespace {
 constexpr int kRowsTC = 128;      // query rows per block (MMA M)
 constexpr int kKeysTC = 64;       // keys per tile (MMA N of S)
 constexpr int kPagesTC = kKeysTC / kPage;
-constexpr int kSoftWarps = 8;           // two threads per query row, 32 keys each
+constexpr int kSoftWarps = 8;           // two groups of 4 warps, one thread per query row
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kThreadsTC = (kSoftWarps + 2) * 32;
+constexpr int kThreadsTC = (kSoftWarps + 4) * 32;  // + two MMA issuers, K and V producers
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only beyond this margin
 
 struct TParams {
@@ -62,19 +68,21 @@ struct TSmem {
   static constexpr int qTile = kRowsTC * D * 2;        // one BF16 query tile
   static constexpr int stage = kPagesTC * kBlk;        // the K (or V) blocks of one tile
   static constexpr int KST = QSPLIT ? 2 : 3;           // stages of each of the K and V rings
-  static constexpr int pTile = kRowsTC * kKeysTC * 2;  // one BF16 probability tile
   static constexpr int q0 = 0;
   static constexpr int k0 = q0 + (QSPLIT ? 2 : 1) * qTile;
   static constexpr int v0 = k0 + KST * stage;
-  static constexpr int p0 = v0 + KST * stage;           // [buffer][hi, lo]
-  static constexpr int bar0 = p0 + 2 * 2 * pTile;
-  // barriers: k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], s_free[2],
-  // p_full[2], o_done[2], final, row-max exchange[2], row-sum exchange
-  static constexpr int nbars = 24;
+  static constexpr int bar0 = v0 + KST * stage;
+  // barriers: k_full[3], k_empty[3], v_full[3], v_empty[3], then per softmax group
+  // s_full[2], s_free[2], p_full[2], o_done[2]; final MMA drain; the groups' final exchange
+  static constexpr int nbars = 22;
   static constexpr int misc0 = bar0 + nbars * 8;        // TMEM base address, flags
-  static constexpr int xch0 = misc0 + 16;  // max [2 tiles][2 halves][128], sum [2 halves][128]
-  static constexpr int total = xch0 + 3 * 2 * kRowsTC * 4;
-  static constexpr int tmemCols = (D + 2 * kKeysTC) <= 256 ? 256 : 512;
+  static constexpr int xch0 = misc0 + 16;  // final exchange: max [2 groups][128], sum [2][128]
+  static constexpr int total = xch0 + 2 * 2 * kRowsTC * 4;
+  // TMEM columns: O of group 0 [0, D), O of group 1 [D, 2D), S of group g at 2D + 64 g,
+  // P of group g at 2D + 128 + 64 g (BF16 pairs: high parts in the first 32 columns,
+  // remainders in the next 32)
+  static constexpr int sCol = 2 * D, pCol = 2 * D + 2 * kKeysTC;
+  static constexpr int tmemCols = (2 * D + 4 * kKeysTC) <= 256 ? 256 : 512;
 };
 
 // Byte offset of element (row, col) in a no-swizzle K-major tile whose K extent is
@@ -98,7 +106,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   uint64_t* p_full = bars + 16;
   uint64_t* o_done = bars + 18;
   uint64_t* fin = bars + 20;
-  uint64_t* xbar = bars + 21;  // [2] row-max exchange, [2] row-sum exchange
+  uint64_t* xfin = bars + 21;  // the two softmax groups' final (max, sum) exchange
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sm::misc0);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sm::misc0 + 4);
   __shared__ int s_err;
@@ -139,9 +147,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < Sm::nbars; ++i) {
-      // s_free, p_full and the exchanges: one arrival per softmax thread
-      const bool many = (i >= 14 && i < 18) || i >= 21;
-      mbar_init(&bars[i], many ? kSoftThreads : 1);
+      // s_free and p_full: one arrival per thread of the group; the exchange: every
+      // softmax thread; the rest: one arrival (or tcgen05.commit)
+      const int count = (i >= 14 && i < 18) ? kSoftThreads / 2
+                        : i == 21 ? kSoftThreads
+                        : i == 20 ? 2  // the final drain: one commit from each MMA issuer
+                        : 1;
+      mbar_init(&bars[i], count);
     }
     fence_barrier_init();
     *abort_flag = 0;
@@ -192,216 +204,247 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(smem);
 
-  if (n_tiles > 0 && warp == kSoftWarps + 1) {
-    // ---------------------------------------------------------------- producer
+  if (n_tiles > 0 && (warp == kSoftWarps + 1 || warp == kSoftWarps + 2)) {
+    // ---------------------------------------------------------------- producers
+    // warp kSoftWarps + 1 fills the K ring, warp kSoftWarps + 2 the V ring
     if (lane == 0) {
+      const bool isK = warp == kSoftWarps + 1;
       const uint64_t pol = l2_evict_last_policy();  // every row tile of the group rereads them
       constexpr int KST = Sm::KST;
+      uint64_t* full = isK ? k_full : v_full;
+      uint64_t* empty = isK ? k_empty : v_empty;
+      const uint8_t* src = isK ? p.k : p.v;
+      uint8_t* ring = smem + (isK ? Sm::k0 : Sm::v0);
       int issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % KST, use = j / KST;
         const int np = min(kPagesTC, n_pages - j * kPagesTC);
-        if (j >= KST && !mbar_wait(&k_empty[st], (use - 1) & 1)) { *abort_flag = 1; break; }
+        if (j >= KST && !mbar_wait(&empty[st], (use - 1) & 1)) { *abort_flag = 1; break; }
         if (*abort_flag) break;
-        uint8_t* kst = smem + Sm::k0 + st * Sm::stage;
-        mbar_arrive_expect_tx(&k_full[st], np * Sm::kBlk);
+        mbar_arrive_expect_tx(&full[st], np * Sm::kBlk);
         for (int q = 0; q < np; ++q) {
           const size_t blk = static_cast<size_t>(bt[j * kPagesTC + q]) * p.Hkv + g;
-          bulk_g2s(kst + q * Sm::kBlk, p.k + blk * Sm::kBlk, Sm::kBlk, &k_full[st], pol);
-        }
-        if (j >= KST && !mbar_wait(&v_empty[st], (use - 1) & 1)) { *abort_flag = 1; issued = -(j + 1); break; }
-        uint8_t* vst = smem + Sm::v0 + st * Sm::stage;
-        mbar_arrive_expect_tx(&v_full[st], np * Sm::kBlk);
-        for (int q = 0; q < np; ++q) {
-          const size_t blk = static_cast<size_t>(bt[j * kPagesTC + q]) * p.Hkv + g;
-          bulk_g2s(vst + q * Sm::kBlk, p.v + blk * Sm::kBlk, Sm::kBlk, &v_full[st], pol);
+          bulk_g2s(ring + st * Sm::stage + q * Sm::kBlk, src + blk * Sm::kBlk, Sm::kBlk, &full[st], pol);
         }
         issued = j + 1;
       }
       // leave nothing in flight: the copies of the last issued tiles have landed
-      const int kdone = issued >= 0 ? issued : -issued;   // K issued for tiles < kdone
-      const int vdone = issued >= 0 ? issued : -issued - 1;
-      for (int j = max(0, kdone - KST); j < kdone; ++j) (void)mbar_wait(&k_full[j % KST], (j / KST) & 1);
-      for (int j = max(0, vdone - KST); j < vdone; ++j) (void)mbar_wait(&v_full[j % KST], (j / KST) & 1);
+      for (int j = max(0, issued - KST); j < issued; ++j) (void)mbar_wait(&full[j % KST], (j / KST) & 1);
     }
-  } else if (n_tiles > 0 && warp == kSoftWarps) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (n_tiles > 0 && (warp == kSoftWarps || warp == kSoftWarps + 3)) {
+    // ---------------------------------------------------------------- MMA issuers
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kRowsTC, kKeysTC);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kRowsTC, D);
       constexpr uint32_t sboQK = (D / 8) * 128;  // 8-row groups of Q and of K
       const uint32_t qhi = sbase + Sm::q0, qlo = sbase + Sm::q0 + Sm::qTile;
       constexpr int KST = Sm::KST;
+      // Operand descriptors are built once and stepped by constant offsets, so that issuing
+      // an MMA costs a few instructions.
+      const uint64_t dQhi = tc::smem_desc(qhi, 128, sboQK), dQlo = tc::smem_desc(qlo, 128, sboQK);
+      const uint64_t dK0 = tc::smem_desc(sbase + Sm::k0, 128, sboQK);
+      const uint64_t dV0 = tc::smem_desc(sbase + Sm::v0, 128, 256);
+      // S_j = Q K_j^T into the score buffer of group j & 1, once that group has read S_{j-2}
+      auto issue_s = [&](int j) -> bool {
+        const int x = j & 1;
+        if (!mbar_wait(&k_full[j % KST], (j / KST) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&s_free[x], ((j - 2) >> 1) & 1)) return false;
+        if (*abort_flag) return false;
+        tc::fence_after_sync();
+        const uint64_t dK = tc::desc_add(dK0, (j % KST) * Sm::stage);
+        const uint32_t tS = tmem + Sm::sCol + kKeysTC * x;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t bd = tc::desc_add(dK, ks * 256);
+          tc::mma_bf16(tS, tc::desc_add(dQhi, ks * 256), bd, idS, ks > 0);
+          if constexpr (QSPLIT) tc::mma_bf16(tS, tc::desc_add(dQlo, ks * 256), bd, idS, true);
+        }
+        tc::commit(&s_full[x]);
+        tc::commit(&k_empty[j % KST]);
+        return true;
+      };
+      // O_y += P_i V_i into the accumulator of group y = i & 1 (its first tile starts it)
       auto issue_pv = [&](int i) -> bool {
         const int y = i & 1;
         if (!mbar_wait(&p_full[y], (i >> 1) & 1)) return false;
         if (!mbar_wait(&v_full[i % KST], (i / KST) & 1)) return false;
         tc::fence_after_sync();
-        const uint32_t vst = sbase + Sm::v0 + (i % KST) * Sm::stage;
-        const uint32_t pbuf = sbase + Sm::p0 + y * 2 * Sm::pTile;
+        const uint64_t dV = tc::desc_add(dV0, (i % KST) * Sm::stage);
+        const uint32_t tP = tmem + Sm::pCol + kKeysTC * y;  // A = P straight from TMEM
 #pragma unroll
         for (int q = 0; q < kPagesTC; ++q) {
-          const uint64_t bd = tc::smem_desc(vst + q * Sm::kBlk, 128, 256);
+          const uint64_t bd = tc::desc_add(dV, q * Sm::kBlk);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint64_t ad = tc::smem_desc(pbuf + part * Sm::pTile + q * 256, 128, 1024);
-            tc::mma_bf16(tmem, ad, bd, idO, !(i == 0 && q == 0 && part == 0));
-          }
+          for (int part = 0; part < 2; ++part)
+            tc::mma_bf16_ts(tmem + D * y, tP + 32 * part + 8 * q, bd, idO, !(i < 2 && q == 0 && part == 0));
         }
         tc::commit(&o_done[y]);
         tc::commit(&v_empty[i % KST]);
         return true;
       };
+      // Warp 8 runs ahead through the score tiles (bounded by the two score buffers);
+      // warp 11 follows the softmax groups with the P.V products.
       bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int x = j & 1;
-        ok = mbar_wait(&k_full[j % KST], (j / KST) & 1) &&
-             (j < 2 || mbar_wait(&s_free[x], ((j - 2) >> 1) & 1)) && !*abort_flag;
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint32_t kst = sbase + Sm::k0 + (j % KST) * Sm::stage;
-        const uint32_t tS = tmem + D + kKeysTC * x;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t bd = tc::smem_desc(kst + ks * 256, 128, sboQK);
-          tc::mma_bf16(tS, tc::smem_desc(qhi + ks * 256, 128, sboQK), bd, idS, ks > 0);
-          if constexpr (QSPLIT) tc::mma_bf16(tS, tc::smem_desc(qlo + ks * 256, 128, sboQK), bd, idS, true);
-        }
-        tc::commit(&s_full[x]);
-        tc::commit(&k_empty[j % KST]);
-        if (j >= 1) ok = issue_pv(j - 1);
+      if (warp == kSoftWarps) {
+        for (int j = 0; j < n_tiles && ok; ++j) ok = issue_s(j);
+      } else {
+        for (int i = 0; i < n_tiles && ok; ++i) ok = issue_pv(i);
       }
-      if (ok) ok = issue_pv(n_tiles - 1);
       if (!ok) *abort_flag = 1;
-      // every MMA issued above has completed before TMEM is released
+      // every MMA either issuer started has completed before TMEM is released
       tc::commit(fin);
       (void)mbar_wait(fin, 0);
     }
   } else if (n_tiles > 0) {
     // ---------------------------------------------------------------- softmax rows
+    // group grp (= hf) owns tiles grp, grp + 2, ...: score buffer, P buffer and O
+    // accumulator grp; thread = row r (TMEM lane 32 (warp % 4) + lane)
+    const int grp = hf;
     const int pos = valid_row ? L - Lq + rho / p.G : p_first;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tO = tmem + lane_base + D * grp;
     const float sl = p.scale_log2;
-    float* xch = reinterpret_cast<float*>(smem + Sm::xch0);  // [tile & 1][half][row]
     float m_used = -CUDART_INF_F, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int x = j & 1;
-      ok = mbar_wait(&s_full[x], (j >> 1) & 1) && !*abort_flag;
+    int n_mine = 0;  // tiles this group has finished
+    for (int j = grp; j < n_tiles; j += 2, ++n_mine) {
+      const int k = j >> 1;  // this group's k-th tile
+      ok = mbar_wait(&s_full[grp], k & 1) && !*abort_flag;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc::fence_after_sync();
-      float s[32];
-      tc::ld32(tmem + lane_base + D + kKeysTC * x + 32 * hf, s);
-      tc::fence_before_sync();
-      mbar_arrive(&s_free[x]);
-      const int key0 = j * kKeysTC + 32 * hf;
-      // raw scores; the scale (> 0) is applied inside the exponent with one FMA
-      if (j * kKeysTC + kKeysTC - 1 > p_first || j * kKeysTC + kKeysTC > n_keys) {
+      float s[64];
+      {
+        float t0[32], t1[32];
+        tc::ld32(tmem + lane_base + Sm::sCol + kKeysTC * grp, t0);
+        tc::ld32(tmem + lane_base + Sm::sCol + kKeysTC * grp + 32, t1);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = (key0 + k <= pos) ? s[k] : -CUDART_INF_F;
+        for (int u = 0; u < 32; ++u) { s[u] = t0[u]; s[32 + u] = t1[u]; }
       }
-      float mx = s[0];
+      tc::fence_before_sync();
+      mbar_arrive(&s_free[grp]);
+      const int key0 = j * kKeysTC;
+      // raw scores; the scale (> 0) is applied inside the exponent with one FMA
+      if (key0 + kKeysTC - 1 > p_first || key0 + kKeysTC > n_keys) {
 #pragma unroll
-      for (int k = 1; k < 32; ++k) mx = fmaxf(mx, s[k]);
-      xch[(x * 2 + hf) * kRowsTC + r] = mx;
-      mbar_arrive(&xbar[x]);
-      ok = mbar_wait(&xbar[x], (j >> 1) & 1);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      mx = fmaxf(mx, xch[(x * 2 + (hf ^ 1)) * kRowsTC + r]) * sl;
+        for (int u = 0; u < 64; ++u) s[u] = (key0 + u <= pos) ? s[u] : -CUDART_INF_F;
+      }
+      float t[32];  // pairwise max tree (a flat chain would be 63 dependent steps)
+#pragma unroll
+      for (int u = 0; u < 32; ++u) t[u] = fmaxf(s[u], s[u + 32]);
+#pragma unroll
+      for (int w2 = 16; w2 >= 1; w2 >>= 1)
+#pragma unroll
+        for (int u = 0; u < w2; ++u) t[u] = fmaxf(t[u], t[u + w2]);
+      const float mx = t[0] * sl;
       const bool need = mx > m_used + kRescaleLog2;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_used;
         const float f = need ? fast_exp2(m_used - m_new) : 1.f;
-        if (j >= 1) {
-          // O holds tiles 0 .. j-1: wait for the last P.V, then rescale this half's columns
-          ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        if (k >= 1) {
+          // O holds this group's earlier tiles: wait for their last P.V, then rescale
+          ok = mbar_wait(&o_done[grp], (k - 1) & 1);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc::fence_after_sync();
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             float o[32];
-            const uint32_t ta = tmem + lane_base + (D / 2) * hf + 32 * c;
-            tc::ld32(ta, o);
+            tc::ld32(tO + 32 * c, o);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] *= f;
-            tc::st32(ta, o);
+            for (int u = 0; u < 32; ++u) o[u] *= f;
+            tc::st32(tO + 32 * c, o);
           }
         }
         l *= f;
         m_used = m_new;
       }
-      if (j >= 2) {  // the P buffer being rewritten was read by the P.V of tile j-2
-        ok = mbar_wait(&o_done[x], ((j - 2) >> 1) & 1);
+      if (k >= 1) {  // P buffer grp was read by the P.V of this group's previous tile
+        ok = mbar_wait(&o_done[grp], (k - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
-      uint8_t* phi = smem + Sm::p0 + x * 2 * Sm::pTile;
-      uint8_t* plo = phi + Sm::pTile;
-      const float nm = -m_used;
+      // (a group can meet a row's keys only in a later tile: while its max is still -inf,
+      // every probability is 0, not exp2(-inf + inf))
+      const float nm = m_used == -CUDART_INF_F ? 0.f : -m_used;
+      const uint32_t tP = tmem + lane_base + Sm::pCol + kKeysTC * grp;
+      float ls[4];
 #pragma unroll
-      for (int kc = 0; kc < 4; ++kc) {
-        uint32_t h[4], lo[4];
+      for (int hh = 0; hh < 2; ++hh) {  // keys 32 hh .. 32 hh + 31 -> P columns 16 hh ..
+        uint32_t h[16], lo[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float a = fast_exp2(fmaf(s[8 * kc + 2 * u], sl, nm));
-          const float e = fast_exp2(fmaf(s[8 * kc + 2 * u + 1], sl, nm));
-          l += a + e;
+        for (int u = 0; u < 16; ++u) {
+          const float a = fast_exp2(fmaf(s[32 * hh + 2 * u], sl, nm));
+          const float e = fast_exp2(fmaf(s[32 * hh + 2 * u + 1], sl, nm));
+          if ((u & 7) == 0) ls[2 * hh + (u >> 3)] = a + e;
+          else ls[2 * hh + (u >> 3)] += a + e;
           const __nv_bfloat162 hv = __floats2bfloat162_rn(a, e);
           const float2 hf2 = __bfloat1622float2(hv);
           const __nv_bfloat162 lv = __floats2bfloat162_rn(a - hf2.x, e - hf2.y);
           h[u] = *reinterpret_cast<const uint32_t*>(&hv);
           lo[u] = *reinterpret_cast<const uint32_t*>(&lv);
         }
-        const int col = 32 * hf + 8 * kc;
-        *reinterpret_cast<uint4*>(phi + tile_off(r, col, kKeysTC)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(plo + tile_off(r, col, kKeysTC)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        tc::st16_nowait(tP + 16 * hh, h);
+        tc::st16_nowait(tP + 32 + 16 * hh, lo);
       }
-      if (j * kKeysTC + kKeysTC > n_keys) {
+      tc::st_wait();
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      if (key0 + kKeysTC > n_keys) {
         // keys past the last one any row may see: pages not loaded, or page padding
         // that may hold anything (even NaN); zero them in V so that 0 * V stays 0
         // (after this tile's V copies have landed)
         ok = mbar_wait(&v_full[j % Sm::KST], (j / Sm::KST) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         uint8_t* vst = smem + Sm::v0 + (j % Sm::KST) * Sm::stage;
-        const int kz = n_keys - j * kKeysTC;
-        for (int idx = tid; idx < (kKeysTC - kz) * D; idx += kSoftThreads) {
+        const int kz = n_keys - key0;
+        for (int idx = r; idx < (kKeysTC - kz) * D; idx += kRowsTC) {
           const int key = kz + idx / D, d = idx % D;
           *reinterpret_cast<__nv_bfloat16*>(vst + (key >> 4) * Sm::kBlk + bf16_v_off(d, key & 15)) =
               __float2bfloat16_rn(0.f);
         }
       }
-      fence_proxy_async_smem();  // P (and zeroed V) become visible to the tensor cores
-      tc::fence_before_sync();
-      mbar_arrive(&p_full[x]);
+      fence_proxy_async_smem();  // zeroed V becomes visible to the tensor cores
+      tc::fence_before_sync();   // and so does P in TMEM
+      mbar_arrive(&p_full[grp]);
     }
-    if (ok) {
-      ok = mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1);
-      ok = __all_sync(0xffffffffu, ok);
+    if (ok && n_mine > 0) {  // this group's last P.V
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_done[grp], (n_mine - 1) & 1));
     }
-    // the row sum is split over the two halves (the max buffers are no longer in use
-    // once every thread has passed its last tile's P barrier wait)
-    if (ok) {
-      float* lx = xch + 2 * 2 * kRowsTC;
-      lx[hf * kRowsTC + r] = l;
-      mbar_arrive(&xbar[2]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&xbar[2], 0));
-      l += lx[(hf ^ 1) * kRowsTC + r];
-    }
+    tc::fence_before_sync();
+    // the two groups' (max, sum) of this row, exchanged once
+    float* xm = reinterpret_cast<float*>(smem + Sm::xch0);  // [group][row]
+    float* xl = xm + 2 * kRowsTC;
+    xm[grp * kRowsTC + r] = m_used;
+    xl[grp * kRowsTC + r] = l;
+    mbar_arrive(xfin);
+    ok = __all_sync(0xffffffffu, mbar_wait(xfin, 0) && ok);
     if (!ok) *abort_flag = 1;
     if (ok) {
       tc::fence_after_sync();
-      const float inv = 1.f / l;
+      const float m_o = xm[(grp ^ 1) * kRowsTC + r], l_o = xl[(grp ^ 1) * kRowsTC + r];
+      const float M = fmaxf(m_used, m_o);
+      const float a_me = m_used == -CUDART_INF_F ? 0.f : fast_exp2(m_used - M);
+      const float a_ot = m_o == -CUDART_INF_F ? 0.f : fast_exp2(m_o - M);
+      const float inv = 1.f / (l * a_me + l_o * a_ot);
+      const float wA = (grp == 0 ? a_me : a_ot) * inv, wB = (grp == 0 ? a_ot : a_me) * inv;
+      const bool hasB = n_tiles > 1;  // group 1's accumulator holds data
       float* dst = valid_row ? p.out + (static_cast<size_t>(q0 + rho / p.G) * p.Hq + g * p.G + rho % p.G) * D
                              : nullptr;
+      // group grp writes head_dim columns [grp D/2, (grp + 1) D/2) of its row
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        float o[32];
-        const int col = (D / 2) * hf + 32 * c;
-        tc::ld32(tmem + lane_base + col, o);
+        const int col = (D / 2) * grp + 32 * c;
+        float oa[32], ob[32];
+        tc::ld32(tmem + lane_base + col, oa);
+        if (hasB) {
+          tc::ld32(tmem + lane_base + D + col, ob);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) ob[u] = 0.f;
+        }
         if (dst) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(dst + col + k) =
-                make_float4(o[k] * inv, o[k + 1] * inv, o[k + 2] * inv, o[k + 3] * inv);
+          for (int u = 0; u < 32; u += 4)
+            *reinterpret_cast<float4*>(dst + col + u) =
+                make_float4(oa[u] * wA + ob[u] * wB, oa[u + 1] * wA + ob[u + 1] * wB,
+                            oa[u + 2] * wA + ob[u + 2] * wB, oa[u + 3] * wA + ob[u + 3] * wB);
         }
       }
     }
