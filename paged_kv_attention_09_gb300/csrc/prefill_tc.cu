@@ -67,18 +67,22 @@ struct TSmem {
   static constexpr int kBlk = kPage * D * 2;           // one BF16 page block (K or V)
   static constexpr int qTile = kRowsTC * D * 2;        // one BF16 query tile
   static constexpr int stage = kPagesTC * kBlk;        // the K (or V) blocks of one tile
-  static constexpr int KST = QSPLIT ? 2 : 3;           // stages of each of the K and V rings
+  static constexpr int KST = QSPLIT ? 2 : 3;           // stages of the V ring (one tile each)
+  static constexpr int KSP = 2;                        // stages of the K ring (a tile pair each)
+  static constexpr int kStage = 2 * stage;
   static constexpr int q0 = 0;
   static constexpr int k0 = q0 + (QSPLIT ? 2 : 1) * qTile;
-  static constexpr int v0 = k0 + KST * stage;
+  static constexpr int v0 = k0 + KSP * kStage;
   static constexpr int bar0 = v0 + KST * stage;
-  // barriers: k_full[3], k_empty[3], v_full[3], v_empty[3], then per softmax group
-  // s_full[2], s_free[2], p_full[2], o_done[2]; final MMA drain; the groups' final exchange
+  // barriers: k_full[2], k_empty[2] (+1 spare each), v_full[3], v_empty[3]; s_full,
+  // s_free (+1 spare each); per softmax group p_full[2], o_done[2]; final MMA drain; the
+  // groups' final exchange
   static constexpr int nbars = 22;
   static constexpr int misc0 = bar0 + nbars * 8;        // TMEM base address, flags
   static constexpr int xch0 = misc0 + 16;  // final exchange: max [2 groups][128], sum [2][128]
   static constexpr int total = xch0 + 2 * 2 * kRowsTC * 4;
-  // TMEM columns: O of group 0 [0, D), O of group 1 [D, 2D), S of group g at 2D + 64 g,
+  // TMEM columns: O of group 0 [0, D), O of group 1 [D, 2D), S of a tile pair at 2D
+  // (group g's 64 keys at 2D + 64 g),
   // P of group g at 2D + 128 + 64 g (BF16 pairs: high parts in the first 32 columns,
   // remainders in the next 32)
   static constexpr int sCol = 2 * D, pCol = 2 * D + 2 * kKeysTC;
@@ -147,9 +151,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < Sm::nbars; ++i) {
-      // s_free and p_full: one arrival per thread of the group; the exchange: every
+      // p_full: one arrival per thread of the group; s_free and the exchange: every
       // softmax thread; the rest: one arrival (or tcgen05.commit)
-      const int count = (i >= 14 && i < 18) ? kSoftThreads / 2
+      const int count = i == 14 ? kSoftThreads   // s_free: both groups read the pair
+                        : (i == 16 || i == 17) ? kSoftThreads / 2
                         : i == 21 ? kSoftThreads
                         : i == 20 ? 2  // the final drain: one commit from each MMA issuer
                         : 1;
@@ -210,31 +215,35 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     if (lane == 0) {
       const bool isK = warp == kSoftWarps + 1;
       const uint64_t pol = l2_evict_last_policy();  // every row tile of the group rereads them
-      constexpr int KST = Sm::KST;
+      // K moves a tile pair (8 pages) per stage, V one tile (4 pages) per stage
+      const int RS = isK ? Sm::KSP : Sm::KST;
+      const int per = isK ? 2 * kPagesTC : kPagesTC;
+      const int sbytes = isK ? Sm::kStage : Sm::stage;
+      const int n_units = isK ? (n_tiles + 1) / 2 : n_tiles;
       uint64_t* full = isK ? k_full : v_full;
       uint64_t* empty = isK ? k_empty : v_empty;
       const uint8_t* src = isK ? p.k : p.v;
       uint8_t* ring = smem + (isK ? Sm::k0 : Sm::v0);
       int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % KST, use = j / KST;
-        const int np = min(kPagesTC, n_pages - j * kPagesTC);
-        if (j >= KST && !mbar_wait(&empty[st], (use - 1) & 1)) { *abort_flag = 1; break; }
+      for (int j = 0; j < n_units; ++j) {
+        const int st = j % RS, use = j / RS;
+        const int np = min(per, n_pages - j * per);
+        if (j >= RS && !mbar_wait(&empty[st], (use - 1) & 1)) { *abort_flag = 1; break; }
         if (*abort_flag) break;
         mbar_arrive_expect_tx(&full[st], np * Sm::kBlk);
         for (int q = 0; q < np; ++q) {
-          const size_t blk = static_cast<size_t>(bt[j * kPagesTC + q]) * p.Hkv + g;
-          bulk_g2s(ring + st * Sm::stage + q * Sm::kBlk, src + blk * Sm::kBlk, Sm::kBlk, &full[st], pol);
+          const size_t blk = static_cast<size_t>(bt[j * per + q]) * p.Hkv + g;
+          bulk_g2s(ring + st * sbytes + q * Sm::kBlk, src + blk * Sm::kBlk, Sm::kBlk, &full[st], pol);
         }
         issued = j + 1;
       }
-      // leave nothing in flight: the copies of the last issued tiles have landed
-      for (int j = max(0, issued - KST); j < issued; ++j) (void)mbar_wait(&full[j % KST], (j / KST) & 1);
+      // leave nothing in flight: the copies of the last issued stages have landed
+      for (int j = max(0, issued - RS); j < issued; ++j) (void)mbar_wait(&full[j % RS], (j / RS) & 1);
     }
   } else if (n_tiles > 0 && (warp == kSoftWarps || warp == kSoftWarps + 3)) {
     // ---------------------------------------------------------------- MMA issuers
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16_f32(kRowsTC, kKeysTC);
+      constexpr uint32_t idS = tc::idesc_bf16_f32(kRowsTC, 2 * kKeysTC);  // a tile pair
       constexpr uint32_t idO = tc::idesc_bf16_f32(kRowsTC, D);
       constexpr uint32_t sboQK = (D / 8) * 128;  // 8-row groups of Q and of K
       const uint32_t qhi = sbase + Sm::q0, qlo = sbase + Sm::q0 + Sm::qTile;
@@ -244,23 +253,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const uint64_t dQhi = tc::smem_desc(qhi, 128, sboQK), dQlo = tc::smem_desc(qlo, 128, sboQK);
       const uint64_t dK0 = tc::smem_desc(sbase + Sm::k0, 128, sboQK);
       const uint64_t dV0 = tc::smem_desc(sbase + Sm::v0, 128, 256);
-      // S_j = Q K_j^T into the score buffer of group j & 1, once that group has read S_{j-2}
-      auto issue_s = [&](int j) -> bool {
-        const int x = j & 1;
-        if (!mbar_wait(&k_full[j % KST], (j / KST) & 1)) return false;
-        if (j >= 2 && !mbar_wait(&s_free[x], ((j - 2) >> 1) & 1)) return false;
+      // S of tile pair pr (tiles 2 pr and 2 pr + 1: 128 keys, one N=128 MMA per k-step)
+      // into the score buffer, once both groups have read the previous pair's scores
+      constexpr int KSP = Sm::KSP;
+      auto issue_s = [&](int pr) -> bool {
+        if (!mbar_wait(&k_full[pr % KSP], (pr / KSP) & 1)) return false;
+        if (pr >= 1 && !mbar_wait(&s_free[0], (pr - 1) & 1)) return false;
         if (*abort_flag) return false;
         tc::fence_after_sync();
-        const uint64_t dK = tc::desc_add(dK0, (j % KST) * Sm::stage);
-        const uint32_t tS = tmem + Sm::sCol + kKeysTC * x;
+        const uint64_t dK = tc::desc_add(dK0, (pr % KSP) * Sm::kStage);
+        const uint32_t tS = tmem + Sm::sCol;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t bd = tc::desc_add(dK, ks * 256);
           tc::mma_bf16(tS, tc::desc_add(dQhi, ks * 256), bd, idS, ks > 0);
           if constexpr (QSPLIT) tc::mma_bf16(tS, tc::desc_add(dQlo, ks * 256), bd, idS, true);
         }
-        tc::commit(&s_full[x]);
-        tc::commit(&k_empty[j % KST]);
+        tc::commit(&s_full[0]);
+        tc::commit(&k_empty[pr % KSP]);
         return true;
       };
       // O_y += P_i V_i into the accumulator of group y = i & 1 (its first tile starts it)
@@ -282,11 +292,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         tc::commit(&v_empty[i % KST]);
         return true;
       };
-      // Warp 8 runs ahead through the score tiles (bounded by the two score buffers);
+      // Warp 8 runs ahead through the tile pairs (bounded by the one score buffer);
       // warp 11 follows the softmax groups with the P.V products.
       bool ok = true;
       if (warp == kSoftWarps) {
-        for (int j = 0; j < n_tiles && ok; ++j) ok = issue_s(j);
+        for (int pr = 0; pr < (n_tiles + 1) / 2 && ok; ++pr) ok = issue_s(pr);
       } else {
         for (int i = 0; i < n_tiles && ok; ++i) ok = issue_pv(i);
       }
@@ -309,7 +319,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     int n_mine = 0;  // tiles this group has finished
     for (int j = grp; j < n_tiles; j += 2, ++n_mine) {
       const int k = j >> 1;  // this group's k-th tile
-      ok = mbar_wait(&s_full[grp], k & 1) && !*abort_flag;
+      ok = mbar_wait(&s_full[0], k & 1) && !*abort_flag;  // the scores of pair k
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc::fence_after_sync();
       float s[64];
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         for (int u = 0; u < 32; ++u) { s[u] = t0[u]; s[32 + u] = t1[u]; }
       }
       tc::fence_before_sync();
-      mbar_arrive(&s_free[grp]);
+      mbar_arrive(&s_free[0]);
       const int key0 = j * kKeysTC;
       // raw scores; the scale (> 0) is applied inside the exponent with one FMA
       if (key0 + kKeysTC - 1 > p_first || key0 + kKeysTC > n_keys) {
