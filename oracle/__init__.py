@@ -58,6 +58,13 @@ def _bind(lib):
     lib.oracle_decode.restype = i
     lib.oracle_prefill.argtypes = [i, i, i, i, i, p, p, p, p, p, i, i, i, p, p, i, p, d, p, i, i]
     lib.oracle_prefill.restype = i
+    lib.oracle_rope_f64.argtypes = [p, p, i, i, d]
+    lib.oracle_rope_f64.restype = None
+    lib.oracle_rope_f32.argtypes = [p, p, i, i, d]
+    lib.oracle_rope_f32.restype = None
+    lib.oracle_decode_step.argtypes = [i, i, i, i, i, p, p, p, p, p, i, p, p, i, p, p, d, i, i,
+                                       p, i, p, d, p, i, i]
+    lib.oracle_decode_step.restype = i
     return lib
 
 
@@ -190,6 +197,51 @@ def prefill(cache: HostCache, q, q_dtype, q_start_loc, block_tables, context_len
         with ThreadPoolExecutor(n) as ex:
             bad = sum(ex.map(run, seqs))
     prefill.last_bad = bad
+    return out
+
+
+def rope_f64(x, pos, theta):
+    """Rotary embedding of one row in double precision (half-split pairs)."""
+    x = _c(x, np.float64)
+    y = np.empty_like(x)
+    load().oracle_rope_f64(_ptr(x), _ptr(y), x.shape[0], int(pos), float(theta))
+    return y
+
+
+def rope_f32(x, pos, theta):
+    """Rotary embedding of one float32 row in the fixed float operation order used for
+    keys that are about to be stored."""
+    x = _c(x, np.float32)
+    y = np.empty_like(x)
+    load().oracle_rope_f32(_ptr(x), _ptr(y), x.shape[0], int(pos), float(theta))
+    return y
+
+
+def decode_step(cache: HostCache, q, q_dtype, k_new, v_new, new_dtype, slot_mapping,
+                positions, theta, block_tables, context_lens, scale, *, seqs=None):
+    """One decode step (rotate, store the new row, attend); mutates ``cache``.
+
+    ``positions`` None: no rotation.  Returns float64 [B, Hq, D]; sequences not listed in
+    ``seqs`` are neither stored nor computed (NaN rows).
+    """
+    q = _c(q, _REAL[q_dtype])
+    k_new = _c(k_new, _REAL[new_dtype])
+    v_new = _c(v_new, _REAL[new_dtype])
+    sm = _c(slot_mapping, np.int32)
+    pos = None if positions is None else _c(positions, np.int32)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    out = np.full((B, Hq, D), np.nan, np.float64)
+    lib = load()
+    seqs = list(range(B)) if seqs is None else [int(s) for s in seqs]
+    bad = 0
+    for b in seqs:
+        bad += lib.oracle_decode_step(*cache.args(), _ptr(q), q_dtype, _ptr(k_new), _ptr(v_new),
+                                      new_dtype, _ptr(sm), _ptr(pos), float(theta), B, Hq,
+                                      _ptr(bt), bt.shape[1], _ptr(cl), float(scale), _ptr(out),
+                                      b, b + 1)
+    decode_step.last_bad = bad
     return out
 
 

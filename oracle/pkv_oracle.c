@@ -36,6 +36,10 @@
  * (IEEE division, round-half-to-even), compiled with -ffp-contract=off and without
  * fast-math, so the stored codes are a function of the inputs alone.
  *
+ * One decode step (rotate the new query and key, store the new row, attend) composes
+ * these: "tinyloop Current Status", model architecture support table (RoPE with a
+ * configurable theta); the rotation convention is a reading (half-split pairs).
+ *
  * Parity pins: every function here is pinned by tests that do not re-type it (dense
  * brute force against a library attention, closed forms, permutation invariance,
  * causality, an exhaustive nearest-code search for the quantiser, and the library
@@ -204,6 +208,64 @@ int oracle_append(int kv_dtype, int num_pages, int P, int Hkv, int D, void* k_ca
   return bad;
 }
 
+/* ---------------------------------------------------------------- rotary embedding */
+
+/*
+ * Rotary position embedding ("tinyloop Current Status", model architecture support
+ * table: RoPE in all forward paths, configurable theta).  The pages give no formula;
+ * the reading taken is the half-split form of the Llama / Qwen families: element i and
+ * element i + D/2 form a pair rotated by the angle
+ *     a_i = pos * theta^(-2i/D),   i = 0 .. D/2 - 1,
+ *     y_i = x_i cos a_i - x_{i+D/2} sin a_i,   y_{i+D/2} = x_{i+D/2} cos a_i + x_i sin a_i.
+ * Two precisions: queries in double (the definition), and keys that are about to be
+ * stored in float with a fixed operation order (angle in double, cos and sin rounded to
+ * float, then one float product and one fused multiply-add per output), because the
+ * stored bits (BF16 rounding, INT8 codes) are decided by that float arithmetic.
+ */
+static double rope_angle(int i, int D, int pos, double theta) {
+#if ORACLE_MUTANT == 10 /* rotation the wrong way */
+  return -(double)pos * pow(theta, -2.0 * (double)i / (double)D);
+#else
+  return (double)pos * pow(theta, -2.0 * (double)i / (double)D);
+#endif
+}
+
+static int rope_partner(int i, int D) {
+#if ORACLE_MUTANT == 9 /* adjacent pairs (2i, 2i+1) instead of (i, i + D/2) */
+  (void)D;
+  return 2 * i + 1;
+#else
+  return i + D / 2;
+#endif
+}
+static int rope_first(int i) {
+#if ORACLE_MUTANT == 9
+  return 2 * i;
+#else
+  return i;
+#endif
+}
+
+void oracle_rope_f64(const double* x, double* y, int D, int pos, double theta) {
+  for (int i = 0; i < D / 2; ++i) {
+    const double a = rope_angle(i, D, pos, theta), c = cos(a), s = sin(a);
+    const int u = rope_first(i), v = rope_partner(i, D);
+    y[u] = x[u] * c - x[v] * s;
+    y[v] = x[v] * c + x[u] * s;
+  }
+}
+
+void oracle_rope_f32(const float* x, float* y, int D, int pos, double theta) {
+  for (int i = 0; i < D / 2; ++i) {
+    const double a = rope_angle(i, D, pos, theta);
+    const float c = (float)cos(a), s = (float)sin(a);
+    const int u = rope_first(i), v = rope_partner(i, D);
+    const float t = x[v] * s, w = x[u] * s;
+    y[u] = fmaf(x[u], c, -t);
+    y[v] = fmaf(x[v], c, w);
+  }
+}
+
 /* ---------------------------------------------------------------- attention core */
 
 /*
@@ -295,6 +357,77 @@ int oracle_decode(int kv_dtype, int num_pages, int P, int Hkv, int D, const void
   }
   free(qd);
   free(scores);
+  return bad;
+}
+
+/*
+ * One decode step: for each sequence b whose slot_mapping[b] is >= 0, the new token's
+ * key row k_new[b] ([B][Hkv][D], float32 or bfloat16) is rotated (float form) at
+ * positions[b] and stored with v_new[b] at slot_mapping[b] exactly as oracle_append
+ * stores rows; then every query row q[b] is rotated (double form) at positions[b] and
+ * attends over context_lens[b] tokens as in oracle_decode.  positions == NULL means no
+ * rotation.  The new token must sit at logical position context_lens[b] - 1: a slot that
+ * is not that position's slot (or a length below 1) gives NaN rows for b and nothing is
+ * stored.  slot_mapping[b] < 0: nothing is stored and b attends over the cache as is.
+ * Sequences b_begin .. b_end - 1 only.  Returns the number of sequences given NaN rows.
+ */
+int oracle_decode_step(int kv_dtype, int num_pages, int P, int Hkv, int D, void* k_cache,
+                       void* v_cache, float* k_scale, float* v_scale, const void* q,
+                       int q_dtype, const void* k_new, const void* v_new, int new_dtype,
+                       const int32_t* slot_mapping, const int32_t* positions, double theta,
+                       int B, int Hq, const int32_t* block_tables, int max_blocks,
+                       const int32_t* context_lens, double scale, double* out, int b_begin,
+                       int b_end) {
+  int G = Hq / Hkv, bad = 0;
+  int max_len = max_blocks * P;
+  double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+  double* qr = (double*)malloc(sizeof(double) * (size_t)D);
+  double* scores = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+  float* xk = (float*)malloc(sizeof(float) * (size_t)Hkv * D);
+  float* xv = (float*)malloc(sizeof(float) * (size_t)Hkv * D);
+  float* row = (float*)malloc(sizeof(float) * (size_t)D);
+  if (b_end > B) b_end = B;
+  for (int b = b_begin; b < b_end; ++b) {
+    int L = context_lens[b];
+    const int32_t* bt = block_tables + (size_t)b * max_blocks;
+    int ok = (L >= 0 && L <= max_len);
+    for (int j = 0; ok && j < (L + P - 1) / P; ++j)
+      if (bt[j] < 0 || bt[j] >= num_pages) ok = 0;
+    const int slot = slot_mapping[b];
+    if (ok && slot >= 0 && (L < 1 || slot != bt[(L - 1) / P] * P + (L - 1) % P)) ok = 0;
+    const int pos = positions ? positions[b] : 0;
+    if (ok && slot >= 0) {
+      /* the new row, rotated in float, stored through the append definition */
+      for (int h = 0; h < Hkv; ++h) {
+        for (int d = 0; d < D; ++d) row[d] = read_real_f(k_new, new_dtype, ((size_t)b * Hkv + h) * D + d);
+        if (positions) oracle_rope_f32(row, xk + (size_t)h * D, D, pos, theta);
+        else for (int d = 0; d < D; ++d) xk[(size_t)h * D + d] = row[d];
+        for (int d = 0; d < D; ++d) xv[(size_t)h * D + d] = read_real_f(v_new, new_dtype, ((size_t)b * Hkv + h) * D + d);
+      }
+      int32_t one_slot = slot;
+      oracle_append(kv_dtype, num_pages, P, Hkv, D, k_cache, v_cache, k_scale, v_scale, xk,
+                    xv, 0 /* float32 rows */, &one_slot, 1);
+    }
+    for (int h = 0; h < Hq; ++h) {
+      double* o = out + ((size_t)b * Hq + h) * D;
+      if (!ok) {
+        for (int d = 0; d < D; ++d) o[d] = NAN;
+        continue;
+      }
+      for (int d = 0; d < D; ++d) qd[d] = read_real(q, q_dtype, ((size_t)b * Hq + h) * D + d);
+      if (positions) oracle_rope_f64(qd, qr, D, pos, theta);
+      else for (int d = 0; d < D; ++d) qr[d] = qd[d];
+      attend_one(qr, L, bt, h / G, k_cache, v_cache, k_scale, v_scale, kv_dtype, Hkv, P, D,
+                 scale, scores, o);
+    }
+    if (!ok) ++bad;
+  }
+  free(qd);
+  free(qr);
+  free(scores);
+  free(xk);
+  free(xv);
+  free(row);
   return bad;
 }
 

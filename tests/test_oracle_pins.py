@@ -424,12 +424,135 @@ def test_invalid_inputs_give_nan_rows_and_counts():
 
 # --------------------------------------------------------------------------- planted mistakes
 
+# --------------------------------------------------------------------------- rotary embedding
+# "tinyloop Current Status", model architecture support table (RoPE, configurable theta);
+# the half-split pairing (i, i + D/2) is the reading taken.
+
+def rope_complex(x, pos, theta):
+    """The rotation written as complex multiplication: pair (x_i, x_{i+D/2}) is the
+    complex number x_i + 1j x_{i+D/2}, multiplied by exp(1j * pos * theta^(-2i/D))."""
+    x = np.asarray(x, np.float64)
+    D = x.shape[0]
+    h = D // 2
+    z = (x[:h] + 1j * x[h:]) * np.exp(1j * pos * theta ** (-2.0 * np.arange(h) / D))
+    return np.concatenate([z.real, z.imag])
+
+
+def check_rope():
+    rng = np.random.default_rng(11)
+    for D in (64, 128):
+        for pos in (0, 1, 37, 4095, 32767):
+            for theta in (10000.0, 1.0e6):
+                x = rng.standard_normal(D)
+                ref = rope_complex(x, pos, theta)
+                if np.max(np.abs(oracle.rope_f64(x, pos, theta) - ref)) > 1e-10 * np.abs(x).max():
+                    return False
+                xf = x.astype(np.float32)
+                reff = rope_complex(xf, pos, theta)
+                if np.max(np.abs(oracle.rope_f32(xf, pos, theta) - reff)) > 1e-6 * np.abs(x).max():
+                    return False
+    x = rng.standard_normal(64).astype(np.float32)
+    if not np.array_equal(oracle.rope_f32(x, 0, 1.0e4), x):  # position 0: identity
+        return False
+    # relative positions: <R(q, m), R(k, n)> depends on m - n only
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    a = oracle.rope_f64(q, 100, 1.0e4) @ oracle.rope_f64(k, 40, 1.0e4)
+    b = oracle.rope_f64(q, 1060, 1.0e4) @ oracle.rope_f64(k, 1000, 1.0e4)
+    return abs(a - b) <= 1e-9 * (1 + abs(a))
+
+
+def test_rope_is_the_complex_rotation():
+    assert check_rope()
+
+
+# --------------------------------------------------------------------------- decode step
+
+def step_inputs(wl):
+    """The newest token of every decode sequence: its source rows, slot and position."""
+    batch = wl.batches[0]
+    rows = wl.step_rows[:batch.num_seqs]
+    return (wl.k_src[rows], wl.v_src[rows], wl.slots[rows].astype(np.int32),
+            (batch.context_lens - 1).astype(np.int32))
+
+
+def copy_cache(c):
+    d = HostCache(c.kv_dtype, c.num_pages, c.page_size, c.num_kv_heads, c.head_dim)
+    d.k[...] = c.k
+    d.v[...] = c.v
+    if c.k_scale is not None:
+        d.k_scale[...] = c.k_scale
+        d.v_scale[...] = c.v_scale
+    return d
+
+
+def same_cache(a, b):
+    ok = np.array_equal(a.k, b.k) and np.array_equal(a.v, b.v)
+    if a.k_scale is not None:
+        ok = ok and np.array_equal(a.k_scale, b.k_scale) and np.array_equal(a.v_scale, b.v_scale)
+    return ok
+
+
+def rows_f32(x, dtype):
+    return bf16_to_f32(x) if dtype == BF16 else np.asarray(x, np.float32)
+
+
+def check_decode_step():
+    theta = 1.0e4
+    for i, (kv, qd, Hq, Hkv, D, lens) in enumerate(CASES):
+        wl = W.small_workload(400 + i, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                              kv_dtype=kv, q_dtype=qd, decode_lens=lens)
+        batch = wl.batches[0]
+        hist = oracle.cache_from_workload(wl, rows=wl.history_rows)
+        k_new, v_new, slots, pos = step_inputs(wl)
+        args = (batch.block_tables, batch.context_lens, wl.scale)
+        # no rotation: exactly append, then decode
+        c1, c2 = copy_cache(hist), copy_cache(hist)
+        got = oracle.decode_step(c1, batch.q, qd, k_new, v_new, wl.new_dtype, slots, None,
+                                 theta, *args)
+        oracle.append(c2, k_new, v_new, wl.new_dtype, slots)
+        if not (same_cache(c1, c2) and np.array_equal(got, oracle.decode(c2, batch.q, qd, *args))):
+            return False
+        # rotation: the stored keys are the float-form rotation of the inputs, and the output
+        # is dense attention of the double-form rotated queries over the reassembled cache
+        c3, c4 = copy_cache(hist), copy_cache(hist)
+        got = oracle.decode_step(c3, batch.q, qd, k_new, v_new, wl.new_dtype, slots, pos,
+                                 theta, *args)
+        kf = rows_f32(k_new, wl.new_dtype)
+        krot = np.stack([[oracle.rope_f32(kf[b, h], pos[b], theta) for h in range(Hkv)]
+                         for b in range(batch.num_seqs)])
+        oracle.append(c4, krot, rows_f32(v_new, wl.new_dtype), F32, slots)
+        if not same_cache(c3, c4):
+            return False
+        G = Hq // Hkv
+        q = q_f64(batch.q, qd)
+        for b in range(batch.num_seqs):
+            L = int(batch.context_lens[b])
+            for g in range(Hkv):
+                k, v = logical_kv(c4, batch.block_tables[b], L, g)
+                qr = np.stack([oracle.rope_f64(q[b, h], pos[b], theta) for h in range(g * G, (g + 1) * G)])
+                if np.max(np.abs(got[b, g * G:(g + 1) * G] - sdpa(qr, k, v, wl.scale))) > 1e-12:
+                    return False
+        # a slot that is not position L - 1's slot: NaN rows, nothing stored
+        c5 = copy_cache(hist)
+        bad = slots.copy()
+        bad[0] = (bad[0] + 1) % (wl.num_pages * P)
+        got = oracle.decode_step(c5, batch.q, qd, k_new, v_new, wl.new_dtype, bad, pos, theta,
+                                 *args, seqs=[0])
+        if not (np.all(np.isnan(got[0])) and oracle.decode_step.last_bad == 1 and same_cache(c5, hist)):
+            return False
+    return True
+
+
+def test_decode_step_is_rotate_store_attend():
+    assert check_decode_step()
+
+
 PINS = [check_bf16_rounding, check_quantiser, check_decode_bruteforce,
         check_prefill_bruteforce, check_closed_forms, check_page_permutation_invariance,
-        check_gqa_equals_replicated_mha, check_causality]
+        check_gqa_equals_replicated_mha, check_causality, check_rope, check_decode_step]
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
 def test_planted_mistake_is_caught(mutant, monkeypatch):
     path = oracle.build(defines=[f"ORACLE_MUTANT={mutant}"], name=f"liboracle_m{mutant}.so")
     monkeypatch.setattr(oracle, "_lib", oracle.load(path))
