@@ -6,6 +6,8 @@
  *   pkv_append              write new tokens' K/V rows into cache pages via a slot map
  *   pkv_decode_attn         one query token per sequence against its paged context
  *   pkv_prefill_chunk_attn  a causal chunk of query tokens against its paged context
+ *   pkv_decode_step         one launch for a whole decode step: rotary embedding of the
+ *                           new query and key, append of the new K/V row, attention
  *
  * Sources (page title, section):
  *   "Tiny-LLM-Inference Project_Status", feature list and dtype contract: paged KV
@@ -112,8 +114,8 @@ pkv_status pkv_append(const pkv_cache* cache, const void* k_new, const void* v_n
                       int32_t* dev_status, void* stream);
 
 /*
- * Scratch bytes pkv_decode_attn needs for this shape on the current device (host
- * call, no launch).  The split of long contexts across thread blocks is a fixed
+ * Scratch bytes pkv_decode_attn (and pkv_decode_step) needs for this shape on the
+ * current device (host call, no launch).  The split of long contexts across thread blocks is a fixed
  * function of (shape, device SM count, pkv_set_decode_chunk_pages), so equal
  * arguments give bit-identical results.  Writes the size to *bytes (0 is possible).
  */
@@ -141,6 +143,41 @@ pkv_status pkv_decode_attn(const pkv_cache* cache, const void* q, int32_t q_dtyp
                            int32_t max_blocks_per_seq, const int32_t* context_lens,
                            float scale, float* out, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, void* stream);
+
+/*
+ * One decode step in one launch ("tinyloop Current Status", model architecture support
+ * table: RoPE in every forward path with a configurable theta; KV cache modes table:
+ * 16-token pages, INT8 KV).  For every sequence b it computes exactly
+ *     rotate q[b] and k_new[b] at positions[b];  pkv_append(k_new[b], v_new[b] at
+ *     slot_mapping[b]);  pkv_decode_attn over context_lens[b] tokens,
+ * with the new token's K/V used straight from registers by the blocks that need it.
+ *   q              [num_seqs][num_q_heads][head_dim], PKV_F32 or PKV_BF16 (as decode).
+ *   k_new, v_new   [num_seqs][num_kv_heads][head_dim], new_dtype PKV_F32 or PKV_BF16:
+ *                  the new token's key (before rotation) and value; stored as
+ *                  pkv_append stores rows (BF16 rounding, INT8 codes and scale).
+ *   slot_mapping   int32 [num_seqs]: the new token's slot, which must be the slot of
+ *                  logical position context_lens[b] - 1 (else PKV_DEV_BAD_SLOT and NaN
+ *                  rows for b, nothing stored); < 0: no new token, b attends over the
+ *                  cache as it is.  A page being appended to must not be read by another
+ *                  sequence of the same call.
+ *   positions      int32 [num_seqs] rotation position of each new token, or NULL for no
+ *                  rotation.  Rotation: elements i and i + head_dim/2 form a pair turned
+ *                  by the angle positions[b] * rope_theta^(-2i/head_dim) (the half-split
+ *                  convention); angles, cos and sin in double, rounded to float; the key
+ *                  is rotated in float as y_i = fma(x_i, c, -(x_{i+D/2} s)),
+ *                  y_{i+D/2} = fma(x_{i+D/2}, c, x_i s) (its bits decide the stored
+ *                  values); rope_theta must exceed 1 when positions is not NULL.
+ *   Other arguments and the workspace are those of pkv_decode_attn (the size returned
+ *   by pkv_decode_workspace_size covers both calls).
+ */
+pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                           const void* k_new, const void* v_new, int32_t new_dtype,
+                           const int32_t* slot_mapping, const int32_t* positions,
+                           double rope_theta, int32_t num_seqs, int32_t num_q_heads,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, float scale, float* out,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream);
 
 /*
  * Scratch bytes pkv_prefill_chunk_attn needs (host call, no launch); see above.

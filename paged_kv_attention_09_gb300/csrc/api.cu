@@ -84,11 +84,14 @@ pkv_status pkv_decode_workspace_size(const pkv_cache* cache, int32_t num_seqs,
   if (s != PKV_OK) return s;
   int dev = 0;
   if ((s = current_device(&dev)) != PKV_OK) return s;
-  pkv::DecodePlan plan{};
+  // one size for both pkv_decode_attn and pkv_decode_step (their plans may differ)
+  pkv::DecodePlan plan{}, plan_step{};
   if (!pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, PKV_F32, dev,
-                        g_chunk_override.load(), &plan))
+                        g_chunk_override.load(), &plan) ||
+      !pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, PKV_F32, dev,
+                        g_chunk_override.load(), &plan_step, true))
     return PKV_ERR_DEVICE;
-  *bytes = plan.ws_bytes;
+  *bytes = plan.ws_bytes > plan_step.ws_bytes ? plan.ws_bytes : plan_step.ws_bytes;
   return PKV_OK;
 }
 
@@ -132,6 +135,69 @@ pkv_status pkv_decode_attn(const pkv_cache* cache, const void* q, int32_t q_dtyp
   a.out = out;
   a.ws = workspace;
   a.dev_status = dev_status;
+  const cudaError_t e = pkv::launch_decode(a, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                           const void* k_new, const void* v_new, int32_t new_dtype,
+                           const int32_t* slot_mapping, const int32_t* positions,
+                           double rope_theta, int32_t num_seqs, int32_t num_q_heads,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, float scale, float* out,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream) {
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
+  if (s != PKV_OK) return s;
+  if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (new_dtype != PKV_F32 && new_dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (positions && !(rope_theta > 1.0)) return PKV_ERR_SHAPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_new || !v_new || !slot_mapping || !block_tables || !context_lens || !out)
+    return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned4(block_tables) || !aligned4(context_lens) || !aligned4(slot_mapping) ||
+      (positions && !aligned4(positions)))
+    return PKV_ERR_ALIGN;
+  if (dev_status && !aligned4(dev_status)) return PKV_ERR_ALIGN;
+  int dev = 0;
+  if ((s = current_device(&dev)) != PKV_OK) return s;
+  pkv::DecodePlan plan{};
+  if (!pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, q_dtype, dev,
+                        g_chunk_override.load(), &plan, true))
+    return PKV_ERR_DEVICE;
+  if (static_cast<long long>(cache->num_kv_heads) * plan.head_groups > 65535)
+    return PKV_ERR_UNSUPPORTED;
+  if (plan.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.ws_bytes) return PKV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PKV_ERR_ALIGN;
+  }
+  pkv::DecodeArgs a{};
+  a.c = view(cache);
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.B = num_seqs;
+  a.Hq = num_q_heads;
+  a.MB = max_blocks_per_seq;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.scale = scale;
+  a.out = out;
+  a.ws = workspace;
+  a.dev_status = dev_status;
+  a.step = true;
+  a.kw = cache->k_cache;
+  a.vw = cache->v_cache;
+  a.ksw = cache->k_scale;
+  a.vsw = cache->v_scale;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.new_dtype = new_dtype;
+  a.slots = slot_mapping;
+  a.positions = positions;
+  a.rope_theta = rope_theta;
   const cudaError_t e = pkv::launch_decode(a, plan, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }

@@ -2,13 +2,12 @@
 //
 // "Tiny-LLM-Inference Project_Status" (feature list: paged KV cache; dtype contract:
 // FP32 or BF16 KV) and "tinyloop Current Status" (KV cache modes table: INT8 KV cache).
-// One warp per (token, kv head) writes both the K row and the V column of that slot.
-// INT8 rows are quantised symmetrically: s = max|x| / 127 with IEEE division and
-// code = clamp(rint(x / s), -127, 127) with round-half-to-even, so the stored codes
-// are exactly reproducible by any IEEE float implementation.
+// One warp per (token, kv head) writes both the K row and the V column of that slot;
+// INT8 rows go through the shared quantiser (kvrow.cuh).
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "kvrow.cuh"
 
 namespace pkv {
 namespace {
@@ -56,19 +55,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int e = 0; e < E; ++e) x[e] = load_src<NEW_DT>(src, src_row + lane * E + e);
 
     if constexpr (KV_DT == kINT8) {
-      float amax = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float s = __fdiv_rn(amax, 127.0f);
       int8_t code[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        float r = 0.f;
-        if (s != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[e], s)), -127.f), 127.f);
-        code[e] = static_cast<int8_t>(static_cast<int>(r));
-      }
+      const float s = quantize_row_int8<E>(x, code);
       int8_t* dst = static_cast<int8_t*>(which ? v_cache : k_cache);
       if (which == 0) {
 #pragma unroll

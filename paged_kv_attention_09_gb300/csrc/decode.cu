@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "kvrow.cuh"
 #include "ptx.cuh"
 
 namespace pkv {
@@ -64,6 +65,17 @@ struct DParams {
   int32_t* dev_status;
   int q_dtype, Hkv, Hq, G, hpc, head_groups, MB, B, num_pages, chunk;
   float scale_log2;
+  // the fused decode step (STEP kernels only)
+  uint8_t* kw;
+  uint8_t* vw;
+  float* ksw;
+  float* vsw;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* slots;
+  const int32_t* positions;
+  double rope_theta;
+  int new_dtype;
 };
 
 template <int KVT>
@@ -108,7 +120,7 @@ struct Layout {
   static constexpr int stageBytes = PPI * pageBytes;
 };
 
-template <int KVT, int D>
+template <int KVT, int D, bool STEP = false>
 struct Smem {
   using Lo = Layout<KVT, D>;
   static constexpr int kW = Tune<KVT, D>::W;
@@ -121,7 +133,13 @@ struct Smem {
   // built once by warp 0 and read by every warp
   static constexpr int aux = KVT == kINT8 ? (D / 16) * 32 * 16 + 2 * kMaxHeads * 4 : 0;
   static constexpr int bars = kW * Lo::S * 8;
-  static constexpr int total = big + probs + aux + bars;
+  // fused step: the block's rotated query rows (float), cos and sin of the rotation
+  // angles, the new token's K and V rows in storage format (+ their scales)
+  static constexpr int stepQ = STEP ? kMaxHeads * D * 4 : 0;
+  static constexpr int stepRope = STEP ? D * 4 : 0;
+  static constexpr int stepRow = STEP ? 2 * (D * ElemSize<KVT>::value + 16) : 0;
+  static constexpr int step0 = big + probs + aux + bars;
+  static constexpr int total = step0 + stepQ + stepRope + stepRow;
 };
 
 __device__ __forceinline__ float4 load_q4(const void* q, int q_dtype, size_t i) {
@@ -179,7 +197,9 @@ struct F32Warp {
   // (loading the queries before the first copy measured slower here: they are only
   // consumed by the first page anyway)
   __device__ void prefetch(const DParams&, int, int, int, int, int) {}
-  __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t*, int) {
+  // sq: the block's query rows as float in shared memory (the fused step), else nullptr
+  __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t*, int,
+                       const float* sq) {
     const int c8 = lane & 7;
 #pragma unroll
     for (int h = 0; h < HM; ++h) {
@@ -188,9 +208,10 @@ struct F32Warp {
 #pragma unroll
       for (int i = 0; i < NC; ++i) {
         o[h][i] = 0.f;
-        q[h][i] = h < nh ? load_q4(p.q, p.q_dtype,
-                                   (static_cast<size_t>(b) * p.Hq + h0 + h) * D + (c8 + 8 * i) * 4)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        q[h][i] = h >= nh ? make_float4(0.f, 0.f, 0.f, 0.f)
+                  : sq    ? *reinterpret_cast<const float4*>(sq + h * D + (c8 + 8 * i) * 4)
+                          : load_q4(p.q, p.q_dtype,
+                                    (static_cast<size_t>(b) * p.Hq + h0 + h) * D + (c8 + 8 * i) * 4);
       }
     }
   }
@@ -335,13 +356,18 @@ struct Bf16Warp {
       }
     }
   }
-  __device__ void init(const DParams& p, int, int, int, int, uint8_t*, int) {
+  __device__ void init(const DParams& p, int, int, int nh, int lane, uint8_t*, int,
+                       const float* sq) {
+    const int r = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float2 v;
-        if (p.q_dtype == kBF16) {
+        if (sq) {  // the fused step's rotated query rows
+          v = r < nh ? *reinterpret_cast<const float2*>(sq + r * D + 16 * ks + 8 * half + 2 * c)
+                     : make_float2(0.f, 0.f);
+        } else if (p.q_dtype == kBF16) {
           v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qa[ks][2 * half]));
         } else {
           v = make_float2(__uint_as_float(qa[ks][2 * half]), __uint_as_float(qa[ks][2 * half + 1]));
@@ -465,7 +491,8 @@ struct Int8Warp {
 
   // Warp 0 builds the fragments and the per-row constants; the caller synchronises the
   // block before any warp reads them (finish()).
-  __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t* aux, int w) {
+  __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t* aux, int w,
+                       const float* sq) {
     uint4* frag = reinterpret_cast<uint4*>(aux);
     float* rowc = reinterpret_cast<float*>(aux + KS * 32 * 16);
     if (w == 0) {
@@ -475,8 +502,9 @@ struct Int8Warp {
       float qmax = 0.f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        qv[ks] = has ? load_q4(p.q, p.q_dtype, (static_cast<size_t>(b) * p.Hq + h0 + r) * D + kslot_d(ks, c))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[ks] = !has ? make_float4(0.f, 0.f, 0.f, 0.f)
+                 : sq ? *reinterpret_cast<const float4*>(sq + r * D + kslot_d(ks, c))
+                      : load_q4(p.q, p.q_dtype, (static_cast<size_t>(b) * p.Hq + h0 + r) * D + kslot_d(ks, c));
         qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(qv[ks].x), fabsf(qv[ks].y)),
                                  fmaxf(fabsf(qv[ks].z), fabsf(qv[ks].w))));
       }
@@ -682,11 +710,11 @@ struct WarpOf<kINT8, D> {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int KVT, int D>
+template <int KVT, int D, bool STEP>
 __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     decode_kernel(const __grid_constant__ DParams p) {
   using Lo = Layout<KVT, D>;
-  using Sm = Smem<KVT, D>;
+  using Sm = Smem<KVT, D, STEP>;
   constexpr int S = Lo::S, PPI = Lo::PPI;
   constexpr int kW = Tune<KVT, D>::W, kThreads = kW * 32;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -711,7 +739,9 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   const int j_first = pb + (w + (lane / PPI) * kW) * PPI + lane % PPI;
   const int raw_first = j_first < min(p.MB, pb + p.chunk) ? bt[j_first] : -1;
   typename WarpOf<KVT, D>::type st;
-  st.prefetch(p, b, h0, nh, lane, w);  // query loads, in flight with the length and table reads
+  // query loads, in flight with the length and table reads (the fused step reads its
+  // rotated queries from shared memory instead)
+  if constexpr (!STEP) st.prefetch(p, b, h0, nh, lane, w);
   const int L = p.lens[b];
   const bool len_ok = L >= 0 && L <= p.MB * kPage;
   const int np = len_ok ? (L + kPage - 1) / kPage : 0;
@@ -783,7 +813,139 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     issue(0, 0);
   }
 
-  st.init(p, b, h0, nh, lane, aux, w);
+  // ---- the fused decode step: the rotated query rows, and the new token's K and V rows
+  // in storage format for the block that holds the sequence's last page (which patches
+  // them into that page once it lands, and, for head group 0, stores them in the cache)
+  const float* sq = nullptr;
+  bool patch = false;
+  int t_new = 0;
+  uint8_t* const nrow = smem + Sm::step0 + Sm::stepQ + Sm::stepRope;
+  if constexpr (STEP) {
+    constexpr int esz = ElemSize<KVT>::value;
+    float* sqw = reinterpret_cast<float*>(smem + Sm::step0);
+    float* rc = reinterpret_cast<float*>(smem + Sm::step0 + Sm::stepQ);
+    float* rs = rc + D / 2;
+    const int slot = p.slots[b];
+    const bool rope = p.positions != nullptr;
+    const int pos = rope ? p.positions[b] : 0;
+    bool slot_ok = true;  // the new token must sit at logical position L - 1
+    if (slot >= 0) {
+      const int lp = len_ok && L >= 1 ? bt[(L - 1) / kPage] : -1;
+      slot_ok = lp >= 0 && lp < p.num_pages && slot == lp * kPage + (L - 1) % kPage;
+      if (!slot_ok && tid == 0) atomicOr(&s_flag, 0x4);  // PKV_DEV_BAD_SLOT
+    }
+    if (rope) {
+      // rotation angles pos * theta^(-2i/D) in double, cos and sin rounded to float
+      for (int i = tid; i < D / 2; i += kThreads) {
+        const double a = static_cast<double>(pos) * pow(p.rope_theta, -2.0 * i / D);
+        rc[i] = static_cast<float>(cos(a));
+        rs[i] = static_cast<float>(sin(a));
+      }
+      __syncthreads();
+    }
+    for (int idx = tid; idx < nh * (D / 2); idx += kThreads) {
+      const int h = idx / (D / 2), i = idx % (D / 2);
+      const size_t qi = (static_cast<size_t>(b) * p.Hq + h0 + h) * D + i;
+      float x0, x1;
+      if (p.q_dtype == kBF16) {
+        x0 = __bfloat162float(static_cast<const __nv_bfloat16*>(p.q)[qi]);
+        x1 = __bfloat162float(static_cast<const __nv_bfloat16*>(p.q)[qi + D / 2]);
+      } else {
+        x0 = static_cast<const float*>(p.q)[qi];
+        x1 = static_cast<const float*>(p.q)[qi + D / 2];
+      }
+      if (rope) {  // pair (i, i + D/2) rotated by angle i
+        const float c = rc[i], sn = rs[i];
+        const float t = __fmul_rn(x1, sn), u = __fmul_rn(x0, sn);
+        x0 = __fmaf_rn(x0, c, -t);
+        x1 = __fmaf_rn(x1, c, u);
+      }
+      sqw[h * D + i] = x0;
+      sqw[h * D + i + D / 2] = x1;
+    }
+    patch = slot >= 0 && slot_ok && np > 0 && pe == np;
+    t_new = (L - 1) & (kPage - 1);
+    if (patch && w == 0) {
+      constexpr int E = D / 32;  // lane l holds elements E l .. E l + E - 1
+      const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D + lane * E;
+      float kx[E], vx[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (p.new_dtype == kBF16) {
+          kx[e] = __bfloat162float(static_cast<const __nv_bfloat16*>(p.k_new)[src + e]);
+          vx[e] = __bfloat162float(static_cast<const __nv_bfloat16*>(p.v_new)[src + e]);
+        } else {
+          kx[e] = static_cast<const float*>(p.k_new)[src + e];
+          vx[e] = static_cast<const float*>(p.v_new)[src + e];
+        }
+      }
+      if (rope) {
+        // element d's partner d +- D/2 sits in lane l +- 16 at the same e; the operation
+        // order is fixed (it decides the stored bits): two products, then a fused
+        // multiply-add per output
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int d = lane * E + e, i = d & (D / 2 - 1);
+          const float partner = __shfl_xor_sync(0xffffffffu, kx[e], 16);
+          const float c = rc[i], sn = rs[i];
+          const float t = __fmul_rn(partner, sn);
+          kx[e] = d < D / 2 ? __fmaf_rn(kx[e], c, -t) : __fmaf_rn(kx[e], c, t);
+        }
+      }
+      // storage format, in shared memory (the patch) and, by head group 0, in the cache
+      const int page = slot / kPage, off = slot % kPage;
+      const size_t blk = static_cast<size_t>(page) * p.Hkv + g;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float(&x)[E] = which ? vx : kx;
+        uint8_t* nr = nrow + which * (D * esz + 16);
+        uint8_t* cache = which ? p.vw : p.kw;
+        if constexpr (KVT == kINT8) {
+          int8_t code[E];
+          const float sc = quantize_row_int8<E>(x, code);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            nr[d] = static_cast<uint8_t>(code[e]);
+            if (hg == 0) {
+              if (which == 0) cache[(blk * kPage + off) * D + d] = static_cast<uint8_t>(code[e]);
+              else cache[blk * D * kPage + static_cast<size_t>(d) * kPage + off] = static_cast<uint8_t>(code[e]);
+            }
+          }
+          if (lane == 0) {
+            *reinterpret_cast<float*>(nr + D) = sc;
+            if (hg == 0) (which ? p.vsw : p.ksw)[blk * kPage + off] = sc;
+          }
+        } else if constexpr (KVT == kBF16) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            const __nv_bfloat16 v = __float2bfloat16_rn(x[e]);
+            reinterpret_cast<__nv_bfloat16*>(nr)[d] = v;
+            if (hg == 0) {
+              const int o = which == 0 ? bf16_k_off(off, d, D) : bf16_v_off(d, off);
+              *reinterpret_cast<__nv_bfloat16*>(cache + blk * kPage * D * 2 + o) = v;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            reinterpret_cast<float*>(nr)[d] = x[e];
+            if (hg == 0) {
+              float* cf = reinterpret_cast<float*>(cache);
+              if (which == 0) cf[(blk * kPage + off) * D + d] = x[e];
+              else cf[blk * D * kPage + static_cast<size_t>(d) * kPage + off] = x[e];
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // rotated queries and the new row are ready
+    sq = sqw;
+  }
+
+  st.init(p, b, h0, nh, lane, aux, w, sq);
   if constexpr (KVT == kINT8) __syncthreads();  // warp 0 built the shared query fragments
   st.finish(aux, lane);
   __syncwarp();
@@ -799,6 +961,39 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     }
     const uint8_t* sp = my_stages + stage * Lo::stageBytes;
     const int j0 = pb + (w + i * kW) * PPI;
+    if constexpr (STEP) {
+      // the fused step: the new token replaces whatever the cache held at its slot
+      if (patch && j0 <= np - 1 && np - 1 < j0 + PPI) {
+        constexpr int esz = ElemSize<KVT>::value;
+        uint8_t* pg = my_stages + stage * Lo::stageBytes + (np - 1 - j0) * Lo::pageBytes;
+        const uint8_t* nk = nrow;
+        const uint8_t* nv = nrow + D * esz + 16;
+        for (int d = lane; d < D; d += 32) {
+          if constexpr (KVT == kINT8) {
+            pg[t_new * D + d] = nk[d];
+            pg[Lo::kBytes + d * kPage + t_new] = nv[d];
+          } else if constexpr (KVT == kBF16) {
+            *reinterpret_cast<__nv_bfloat16*>(pg + bf16_k_off(t_new, d, D)) =
+                reinterpret_cast<const __nv_bfloat16*>(nk)[d];
+            *reinterpret_cast<__nv_bfloat16*>(pg + Lo::kBytes + bf16_v_off(d, t_new)) =
+                reinterpret_cast<const __nv_bfloat16*>(nv)[d];
+          } else {
+            reinterpret_cast<float*>(pg)[t_new * D + d] = reinterpret_cast<const float*>(nk)[d];
+            reinterpret_cast<float*>(pg + Lo::kBytes)[d * kPage + t_new] =
+                reinterpret_cast<const float*>(nv)[d];
+          }
+        }
+        if constexpr (KVT == kINT8) {
+          if (lane == 0) {
+            reinterpret_cast<float*>(pg + 2 * Lo::kBytes)[t_new] = *reinterpret_cast<const float*>(nk + D);
+            reinterpret_cast<float*>(pg + 2 * Lo::kBytes + Lo::sBytes)[t_new] =
+                *reinterpret_cast<const float*>(nv + D);
+          }
+        }
+        fence_proxy_async_smem();  // ordered before the stage's next bulk copy
+        __syncwarp();
+      }
+    }
     if constexpr (KVT == kF32) {
       const int valid = min(kPage, L - j0 * kPage);
       constexpr int HM = f32_head_cap<D>();
@@ -1025,9 +1220,9 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   if (tid == 0) *ticket = 0;  // leave the counter ready for the next call
 }
 
-template <int KVT, int D>
+template <int KVT, int D, bool STEP>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_kernel<KVT, D>);
+  return reinterpret_cast<const void*>(&decode_kernel<KVT, D, STEP>);
 }
 
 struct Variant {
@@ -1044,16 +1239,24 @@ constexpr int max_splits_of() {
   return Smem<KVT, D>::big / (2 * kMaxHeads * 4) - 1;
 }
 
-#define PKV_VARIANT(T, D, I) \
-  {kernel_ptr<T, D>(), Smem<T, D>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>(), Tune<T, D>::W}
-Variant variant(int dtype, int D) {
-  switch (dtype * 1000 + D) {
-    case kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, 0);
-    case kF32 * 1000 + 128: return PKV_VARIANT(kF32, 128, 1);
-    case kBF16 * 1000 + 64: return PKV_VARIANT(kBF16, 64, 2);
-    case kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, 3);
-    case kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, 4);
-    case kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, 5);
+#define PKV_VARIANT(T, D, ST, I)                                                        \
+  {kernel_ptr<T, D, ST>(), Smem<T, D, ST>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>(), \
+   Tune<T, D>::W}
+// step: the fused decode-step kernels (indices 6 .. 11)
+Variant variant(int dtype, int D, bool step) {
+  switch (dtype * 1000 + D + (step ? 100000 : 0)) {
+    case kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, false, 0);
+    case kF32 * 1000 + 128: return PKV_VARIANT(kF32, 128, false, 1);
+    case kBF16 * 1000 + 64: return PKV_VARIANT(kBF16, 64, false, 2);
+    case kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, false, 3);
+    case kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, false, 4);
+    case kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, false, 5);
+    case 100000 + kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, true, 6);
+    case 100000 + kF32 * 1000 + 128: return PKV_VARIANT(kF32, 128, true, 7);
+    case 100000 + kBF16 * 1000 + 64: return PKV_VARIANT(kBF16, 64, true, 8);
+    case 100000 + kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, true, 9);
+    case 100000 + kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, true, 10);
+    case 100000 + kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, true, 11);
     default: return {nullptr, 0, -1, 1, 1, 4};
   }
 }
@@ -1064,7 +1267,7 @@ Variant variant(int dtype, int D) {
 constexpr int kMaxDevices = 64;
 struct DevInfo {
   int sms = 0;
-  int occ[6] = {0, 0, 0, 0, 0, 0};
+  int occ[12] = {};
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -1093,9 +1296,9 @@ bool device_facts(int device, const Variant& v, int* sms, int* occ) {
 }  // namespace
 
 bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int device,
-                 int chunk_override, DecodePlan* plan) {
+                 int chunk_override, DecodePlan* plan, bool step) {
   (void)q_dtype;
-  const Variant v = variant(c.dtype, c.D);
+  const Variant v = variant(c.dtype, c.D, step);
   if (!v.fn) return false;
   const int G = Hq / c.Hkv;
   const int cap = (c.dtype == kF32 && c.D == 128) ? f32_head_cap<128>() : kMaxHeads;
@@ -1139,7 +1342,7 @@ bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int dev
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st) {
-  const Variant v = variant(a.c.dtype, a.c.D);
+  const Variant v = variant(a.c.dtype, a.c.D, a.step);
   if (!v.fn) return cudaErrorInvalidValue;
   DParams p{};
   p.k = static_cast<const uint8_t*>(a.c.k);
@@ -1162,6 +1365,18 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   p.num_pages = a.c.num_pages;
   p.chunk = plan.chunk_pages;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  if (a.step) {
+    p.kw = static_cast<uint8_t*>(a.kw);
+    p.vw = static_cast<uint8_t*>(a.vw);
+    p.ksw = a.ksw;
+    p.vsw = a.vsw;
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.new_dtype = a.new_dtype;
+    p.slots = a.slots;
+    p.positions = a.positions;
+    p.rope_theta = a.rope_theta;
+  }
   if (plan.n_splits > 1) {
     const size_t tickets = static_cast<size_t>(a.B) * a.c.Hkv * plan.head_groups;
     uint8_t* base = static_cast<uint8_t*>(a.ws);

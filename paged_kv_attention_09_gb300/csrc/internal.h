@@ -54,11 +54,24 @@ struct DecodeArgs {
   float* out;
   void* ws;
   int32_t* dev_status;
+  // the fused decode step (step == true): the new token of each sequence
+  bool step = false;
+  void* kw = nullptr;  // the cache again, writable (the new rows are stored)
+  void* vw = nullptr;
+  float* ksw = nullptr;
+  float* vsw = nullptr;
+  const void* k_new = nullptr;  // [B][Hkv][D]
+  const void* v_new = nullptr;
+  int new_dtype = 0;
+  const int32_t* slots = nullptr;      // [B]; < 0: no new token
+  const int32_t* positions = nullptr;  // [B]; nullptr: no rotation
+  double rope_theta = 10000.0;
 };
 
 // Fills `plan` for this shape on `device`; returns false for unsupported shapes.
+// step: plan for the fused decode-step kernels (their shared memory is a little larger).
 bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int device,
-                 int chunk_override, DecodePlan* plan);
+                 int chunk_override, DecodePlan* plan, bool step = false);
 // The process-wide split override set by pkv_set_decode_chunk_pages (0 = automatic).
 int decode_chunk_override();
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st);

@@ -22,7 +22,7 @@ DEV_BAD_PAGE, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_BAD_CHUNK, DEV_TIMEOUT = 0x1, 0x2, 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_DTYPE",
           4: "PKV_ERR_PAGE_SIZE", 5: "PKV_ERR_ALIGN", 6: "PKV_ERR_WORKSPACE",
           7: "PKV_ERR_UNSUPPORTED", 8: "PKV_ERR_LAUNCH", 9: "PKV_ERR_DEVICE"}
-EXPORTS = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn",
+EXPORTS = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn", "pkv_decode_step",
            "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn",
            "pkv_decode_attn_noalloc", "pkv_set_decode_chunk_pages", "pkv_status_string")
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -58,10 +58,12 @@ def load(path: str = LIB_PATH):
     lib.pkv_append.argtypes = [C, P, P, I32, P, I32, P, P]
     lib.pkv_decode_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.pkv_decode_attn.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, P, SZ, P, P]
+    lib.pkv_decode_step.argtypes = [C, P, I32, P, P, I32, P, P, ctypes.c_double, I32, I32, P,
+                                    I32, P, F, P, P, SZ, P, P]
     lib.pkv_prefill_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.pkv_prefill_chunk_attn.argtypes = [C, P, I32, I32, I32, P, I32, P, I32, P, F, P, P, SZ,
                                            P, P]
-    for fn in ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn",
+    for fn in ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn", "pkv_decode_step",
                "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn"):
         getattr(lib, fn).restype = ctypes.c_int
     lib.pkv_decode_attn_noalloc.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, P, P]
@@ -163,6 +165,23 @@ def pkv_decode_attn(cache: KVCache, q: torch.Tensor, block_tables: torch.Tensor,
                                   _ptr(block_tables), int(block_tables.shape[1]),
                                   _ptr(context_lens), float(scale), _ptr(out), _ptr(workspace),
                                   wb, _ptr(dev_status), _stream(stream)), "pkv_decode_attn")
+
+
+def pkv_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    slot_mapping: torch.Tensor, positions: Optional[torch.Tensor],
+                    rope_theta: float, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                    scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                    dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """One fused decode step (rotate, append the new row, attend); see include/pkv.h."""
+    c = cache.struct()
+    B, Hq, _ = q.shape
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_decode_step(ctypes.byref(c), _ptr(q), _CODE[q.dtype], _ptr(k_new),
+                                  _ptr(v_new), _CODE[k_new.dtype], _ptr(slot_mapping),
+                                  _ptr(positions), float(rope_theta), B, Hq, _ptr(block_tables),
+                                  int(block_tables.shape[1]), _ptr(context_lens), float(scale),
+                                  _ptr(out), _ptr(workspace), wb, _ptr(dev_status),
+                                  _stream(stream)), "pkv_decode_step")
 
 
 def pkv_decode_attn_noalloc(cache: KVCache, q: torch.Tensor, block_tables: torch.Tensor,

@@ -110,3 +110,24 @@ def run_step(dw: DeviceWorkload, step_k=None, step_v=None, step_slots=None, stre
     if step_slots.numel():
         pkv.pkv_append(dw.cache, step_k, step_v, step_slots, dw.dev_status, stream)
     return [run_batch(dw, i, stream) for i in range(len(dw.batches))]
+
+
+def decode_step_inputs(dw: DeviceWorkload, i: int = 0, rope: bool = True):
+    """The new token of every sequence of decode batch ``i`` (the workload's newest row of
+    each decode sequence): K and V rows, slots, and rotation positions (context - 1)."""
+    b = dw.batches[i]
+    B = b.q.shape[0]
+    rows = dw.step_rows[:B]
+    pos = (b.context_lens - 1).to(torch.int32).contiguous() if rope else None
+    return (dw.k_src[rows].contiguous(), dw.v_src[rows].contiguous(),
+            dw.slots[rows].contiguous(), pos)
+
+
+def run_decode_step(dw: DeviceWorkload, inputs, i: int = 0, rope_theta: float = 10000.0,
+                    stream=None) -> torch.Tensor:
+    """Decode batch ``i`` as one fused step (rotate, append the new rows, attend)."""
+    b = dw.batches[i]
+    k, v, slots, pos = inputs
+    pkv.pkv_decode_step(dw.cache, b.q, k, v, slots, pos, rope_theta, b.block_tables,
+                        b.context_lens, dw.wl.scale, b.out, b.workspace, dw.dev_status, stream)
+    return b.out
