@@ -1,8 +1,12 @@
 """Benchmark: paged decode attention (append + decode [+ chunked prefill]) on GB300.
 
-One step = one pass of the hot path over one batch: append the step's new K/V rows into
-the paged cache, then run every batch of the workload (decode and, for the mixed
-workload, chunked prefill).  The default workload is the batch-256 TinyLlama-shaped INT8
+One step = one pass of the hot path over one batch: the new K/V rows go into the paged
+cache and every batch of the workload runs (decode and, for the mixed workload, chunked
+prefill): pkv_append of the new rows, then pkv_decode_attn / pkv_prefill_chunk_attn.
+``--fused`` runs the decode batch as one fused launch instead (pkv_decode_step: append of
+the new row and attention; the prefill chunks' rows still go through pkv_append), and
+``--rope`` adds the rotary embedding of the new query and key at position context - 1 to
+that launch.  The default workload is the batch-256 TinyLlama-shaped INT8
 decode.  Inputs are synthetic and seeded; R replicas of every input rotate so that each
 step reads data that is not in L2.
 
@@ -29,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode attn achieved HBM GB/s & seq-tokens/s vs 8 TB/s roofline, 1 GB300"
+ROPE_THETA = 10000.0
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -44,6 +49,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=10.0)
+    ap.add_argument("--fused", action="store_true",
+                    help="the decode batch as one pkv_decode_step launch")
+    ap.add_argument("--rope", action="store_true",
+                    help="with --fused: the step also applies the rotary embedding")
     return ap.parse_args()
 
 
@@ -191,12 +200,15 @@ def traffic_from_profiles(kernel_tag, workload):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_rate(wl, seconds, threads):
+def cpu_oracle_rate(wl, seconds, threads, fused=True, rope=False):
     """Time the oracle (as it stands) on a bounded sample of the workload: whole
-    sequences of the decode batch (and prefill rows as whole sequences), taken in order
-    until about ``seconds`` of wall time.  Returns (GB/s, tokens/s, sample description)."""
+    sequences of the decode batch (as the same fused step when ``fused``) and of the
+    prefill batch, taken in order until about ``seconds`` of wall time.  Returns (GB/s,
+    tokens/s, sample description)."""
     import oracle
     oc = oracle.cache_from_workload(wl)
+    d0 = wl.batches[0]
+    new_rows = wl.step_rows[:d0.num_seqs]
     done_bytes, done_tok, t_total, sample = 0, 0, 0.0, []
     for b in wl.batches:
         B = b.num_seqs
@@ -204,7 +216,14 @@ def cpu_oracle_rate(wl, seconds, threads):
         while True:
             seqs = list(range(min(B, n)))
             t0 = time.perf_counter()
-            if b.kind == "decode":
+            if b.kind == "decode" and fused:
+                oracle.decode_step(oc, b.q, b.q_dtype, wl.k_src[new_rows], wl.v_src[new_rows],
+                                   wl.new_dtype, wl.slots[new_rows],
+                                   (b.context_lens - 1).astype(np.int32) if rope else None,
+                                   ROPE_THETA,
+                                   b.block_tables, b.context_lens, wl.scale, seqs=seqs,
+                                   threads=threads)
+            elif b.kind == "decode":
                 oracle.decode(oc, b.q, b.q_dtype, b.block_tables, b.context_lens, wl.scale,
                               seqs=seqs, threads=threads)
             else:
@@ -241,9 +260,15 @@ def run_ours(args, rank, world):
     ws_bytes = acc["total"]
     R = args.replicas or max(2, math.ceil(4 * L2_BYTES / max(ws_bytes, 1)))
     base = runner.upload(wl, f"cuda:{dev}")
+    fused = args.fused and wl.batches[0].kind == "decode"
     rows = base.step_rows
+    dec_in = None
+    if fused:  # the decode batch's new rows go through pkv_decode_step
+        dec_in = runner.decode_step_inputs(base, 0, rope=args.rope)
+        rows = rows[wl.batches[0].num_seqs:]
     step_k, step_v, step_s = (base.k_src[rows].contiguous(), base.v_src[rows].contiguous(),
                               base.slots[rows].contiguous())
+    n_append = int(step_s.numel())
     reps = [base]
     for _ in range(R - 1):
         c = base.cache
@@ -264,15 +289,22 @@ def run_ours(args, rank, world):
 
     def append_only(i):
         dw = reps[i % R]
-        pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
+        if n_append:
+            pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
+
+    def run_j(dw, j):
+        if fused and j == 0:
+            runner.run_decode_step(dw, dec_in, 0, ROPE_THETA, stream)
+        else:
+            runner.run_batch(dw, j, stream)
 
     def batch_only(j):
-        return lambda i: runner.run_batch(reps[i % R], j, stream)
+        return lambda i: run_j(reps[i % R], j)
 
     def step(i):
         append_only(i)
         for j in range(n_batches):
-            runner.run_batch(reps[i % R], j, stream)
+            run_j(reps[i % R], j)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -305,7 +337,8 @@ def run_ours(args, rank, world):
     # every kernel in it is ours.  Per-kernel averages come from graphs of that kernel
     # alone over the same rotating replicas.
     g_step = capture(step)
-    g_kern = [capture(append_only)] + [capture(batch_only(j)) for j in range(n_batches)]
+    g_kern = ([capture(append_only)] if n_append else []) + \
+        [capture(batch_only(j)) for j in range(n_batches)]
     with torch.cuda.stream(stream):
         g_step.replay()
     torch.cuda.synchronize()
@@ -328,7 +361,8 @@ def run_ours(args, rank, world):
     # (q, new K/V, slots, tables, lengths) from pinned memory, the calls, D2H of outputs
     e2e = None
     if not args.no_e2e:
-        host_in = [t.cpu().pin_memory() for t in (step_k, step_v, step_s)]
+        step_dev = [step_k, step_v, step_s] + ([t for t in dec_in if t is not None] if fused else [])
+        host_in = [t.cpu().pin_memory() for t in step_dev]
         for b in base.batches:
             host_in += [b.q.cpu().pin_memory(), b.block_tables.cpu().pin_memory(),
                         b.context_lens.cpu().pin_memory()]
@@ -340,16 +374,17 @@ def run_ours(args, rank, world):
 
         def e2e_step(i):
             dw = reps[i % R]
-            dev_in = [step_k, step_v, step_s]
+            dev_in = list(step_dev)
             for b in dw.batches:
                 dev_in += [b.q, b.block_tables, b.context_lens]
                 if b.q_start_loc is not None:
                     dev_in.append(b.q_start_loc)
             for d, h in zip(dev_in, host_in):
                 d.copy_(h, non_blocking=True)  # on `stream` (the current stream here)
-            pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
+            if n_append:
+                pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
             for j in range(n_batches):
-                runner.run_batch(dw, j, stream)
+                run_j(dw, j)
             for b, h in zip(dw.batches, host_out):
                 h.copy_(b.out, non_blocking=True)
 
@@ -374,7 +409,7 @@ def run_ours(args, rank, world):
     status = int(base.dev_status.item())
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed steps")
-    return wl, acc, R, ms, kern_ms, clk.summary(), e2e
+    return wl, acc, R, ms, kern_ms, clk.summary(), e2e, fused, n_append
 
 
 def main():
@@ -388,9 +423,9 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    wl, acc, R, ms, kern_ms, clocks, e2e = run_ours(args, rank, world)
+    wl, acc, R, ms, kern_ms, clocks, e2e, fused, n_append = run_ours(args, rank, world)
     K = args.steps
-    names = ["append"] + [b.kind for b in wl.batches]
+    names = (["append"] if n_append else []) + [b.kind for b in wl.batches]
     avg = {n: statistics.fmean(v) for n, v in zip(names, kern_ms)}
     peak, peak_kind = measured_hbm()
     value = acc["total"] * world / (ms * 1e-3) / 1e9
@@ -405,7 +440,12 @@ def main():
             "head_dim": wl.head_dim, "page_size": wl.page_size, "num_pages": wl.num_pages,
             "batches": [{"kind": b.kind, "num_seqs": b.num_seqs,
                          "context_tokens": int(b.context_lens.sum())} for b in wl.batches],
-            "step": "append new K/V rows, then attention over every batch",
+            "step": ((("decode batch as one fused launch (rotary embedding of the new query and "
+                       "key, append of the new row, attention)") if args.rope else
+                      "decode batch as one fused launch (append of the new row, attention)") +
+                     ("; prefill chunk rows appended, then prefill attention"
+                      if len(wl.batches) > 1 else "") if fused else
+                     "append new K/V rows, then attention over every batch"),
             "timing": "CUDA events around one CUDA-graph replay of the K steps",
             "bytes_per_step": acc["total"], "replicas": R,
             "l2": f"rotating {R} replicas of every input ({R} x {acc['total'] / 1e6:.1f} MB "
@@ -415,12 +455,13 @@ def main():
         "seq_tokens_per_s": round(acc["kv_tokens"] * world / (ms * 1e-3), 1),
         "decode_steps_per_s": round(acc["seqs"] * world / (ms * 1e-3), 1),
         "kernel_ms": {n: round(v, 5) for n, v in avg.items()},
-        "gpu_launches": K * (1 + len(wl.batches)),
+        "gpu_launches": K * ((1 if n_append else 0) + len(wl.batches)),
     }
     dec = avg.get("decode")
     if dec:
         achieved = acc["decode"] / (dec * 1e-3) / 1e9
-        line["roofline"] = {"bound": "hbm", "kernel": "decode_kernel",
+        line["roofline"] = {"bound": "hbm",
+                            "kernel": "decode_kernel (fused step)" if fused else "decode_kernel",
                             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                             "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                             "frac_of_8tbs": round(achieved / 8000.0, 4),
@@ -434,7 +475,8 @@ def main():
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = len(os.sched_getaffinity(0))
-        gbs, tps, sample, secs = cpu_oracle_rate(wl, args.cpu_sample_seconds, threads)
+        gbs, tps, sample, secs = cpu_oracle_rate(wl, args.cpu_sample_seconds, threads, fused,
+                                                 args.rope)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": sample + f" ({secs:.1f} s wall)",
                                 "seq_tokens_per_s": round(tps, 1)}
@@ -452,10 +494,10 @@ def main_reference(args):
     threads = len(os.sched_getaffinity(0))
     per_step = max(0.5, args.cpu_sample_seconds / max(1, args.steps + args.warmup) * 4)
     for _ in range(args.warmup):
-        cpu_oracle_rate(wl, per_step / 4, threads)
+        cpu_oracle_rate(wl, per_step / 4, threads, args.fused, args.rope)
     vals, secs = [], 0.0
     for _ in range(args.steps):
-        gbs, tps, sample, s = cpu_oracle_rate(wl, per_step, threads)
+        gbs, tps, sample, s = cpu_oracle_rate(wl, per_step, threads, args.fused, args.rope)
         vals.append(gbs)
         secs += s
     v = statistics.fmean(vals)

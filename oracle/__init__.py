@@ -218,11 +218,13 @@ def rope_f32(x, pos, theta):
 
 
 def decode_step(cache: HostCache, q, q_dtype, k_new, v_new, new_dtype, slot_mapping,
-                positions, theta, block_tables, context_lens, scale, *, seqs=None):
+                positions, theta, block_tables, context_lens, scale, *, seqs=None,
+                threads=None):
     """One decode step (rotate, store the new row, attend); mutates ``cache``.
 
     ``positions`` None: no rotation.  Returns float64 [B, Hq, D]; sequences not listed in
-    ``seqs`` are neither stored nor computed (NaN rows).
+    ``seqs`` are neither stored nor computed (NaN rows).  ``threads`` > 1 runs sequences
+    on a thread pool (each stores only its own slot).
     """
     q = _c(q, _REAL[q_dtype])
     k_new = _c(k_new, _REAL[new_dtype])
@@ -235,12 +237,18 @@ def decode_step(cache: HostCache, q, q_dtype, k_new, v_new, new_dtype, slot_mapp
     out = np.full((B, Hq, D), np.nan, np.float64)
     lib = load()
     seqs = list(range(B)) if seqs is None else [int(s) for s in seqs]
-    bad = 0
-    for b in seqs:
-        bad += lib.oracle_decode_step(*cache.args(), _ptr(q), q_dtype, _ptr(k_new), _ptr(v_new),
+    def run(b):
+        return lib.oracle_decode_step(*cache.args(), _ptr(q), q_dtype, _ptr(k_new), _ptr(v_new),
                                       new_dtype, _ptr(sm), _ptr(pos), float(theta), B, Hq,
                                       _ptr(bt), bt.shape[1], _ptr(cl), float(scale), _ptr(out),
                                       b, b + 1)
+
+    n = _threads(len(seqs), threads)
+    if n == 1:
+        bad = sum(run(b) for b in seqs)
+    else:
+        with ThreadPoolExecutor(n) as ex:
+            bad = sum(ex.map(run, seqs))
     decode_step.last_bad = bad
     return out
 

@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "internal.h"
@@ -48,6 +49,7 @@ namespace pkv {
 namespace {
 
 constexpr int kMaxHeads = 8;     // query heads per block
+constexpr int kMaxHeadDim = 128;
 
 struct DParams {
   const uint8_t* k;
@@ -74,8 +76,9 @@ struct DParams {
   const void* v_new;
   const int32_t* slots;
   const int32_t* positions;
-  double rope_theta;
   int new_dtype;
+  // theta^(-2i/D), i < D/2, computed on the host (the rotation angle is pos * inv_freq[i])
+  double inv_freq[kMaxHeadDim / 2];
 };
 
 template <int KVT>
@@ -739,9 +742,48 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   const int j_first = pb + (w + (lane / PPI) * kW) * PPI + lane % PPI;
   const int raw_first = j_first < min(p.MB, pb + p.chunk) ? bt[j_first] : -1;
   typename WarpOf<KVT, D>::type st;
-  // query loads, in flight with the length and table reads (the fused step reads its
-  // rotated queries from shared memory instead)
-  if constexpr (!STEP) st.prefetch(p, b, h0, nh, lane, w);
+  // query loads, in flight with the length and table reads (a fused step with rotation
+  // reads its rotated queries from shared memory instead)
+  const bool rope = STEP && p.positions != nullptr;
+  if (!rope) st.prefetch(p, b, h0, nh, lane, w);
+  // the fused step's loads, raw bits, likewise issued before anything waits: thread t
+  // holds query pairs t, t + kThreads, ... (pair (h, i) = elements i and i + D/2 of head
+  // h0 + h); warp 0 holds the new token's K and V rows, E = D/32 elements per lane
+  constexpr int QPT = STEP ? (kMaxHeads * (D / 2) + kThreads - 1) / kThreads : 1;
+  constexpr int NE = D / 32;
+  uint32_t qr[QPT][2], kr[NE], vr[NE];
+  if constexpr (STEP) {
+    const bool qb = p.q_dtype == kBF16, nb = p.new_dtype == kBF16;
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int idx = tid + k * kThreads;
+      qr[k][0] = qr[k][1] = 0u;
+      if (rope && idx < nh * (D / 2)) {
+        const size_t qi = (static_cast<size_t>(b) * p.Hq + h0 + idx / (D / 2)) * D + idx % (D / 2);
+        if (qb) {
+          qr[k][0] = static_cast<const uint16_t*>(p.q)[qi];
+          qr[k][1] = static_cast<const uint16_t*>(p.q)[qi + D / 2];
+        } else {
+          qr[k][0] = static_cast<const uint32_t*>(p.q)[qi];
+          qr[k][1] = static_cast<const uint32_t*>(p.q)[qi + D / 2];
+        }
+      }
+    }
+    const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D + lane * NE;
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+      kr[e] = vr[e] = 0u;
+      if (w == 0) {
+        if (nb) {
+          kr[e] = static_cast<const uint16_t*>(p.k_new)[src + e];
+          vr[e] = static_cast<const uint16_t*>(p.v_new)[src + e];
+        } else {
+          kr[e] = static_cast<const uint32_t*>(p.k_new)[src + e];
+          vr[e] = static_cast<const uint32_t*>(p.v_new)[src + e];
+        }
+      }
+    }
+  }
   const int L = p.lens[b];
   const bool len_ok = L >= 0 && L <= p.MB * kPage;
   const int np = len_ok ? (L + kPage - 1) / kPage : 0;
@@ -826,7 +868,6 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     float* rc = reinterpret_cast<float*>(smem + Sm::step0 + Sm::stepQ);
     float* rs = rc + D / 2;
     const int slot = p.slots[b];
-    const bool rope = p.positions != nullptr;
     const int pos = rope ? p.positions[b] : 0;
     bool slot_ok = true;  // the new token must sit at logical position L - 1
     if (slot >= 0) {
@@ -837,23 +878,21 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     if (rope) {
       // rotation angles pos * theta^(-2i/D) in double, cos and sin rounded to float
       for (int i = tid; i < D / 2; i += kThreads) {
-        const double a = static_cast<double>(pos) * pow(p.rope_theta, -2.0 * i / D);
-        rc[i] = static_cast<float>(cos(a));
-        rs[i] = static_cast<float>(sin(a));
+        double sn, cs;
+        sincos(static_cast<double>(pos) * p.inv_freq[i], &sn, &cs);
+        rc[i] = static_cast<float>(cs);
+        rs[i] = static_cast<float>(sn);
       }
       __syncthreads();
     }
-    for (int idx = tid; idx < nh * (D / 2); idx += kThreads) {
+    const bool qb = p.q_dtype == kBF16;
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int idx = tid + k * kThreads;
+      if (!rope || idx >= nh * (D / 2)) break;
       const int h = idx / (D / 2), i = idx % (D / 2);
-      const size_t qi = (static_cast<size_t>(b) * p.Hq + h0 + h) * D + i;
-      float x0, x1;
-      if (p.q_dtype == kBF16) {
-        x0 = __bfloat162float(static_cast<const __nv_bfloat16*>(p.q)[qi]);
-        x1 = __bfloat162float(static_cast<const __nv_bfloat16*>(p.q)[qi + D / 2]);
-      } else {
-        x0 = static_cast<const float*>(p.q)[qi];
-        x1 = static_cast<const float*>(p.q)[qi + D / 2];
-      }
+      float x0 = __uint_as_float(qb ? qr[k][0] << 16 : qr[k][0]);
+      float x1 = __uint_as_float(qb ? qr[k][1] << 16 : qr[k][1]);
       if (rope) {  // pair (i, i + D/2) rotated by angle i
         const float c = rc[i], sn = rs[i];
         const float t = __fmul_rn(x1, sn), u = __fmul_rn(x0, sn);
@@ -866,18 +905,13 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     patch = slot >= 0 && slot_ok && np > 0 && pe == np;
     t_new = (L - 1) & (kPage - 1);
     if (patch && w == 0) {
-      constexpr int E = D / 32;  // lane l holds elements E l .. E l + E - 1
-      const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D + lane * E;
+      constexpr int E = NE;  // lane l holds elements E l .. E l + E - 1
+      const bool nb = p.new_dtype == kBF16;
       float kx[E], vx[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        if (p.new_dtype == kBF16) {
-          kx[e] = __bfloat162float(static_cast<const __nv_bfloat16*>(p.k_new)[src + e]);
-          vx[e] = __bfloat162float(static_cast<const __nv_bfloat16*>(p.v_new)[src + e]);
-        } else {
-          kx[e] = static_cast<const float*>(p.k_new)[src + e];
-          vx[e] = static_cast<const float*>(p.v_new)[src + e];
-        }
+        kx[e] = __uint_as_float(nb ? kr[e] << 16 : kr[e]);
+        vx[e] = __uint_as_float(nb ? vr[e] << 16 : vr[e]);
       }
       if (rope) {
         // element d's partner d +- D/2 sits in lane l +- 16 at the same e; the operation
@@ -942,7 +976,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
       }
     }
     __syncthreads();  // rotated queries and the new row are ready
-    sq = sqw;
+    if (rope) sq = sqw;  // (without rotation the queries load as in plain decode)
   }
 
   st.init(p, b, h0, nh, lane, aux, w, sq);
@@ -1375,7 +1409,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
     p.new_dtype = a.new_dtype;
     p.slots = a.slots;
     p.positions = a.positions;
-    p.rope_theta = a.rope_theta;
+    if (a.positions) {
+      for (int i = 0; i < a.c.D / 2; ++i) p.inv_freq[i] = std::pow(a.rope_theta, -2.0 * i / a.c.D);
+    }
   }
   if (plan.n_splits > 1) {
     const size_t tickets = static_cast<size_t>(a.B) * a.c.Hkv * plan.head_groups;
