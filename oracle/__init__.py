@@ -54,16 +54,17 @@ def _bind(lib):
     lib.oracle_quantize_row_int8.restype = None
     lib.oracle_append.argtypes = [i, i, i, i, i, p, p, p, p, p, p, i, p, i]
     lib.oracle_append.restype = i
-    lib.oracle_decode.argtypes = [i, i, i, i, i, p, p, p, p, p, i, i, i, p, i, p, d, p, i, i]
+    lib.oracle_decode.argtypes = [i, i, i, i, i, p, p, p, p, p, i, i, i, p, i, p, d, i, p, i, i]
     lib.oracle_decode.restype = i
-    lib.oracle_prefill.argtypes = [i, i, i, i, i, p, p, p, p, p, i, i, i, p, p, i, p, d, p, i, i]
+    lib.oracle_prefill.argtypes = [i, i, i, i, i, p, p, p, p, p, i, i, i, p, p, i, p, d, i, p, i,
+                                   i]
     lib.oracle_prefill.restype = i
     lib.oracle_rope_f64.argtypes = [p, p, i, i, d]
     lib.oracle_rope_f64.restype = None
     lib.oracle_rope_f32.argtypes = [p, p, i, i, d]
     lib.oracle_rope_f32.restype = None
     lib.oracle_decode_step.argtypes = [i, i, i, i, i, p, p, p, p, p, i, p, p, i, p, p, d, i, i,
-                                       p, i, p, d, p, i, i]
+                                       p, i, p, d, i, p, i, i]
     lib.oracle_decode_step.restype = i
     return lib
 
@@ -145,8 +146,10 @@ def _threads(n_items, threads):
 
 
 def decode(cache: HostCache, q, q_dtype, block_tables, context_lens, scale, *,
-           seqs=None, threads=None):
+           window=0, seqs=None, threads=None):
     """Decode attention in FP64 for every sequence (or the listed ``seqs``).
+
+    ``window`` > 0: each query attends to the last ``window`` positions only.
 
     Returns float64 [B, Hq, D]; rows of sequences not listed are left as NaN.
     ``threads`` > 1 runs sequences on a thread pool (ctypes releases the GIL).
@@ -161,7 +164,8 @@ def decode(cache: HostCache, q, q_dtype, block_tables, context_lens, scale, *,
 
     def run(b):
         return lib.oracle_decode(*cache.args(), _ptr(q), q_dtype, B, Hq, _ptr(bt),
-                                 bt.shape[1], _ptr(cl), float(scale), _ptr(out), b, b + 1)
+                                 bt.shape[1], _ptr(cl), float(scale), int(window), _ptr(out),
+                                 b, b + 1)
 
     n = _threads(len(seqs), threads)
     if n == 1:
@@ -174,8 +178,9 @@ def decode(cache: HostCache, q, q_dtype, block_tables, context_lens, scale, *,
 
 
 def prefill(cache: HostCache, q, q_dtype, q_start_loc, block_tables, context_lens, scale,
-            *, seqs=None, threads=None):
-    """Chunked-prefill attention in FP64; returns float64 [total_q, Hq, D]."""
+            *, window=0, seqs=None, threads=None):
+    """Chunked-prefill attention in FP64; returns float64 [total_q, Hq, D].  ``window`` > 0:
+    each row attends to the last ``window`` positions up to its own."""
     q = _c(q, _REAL[q_dtype])
     qsl = _c(q_start_loc, np.int32)
     bt = _c(block_tables, np.int32)
@@ -188,7 +193,8 @@ def prefill(cache: HostCache, q, q_dtype, q_start_loc, block_tables, context_len
 
     def run(b):
         return lib.oracle_prefill(*cache.args(), _ptr(q), q_dtype, B, Hq, _ptr(qsl), _ptr(bt),
-                                  bt.shape[1], _ptr(cl), float(scale), _ptr(out), b, b + 1)
+                                  bt.shape[1], _ptr(cl), float(scale), int(window), _ptr(out),
+                                  b, b + 1)
 
     n = _threads(len(seqs), threads)
     if n == 1:
@@ -218,7 +224,7 @@ def rope_f32(x, pos, theta):
 
 
 def decode_step(cache: HostCache, q, q_dtype, k_new, v_new, new_dtype, slot_mapping,
-                positions, theta, block_tables, context_lens, scale, *, seqs=None,
+                positions, theta, block_tables, context_lens, scale, *, window=0, seqs=None,
                 threads=None):
     """One decode step (rotate, store the new row, attend); mutates ``cache``.
 
@@ -240,8 +246,8 @@ def decode_step(cache: HostCache, q, q_dtype, k_new, v_new, new_dtype, slot_mapp
     def run(b):
         return lib.oracle_decode_step(*cache.args(), _ptr(q), q_dtype, _ptr(k_new), _ptr(v_new),
                                       new_dtype, _ptr(sm), _ptr(pos), float(theta), B, Hq,
-                                      _ptr(bt), bt.shape[1], _ptr(cl), float(scale), _ptr(out),
-                                      b, b + 1)
+                                      _ptr(bt), bt.shape[1], _ptr(cl), float(scale),
+                                      int(window), _ptr(out), b, b + 1)
 
     n = _threads(len(seqs), threads)
     if n == 1:

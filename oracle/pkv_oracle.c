@@ -270,17 +270,18 @@ void oracle_rope_f32(const float* x, float* y, int D, int pos, double theta) {
 
 /*
  * Softmax-weighted sum for one query vector q (length D, already in double) over the
- * logical tokens 0..n_keys-1 of sequence b, kv head g.  Logical token t lives in
- * physical page block_table[t / P] at offset t % P.
+ * logical tokens first_key..n_keys-1 of sequence b, kv head g.  Logical token t lives in
+ * physical page block_table[t / P] at offset t % P; no other table entry is read.
  */
-static void attend_one(const double* q, int n_keys, const int32_t* block_table, int g,
+static void attend_one(const double* q, int first_key, int n_keys,
+                       const int32_t* block_table, int g,
                        const void* k_cache, const void* v_cache, const float* k_scale,
                        const float* v_scale, int kv_dtype, int Hkv, int P, int D,
                        double scale, double* scores, double* out) {
   for (int d = 0; d < D; ++d) out[d] = 0.0;
-  if (n_keys <= 0) return;
+  if (n_keys <= first_key) return;
   double m = -INFINITY;
-  for (int t = 0; t < n_keys; ++t) {
+  for (int t = first_key; t < n_keys; ++t) {
 #if ORACLE_MUTANT == 8 /* pages taken in physical instead of logical order */
     int page = (int)(t / P), off = t % P;
     (void)block_table;
@@ -301,11 +302,11 @@ static void attend_one(const double* q, int n_keys, const int32_t* block_table, 
 #if ORACLE_MUTANT == 7 /* no max subtraction */
   m = 0.0;
 #endif
-  for (int t = 0; t < n_keys; ++t) {
+  for (int t = first_key; t < n_keys; ++t) {
     scores[t] = exp(scores[t] - m);
     denom += scores[t];
   }
-  for (int t = 0; t < n_keys; ++t) {
+  for (int t = first_key; t < n_keys; ++t) {
     int page = block_table[t / P], off = t % P;
     double w = scores[t] / denom;
     for (int d = 0; d < D; ++d)
@@ -314,19 +315,37 @@ static void attend_one(const double* q, int n_keys, const int32_t* block_table, 
 }
 
 /*
+ * Sliding window ("tinyloop Current Status", KV cache modes table: a cache window bounds
+ * the KV storage).  Reading: with window W > 0 the query at position pos attends to the
+ * keys at positions pos - W + 1 .. pos (the W most recent, its own included); W = 0 (or
+ * a window at least as long as the context) is plain causal attention.  Pages wholly
+ * before the window are never read, so their table entries may hold anything.
+ */
+static int window_first_key(int pos, int window) {
+  if (window <= 0) return 0;
+#if ORACLE_MUTANT == 11 /* window one key short */
+  int lo = pos - window + 2;
+#else
+  int lo = pos - window + 1;
+#endif
+  return lo > 0 ? lo : 0;
+}
+
+/*
  * Batched decode: one query token per sequence.  q is [B][Hq][D] (float32 or
  * bfloat16), out is [B][Hq][D] doubles.  Sequence b attends over its first
  * context_lens[b] logical tokens (the current token included).  GQA: query head h
  * reads kv head h / (Hq / Hkv).  A sequence with context length 0 gets a zero row.
+ * With window > 0 it attends to the last `window` of them only (window_first_key).
  * Sequences for which context_lens[b] is negative or above max_blocks * P, or whose
- * block table holds a page outside [0, num_pages), get NaN rows; the return value
- * counts them.
+ * block table holds a page outside [0, num_pages) among the pages it reads, get NaN
+ * rows; the return value counts them.
  */
 int oracle_decode(int kv_dtype, int num_pages, int P, int Hkv, int D, const void* k_cache,
                   const void* v_cache, const float* k_scale, const float* v_scale,
                   const void* q, int q_dtype, int B, int Hq, const int32_t* block_tables,
-                  int max_blocks, const int32_t* context_lens, double scale, double* out,
-                  int b_begin, int b_end) {
+                  int max_blocks, const int32_t* context_lens, double scale, int window,
+                  double* out, int b_begin, int b_end) {
   int G = Hq / Hkv, bad = 0;
   int max_len = max_blocks * P;
   double* qd = (double*)malloc(sizeof(double) * (size_t)D);
@@ -336,7 +355,8 @@ int oracle_decode(int kv_dtype, int num_pages, int P, int Hkv, int D, const void
     int L = context_lens[b];
     const int32_t* bt = block_tables + (size_t)b * max_blocks;
     int ok = (L >= 0 && L <= max_len);
-    for (int j = 0; ok && j < (L + P - 1) / P; ++j)
+    int lo = ok ? window_first_key(L - 1, window) : 0;
+    for (int j = lo / P; ok && j < (L + P - 1) / P; ++j)
       if (bt[j] < 0 || bt[j] >= num_pages) ok = 0;
     for (int h = 0; h < Hq; ++h) {
       double* o = out + ((size_t)b * Hq + h) * D;
@@ -350,7 +370,7 @@ int oracle_decode(int kv_dtype, int num_pages, int P, int Hkv, int D, const void
 #else
       int g = h / G;
 #endif
-      attend_one(qd, L, bt, g, k_cache, v_cache, k_scale, v_scale, kv_dtype, Hkv, P, D,
+      attend_one(qd, lo, L, bt, g, k_cache, v_cache, k_scale, v_scale, kv_dtype, Hkv, P, D,
                  scale, scores, o);
     }
     if (!ok) ++bad;
@@ -369,15 +389,16 @@ int oracle_decode(int kv_dtype, int num_pages, int P, int Hkv, int D, const void
  * rotation.  The new token must sit at logical position context_lens[b] - 1: a slot that
  * is not that position's slot (or a length below 1) gives NaN rows for b and nothing is
  * stored.  slot_mapping[b] < 0: nothing is stored and b attends over the cache as is.
- * Sequences b_begin .. b_end - 1 only.  Returns the number of sequences given NaN rows.
+ * window as in oracle_decode.  Sequences b_begin .. b_end - 1 only.  Returns the number
+ * of sequences given NaN rows.
  */
 int oracle_decode_step(int kv_dtype, int num_pages, int P, int Hkv, int D, void* k_cache,
                        void* v_cache, float* k_scale, float* v_scale, const void* q,
                        int q_dtype, const void* k_new, const void* v_new, int new_dtype,
                        const int32_t* slot_mapping, const int32_t* positions, double theta,
                        int B, int Hq, const int32_t* block_tables, int max_blocks,
-                       const int32_t* context_lens, double scale, double* out, int b_begin,
-                       int b_end) {
+                       const int32_t* context_lens, double scale, int window, double* out,
+                       int b_begin, int b_end) {
   int G = Hq / Hkv, bad = 0;
   int max_len = max_blocks * P;
   double* qd = (double*)malloc(sizeof(double) * (size_t)D);
@@ -391,7 +412,8 @@ int oracle_decode_step(int kv_dtype, int num_pages, int P, int Hkv, int D, void*
     int L = context_lens[b];
     const int32_t* bt = block_tables + (size_t)b * max_blocks;
     int ok = (L >= 0 && L <= max_len);
-    for (int j = 0; ok && j < (L + P - 1) / P; ++j)
+    int lo = ok ? window_first_key(L - 1, window) : 0;
+    for (int j = lo / P; ok && j < (L + P - 1) / P; ++j)
       if (bt[j] < 0 || bt[j] >= num_pages) ok = 0;
     const int slot = slot_mapping[b];
     if (ok && slot >= 0 && (L < 1 || slot != bt[(L - 1) / P] * P + (L - 1) % P)) ok = 0;
@@ -417,8 +439,8 @@ int oracle_decode_step(int kv_dtype, int num_pages, int P, int Hkv, int D, void*
       for (int d = 0; d < D; ++d) qd[d] = read_real(q, q_dtype, ((size_t)b * Hq + h) * D + d);
       if (positions) oracle_rope_f64(qd, qr, D, pos, theta);
       else for (int d = 0; d < D; ++d) qr[d] = qd[d];
-      attend_one(qr, L, bt, h / G, k_cache, v_cache, k_scale, v_scale, kv_dtype, Hkv, P, D,
-                 scale, scores, o);
+      attend_one(qr, lo, L, bt, h / G, k_cache, v_cache, k_scale, v_scale, kv_dtype, Hkv, P,
+                 D, scale, scores, o);
     }
     if (!ok) ++bad;
   }
@@ -436,15 +458,16 @@ int oracle_decode_step(int kv_dtype, int num_pages, int P, int Hkv, int D, void*
  * ([total_q][Hq][D]).  Its context_lens[b] counts every cached token including the
  * chunk, so query row i of the chunk (Lq = chunk length) sits at absolute position
  * p_i = context_lens[b] - Lq + i and attends to the logical tokens 0..p_i (the causal
- * mask is inclusive of its own position).  out is [total_q][Hq][D] doubles.  Sequences
- * with an inconsistent chunk (Lq < 0 or Lq > context length) or bad pages get NaN
- * rows; the return value counts them.
+ * mask is inclusive of its own position); with window > 0, to p_i - window + 1 .. p_i
+ * only (window_first_key).  out is [total_q][Hq][D] doubles.  Sequences with an
+ * inconsistent chunk (Lq < 0 or Lq > context length) or a bad page among those their
+ * rows read get NaN rows; the return value counts them.
  */
 int oracle_prefill(int kv_dtype, int num_pages, int P, int Hkv, int D, const void* k_cache,
                    const void* v_cache, const float* k_scale, const float* v_scale,
                    const void* q, int q_dtype, int B, int Hq, const int32_t* q_start_loc,
                    const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
-                   double scale, double* out, int b_begin, int b_end) {
+                   double scale, int window, double* out, int b_begin, int b_end) {
   int G = Hq / Hkv, bad = 0;
   int max_len = max_blocks * P;
   double* qd = (double*)malloc(sizeof(double) * (size_t)D);
@@ -455,7 +478,9 @@ int oracle_prefill(int kv_dtype, int num_pages, int P, int Hkv, int D, const voi
     int q0 = q_start_loc[b], Lq = q_start_loc[b + 1] - q_start_loc[b];
     const int32_t* bt = block_tables + (size_t)b * max_blocks;
     int ok = (L >= 0 && L <= max_len && Lq >= 0 && Lq <= L);
-    for (int j = 0; ok && j < (L + P - 1) / P; ++j)
+    /* the chunk's first row has the lowest window start */
+    int lo0 = ok ? window_first_key(L - Lq, window) : 0;
+    for (int j = lo0 / P; ok && j < (L + P - 1) / P; ++j)
       if (bt[j] < 0 || bt[j] >= num_pages) ok = 0;
     if (!ok) ++bad;
     for (int i = 0; i < (Lq > 0 ? Lq : 0); ++i) {
@@ -473,8 +498,13 @@ int oracle_prefill(int kv_dtype, int num_pages, int P, int Hkv, int D, const voi
 #else
         int n_keys = pos + 1;
 #endif
-        attend_one(qd, n_keys, bt, h / G, k_cache, v_cache, k_scale, v_scale, kv_dtype,
-                   Hkv, P, D, scale, scores, o);
+#if ORACLE_MUTANT == 12 /* every row of the chunk takes the window of its last row */
+        int first = window_first_key(L - 1, window);
+#else
+        int first = window_first_key(pos, window);
+#endif
+        attend_one(qd, first, n_keys, bt, h / G, k_cache, v_cache, k_scale, v_scale,
+                   kv_dtype, Hkv, P, D, scale, scores, o);
       }
     }
   }

@@ -547,12 +547,129 @@ def test_decode_step_is_rotate_store_attend():
     assert check_decode_step()
 
 
+# --------------------------------------------------------------------------- sliding window
+# "tinyloop Current Status", KV cache modes table (a cache window bounds KV storage); the
+# reading taken: position pos sees positions pos - W + 1 .. pos, pages wholly before that
+# are never read.
+
+WINDOW_CASES = [
+    # kv, q, Hq, Hkv, D, decode lens, windows
+    (F32, F32, 4, 2, 64, [45, 16, 1, 70, 33], [1, 5, 16, 17, 33, 100]),
+    (BF16, BF16, 12, 2, 128, [40, 97], [3, 32, 47]),
+    (INT8, F32, 8, 2, 64, [50, 18], [2, 16, 31]),
+]
+
+
+def check_window_decode():
+    """Decode with a window equals dense attention over the reassembled rows
+    max(0, L - W) .. L - 1, whatever the table holds for the pages before them."""
+    for i, (kv, qd, Hq, Hkv, D, lens, wins) in enumerate(WINDOW_CASES):
+        wl = W.small_workload(500 + i, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                              kv_dtype=kv, q_dtype=qd, decode_lens=lens)
+        c = oracle.cache_from_workload(wl)
+        b = wl.batches[0]
+        q = q_f64(b.q, qd)
+        G = Hq // Hkv
+        for win in wins:
+            got = oracle.decode(c, b.q, qd, b.block_tables, b.context_lens, wl.scale, window=win)
+            for s in range(b.num_seqs):
+                L = int(b.context_lens[s])
+                lo = max(0, L - win)
+                for g in range(Hkv):
+                    k, v = logical_kv(c, b.block_tables[s], L, g)
+                    ref = sdpa(q[s, g * G:(g + 1) * G], k[lo:], v[lo:], wl.scale)
+                    if not np.max(np.abs(got[s, g * G:(g + 1) * G] - ref)) <= 1e-12:
+                        return False
+            # pages wholly before the window released (-1): same result, no error
+            bt = b.block_tables.copy()
+            for s in range(b.num_seqs):
+                bt[s, :max(0, int(b.context_lens[s]) - win) // P] = -1
+            got2 = oracle.decode(c, b.q, qd, bt, b.context_lens, wl.scale, window=win)
+            if oracle.decode.last_bad != 0 or not np.array_equal(got, got2):
+                return False
+    # window 1: the output is the newest V row itself (FP32 cache stores rows exactly)
+    wl = W.small_workload(510, num_q_heads=6, num_kv_heads=3, head_dim=64, kv_dtype=F32,
+                          q_dtype=F32, decode_lens=[29, 1, 48])
+    c = oracle.cache_from_workload(wl)
+    b = wl.batches[0]
+    got = oracle.decode(c, b.q, F32, b.block_tables, b.context_lens, wl.scale, window=1)
+    newest = wl.v_src[wl.step_rows[:3]].astype(np.float64)  # [B, Hkv, D]
+    if not np.array_equal(got, np.repeat(newest, 2, axis=1)):
+        return False
+    # a window at least as long as every context is plain causal attention
+    full = oracle.decode(c, b.q, F32, b.block_tables, b.context_lens, wl.scale)
+    return np.array_equal(full, oracle.decode(c, b.q, F32, b.block_tables, b.context_lens,
+                                              wl.scale, window=48))
+
+
+def test_window_decode_is_attention_over_the_last_w():
+    assert check_window_decode()
+
+
+def check_window_prefill():
+    """Each chunk row sees max(0, pos - W + 1) .. pos: dense attention with a band mask."""
+    for i, (kv, qd, Hq, Hkv, D) in enumerate([(BF16, BF16, 12, 2, 128), (F32, F32, 4, 2, 64),
+                                              (INT8, F32, 8, 2, 64)]):
+        wl = W.small_workload(520 + i, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                              kv_dtype=kv, q_dtype=qd, prefill=[(20, 13), (0, 17), (33, 1),
+                                                                (5, 40)])
+        c = oracle.cache_from_workload(wl)
+        b = wl.batches[0]
+        q = q_f64(b.q, qd)
+        G = Hq // Hkv
+        for win in (1, 7, 16, 30):
+            got = oracle.prefill(c, b.q, qd, b.q_start_loc, b.block_tables, b.context_lens,
+                                 wl.scale, window=win)
+            for s in range(b.num_seqs):
+                L = int(b.context_lens[s])
+                q0, q1 = int(b.q_start_loc[s]), int(b.q_start_loc[s + 1])
+                pos = L - (q1 - q0) + np.arange(q1 - q0)
+                t = np.arange(L)[None, :]
+                mask = (t <= pos[:, None]) & (t > pos[:, None] - win)
+                for g in range(Hkv):
+                    k, v = logical_kv(c, b.block_tables[s], L, g)
+                    for h in range(g * G, (g + 1) * G):
+                        ref = sdpa(q[q0:q1, h], k, v, wl.scale, mask)
+                        if not np.max(np.abs(got[q0:q1, h] - ref)) <= 1e-12:
+                            return False
+    return True
+
+
+def test_window_prefill_is_banded_causal_attention():
+    assert check_window_prefill()
+
+
+def check_window_step():
+    """The decode step with a window is the step's store followed by windowed decode."""
+    theta = 1.0e4
+    for i, (kv, qd, Hq, Hkv, D, lens, wins) in enumerate(WINDOW_CASES):
+        wl = W.small_workload(530 + i, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                              kv_dtype=kv, q_dtype=qd, decode_lens=lens)
+        b = wl.batches[0]
+        hist = oracle.cache_from_workload(wl, rows=wl.history_rows)
+        k_new, v_new, slots, pos = step_inputs(wl)
+        for win in wins[:2]:
+            c1, c2 = copy_cache(hist), copy_cache(hist)
+            got = oracle.decode_step(c1, b.q, qd, k_new, v_new, wl.new_dtype, slots, None, theta,
+                                     b.block_tables, b.context_lens, wl.scale, window=win)
+            oracle.append(c2, k_new, v_new, wl.new_dtype, slots)
+            ref = oracle.decode(c2, b.q, qd, b.block_tables, b.context_lens, wl.scale, window=win)
+            if not (same_cache(c1, c2) and np.array_equal(got, ref)):
+                return False
+    return True
+
+
+def test_window_step_is_store_then_windowed_decode():
+    assert check_window_step()
+
+
 PINS = [check_bf16_rounding, check_quantiser, check_decode_bruteforce,
         check_prefill_bruteforce, check_closed_forms, check_page_permutation_invariance,
-        check_gqa_equals_replicated_mha, check_causality, check_rope, check_decode_step]
+        check_gqa_equals_replicated_mha, check_causality, check_rope, check_decode_step,
+        check_window_decode, check_window_prefill, check_window_step]
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12])
 def test_planted_mistake_is_caught(mutant, monkeypatch):
     path = oracle.build(defines=[f"ORACLE_MUTANT={mutant}"], name=f"liboracle_m{mutant}.so")
     monkeypatch.setattr(oracle, "_lib", oracle.load(path))
