@@ -51,6 +51,15 @@
  *   Element types: PKV_F32 float32, PKV_BF16 bfloat16, PKV_INT8 int8 code c whose value
  *   is c * scale, scale = max|x| / 127 per (token, kv head).
  *   All cache pointers must be 16-byte aligned.
+ *
+ * Sliding window (pkv_cache.window; "tinyloop Current Status", KV cache modes table: a
+ * cache window bounds the KV storage).  With window W > 0 every attention call lets the
+ * query at position pos see the keys at positions pos - W + 1 .. pos only (the W most
+ * recent, its own included); 0 means no window.  Pages wholly before a sequence's window
+ * are never read, so a cache manager may release them and leave any value (-1 included)
+ * in those block-table entries; partly covered pages are read and must hold written
+ * rows.  Several block tables may name the same physical pages (prefix sharing): pages
+ * are only read by the attention calls.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -94,6 +103,7 @@ typedef struct pkv_cache {
   int32_t num_kv_heads;
   int32_t head_dim;
   int32_t kv_dtype; /* pkv_dtype */
+  int32_t window;   /* sliding-window length in tokens, 0 = none (see above); >= 0 */
 } pkv_cache;
 
 /*

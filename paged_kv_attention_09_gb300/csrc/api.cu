@@ -21,6 +21,7 @@ pkv_status check_cache(const pkv_cache* c) {
   if (c->kv_dtype < PKV_F32 || c->kv_dtype > PKV_INT8) return PKV_ERR_DTYPE;
   if (c->page_size != 16) return PKV_ERR_PAGE_SIZE;
   if (c->num_pages < 1 || c->num_kv_heads < 1 || c->head_dim < 1) return PKV_ERR_SHAPE;
+  if (c->window < 0) return PKV_ERR_SHAPE;
   if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (c->kv_dtype == PKV_INT8 && (!c->k_scale || !c->v_scale)) return PKV_ERR_NULL;
   if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PKV_ERR_ALIGN;
@@ -33,7 +34,7 @@ pkv_status check_cache(const pkv_cache* c) {
 
 pkv::CacheView view(const pkv_cache* c) {
   return pkv::CacheView{c->k_cache, c->v_cache, c->k_scale, c->v_scale,
-                        c->num_pages, c->num_kv_heads, c->head_dim, c->kv_dtype};
+                        c->num_pages, c->num_kv_heads, c->head_dim, c->kv_dtype, c->window};
 }
 
 pkv_status current_device(int* dev) {

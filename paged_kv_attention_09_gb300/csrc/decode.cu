@@ -66,6 +66,7 @@ struct DParams {
   int* ws_ticket;
   int32_t* dev_status;
   int q_dtype, Hkv, Hq, G, hpc, head_groups, MB, B, num_pages, chunk;
+  int window;  // sliding window in tokens (0: none)
   float scale_log2;
   // the fused decode step (STEP kernels only)
   uint8_t* kw;
@@ -219,8 +220,10 @@ struct F32Warp {
     }
   }
 
+  // tokens lo .. valid - 1 of the page are attended (lo > 0 only for the first page of a
+  // sliding window)
   template <int NH>
-  __device__ void page(const uint8_t* st, float* probs, int valid, float sl, int lane) {
+  __device__ void page(const uint8_t* st, float* probs, int valid, int lo, float sl, int lane) {
     const float* Ks = reinterpret_cast<const float*>(st);
     const float* Vs = reinterpret_cast<const float*>(st + Layout<kF32, D>::kBytes);
     const int tq = lane >> 3, c8 = lane & 7;
@@ -249,7 +252,7 @@ struct F32Warp {
         a += __shfl_xor_sync(0xffffffffu, a, 1);
         a += __shfl_xor_sync(0xffffffffu, a, 2);
         a += __shfl_xor_sync(0xffffffffu, a, 4);
-        s[ps][h] = t < valid ? a * sl : -CUDART_INF_F;
+        s[ps][h] = t < valid && t >= lo ? a * sl : -CUDART_INF_F;
       }
     }
 #pragma unroll
@@ -288,12 +291,12 @@ struct F32Warp {
 #pragma unroll
       for (int i = 0; i < NC; ++i) {
         float4 vv = *reinterpret_cast<const float4*>(Vs + (lane + 32 * i) * kPage + c4 * 4);
-        if (valid < kPage) {  // padding tokens may hold anything (even NaN): zero them
+        if (valid < kPage || lo > 0) {  // tokens not attended may hold anything: zero them
           const int t0 = c4 * 4;
-          vv.x = t0 + 0 < valid ? vv.x : 0.f;
-          vv.y = t0 + 1 < valid ? vv.y : 0.f;
-          vv.z = t0 + 2 < valid ? vv.z : 0.f;
-          vv.w = t0 + 3 < valid ? vv.w : 0.f;
+          vv.x = t0 + 0 < valid && t0 + 0 >= lo ? vv.x : 0.f;
+          vv.y = t0 + 1 < valid && t0 + 1 >= lo ? vv.y : 0.f;
+          vv.z = t0 + 2 < valid && t0 + 2 >= lo ? vv.z : 0.f;
+          vv.w = t0 + 3 < valid && t0 + 3 >= lo ? vv.w : 0.f;
         }
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -391,7 +394,8 @@ struct Bf16Warp {
   // One page.  K and V arrive as tensor-core tiles, so ldmatrix builds every B fragment
   // from whole 16-byte core-matrix rows without bank conflicts.  n-tile j holds tokens
   // 8j .. 8j+7; lane (r, c) ends up with tokens 2c, 2c+1, 8+2c, 9+2c.
-  __device__ void page(const uint8_t* st, int valid, int lane) {
+  // tokens lo .. valid - 1 are attended (lo > 0 only for the first page of a window)
+  __device__ void page(const uint8_t* st, int valid, int lo, int lane) {
     using Lo = Layout<kBF16, D>;
     const int c = lane & 3;
     const uint32_t Ks = smem_u32(st);
@@ -418,11 +422,12 @@ struct Bf16Warp {
         x[2 * j + e] = ((sacc[j][0][e] + sacc[j][0][2 + e]) + (sacc[j][1][e] + sacc[j][1][2 + e])) *
                        row_scale;
     uint32_t vmask0 = 0xffffffffu, vmask1 = 0xffffffffu;
-    if (valid < kPage) {  // padding tokens may hold NaN: mask scores, zero their V entries
+    if (valid < kPage || lo > 0) {  // tokens not attended may hold NaN: mask scores, zero V
+      auto in = [&](int t) { return t < valid && t >= lo; };
 #pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = (8 * (i >> 1) + 2 * c + (i & 1)) < valid ? x[i] : -CUDART_INF_F;
-      vmask0 = (2 * c + 0 < valid ? 0x0000ffffu : 0u) | (2 * c + 1 < valid ? 0xffff0000u : 0u);
-      vmask1 = (2 * c + 8 < valid ? 0x0000ffffu : 0u) | (2 * c + 9 < valid ? 0xffff0000u : 0u);
+      for (int i = 0; i < 4; ++i) x[i] = in(8 * (i >> 1) + 2 * c + (i & 1)) ? x[i] : -CUDART_INF_F;
+      vmask0 = (in(2 * c + 0) ? 0x0000ffffu : 0u) | (in(2 * c + 1) ? 0xffff0000u : 0u);
+      vmask1 = (in(2 * c + 8) ? 0x0000ffffu : 0u) | (in(2 * c + 9) ? 0xffff0000u : 0u);
     }
     float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -554,8 +559,9 @@ struct Int8Warp {
   }
 
   // PPI consecutive pages at st + pg * pageBytes; valid[pg] tokens each (a page with
-  // valid 0 was not loaded and its stage memory is stale).
-  __device__ void pages(const uint8_t* st, const int (&valid)[PPI], int lane) {
+  // valid 0 was not loaded and its stage memory is stale); the first lo tokens of page 0
+  // are before a sliding window and are not attended.
+  __device__ void pages(const uint8_t* st, const int (&valid)[PPI], int lo, int lane) {
     using Lo = Layout<kINT8, D>;
     const int r = lane >> 2, c = lane & 3;
     float x[PPI][4];
@@ -603,7 +609,7 @@ struct Int8Warp {
         for (int e = 0; e < 2; ++e)
           x[pg][2 * j + e] = (sacc[j][e] + sacc[j][2 + e]) * (row_scale * ksc[pg][2 * j + e]);
     }
-    bool partial = false;
+    bool partial = lo > 0;
 #pragma unroll
     for (int pg = 0; pg < PPI; ++pg) partial |= valid[pg] < kPage;
     if (partial) {  // padding may hold NaN scales: mask by select
@@ -611,7 +617,7 @@ struct Int8Warp {
       for (int pg = 0; pg < PPI; ++pg)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const bool ok = (4 * c + i) < valid[pg];
+          const bool ok = (4 * c + i) < valid[pg] && (pg > 0 || (4 * c + i) >= lo);
           x[pg][i] = ok ? x[pg][i] : -CUDART_INF_F;
           vsc[pg][i] = ok ? vsc[pg][i] : 0.f;
         }
@@ -713,7 +719,9 @@ struct WarpOf<kINT8, D> {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int KVT, int D, bool STEP>
+// WIN: compiled with the sliding-window range and mask (the kernels without it carry no
+// trace of it: the INT8 kernel sits at its register budget)
+template <int KVT, int D, bool STEP, bool WIN>
 __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     decode_kernel(const __grid_constant__ DParams p) {
   using Lo = Layout<KVT, D>;
@@ -736,11 +744,13 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   // The block-table entries of this warp's first 32 pages do not depend on the context
   // length: read them together with it (validated below), so that the first copies wait
   // for one global round trip instead of two.  The warp's page m is the block's logical
-  // page pb + (w + (m / PPI) kW) PPI + m % PPI.
-  const int pb = split * p.chunk;
+  // page pb + (w + (m / PPI) kW) PPI + m % PPI.  (With a sliding window the block's
+  // range starts at the window's first page, known once the length is: a second trip.)
+  const int win = WIN ? p.window : 0;
+  int pb = split * p.chunk;
   const int32_t* bt = p.bt + static_cast<size_t>(b) * p.MB;
-  const int j_first = pb + (w + (lane / PPI) * kW) * PPI + lane % PPI;
-  const int raw_first = j_first < min(p.MB, pb + p.chunk) ? bt[j_first] : -1;
+  const int j_off = (w + (lane / PPI) * kW) * PPI + lane % PPI;
+  int raw_first = win == 0 && pb + j_off < min(p.MB, pb + p.chunk) ? bt[pb + j_off] : -1;
   typename WarpOf<KVT, D>::type st;
   // query loads, in flight with the length and table reads (a fused step with rotation
   // reads its rotated queries from shared memory instead)
@@ -787,8 +797,15 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   const int L = p.lens[b];
   const bool len_ok = L >= 0 && L <= p.MB * kPage;
   const int np = len_ok ? (L + kPage - 1) / kPage : 0;
-  const int nsplit = len_ok ? max(1, (np + p.chunk - 1) / p.chunk) : 1;
+  // first attended key: L - window under a sliding window, else 0; the splits cover the
+  // pages from the one that holds it
+  const int lo = win > 0 && len_ok && L > win ? L - win : 0;
+  const int nsplit = len_ok ? max(1, (np - lo / kPage + p.chunk - 1) / p.chunk) : 1;
   if (split >= nsplit) return;
+  if (win > 0) {
+    pb += lo / kPage;
+    raw_first = pb + j_off < min(np, pb + p.chunk) ? bt[pb + j_off] : -1;
+  }
   const int pe = min(np, pb + p.chunk);
   if (tid == 0) s_flag = len_ok ? 0 : 0x2 /*PKV_DEV_BAD_LEN*/;
 
@@ -1028,23 +1045,25 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
         __syncwarp();
       }
     }
+    // the window's first page (block 0, warp 0, iteration 0) skips the keys before it
+    const int lo_t = WIN && j0 * kPage < lo ? lo - j0 * kPage : 0;
     if constexpr (KVT == kF32) {
       const int valid = min(kPage, L - j0 * kPage);
       constexpr int HM = f32_head_cap<D>();
       switch (nh) {  // the FP32 path unrolls over the block's head count
-        case 1: st.template page<1>(sp, probs, valid, p.scale_log2, lane); break;
-        case 2: st.template page<2>(sp, probs, valid, p.scale_log2, lane); break;
-        case 3: st.template page<3>(sp, probs, valid, p.scale_log2, lane); break;
-        case 4: st.template page<4>(sp, probs, valid, p.scale_log2, lane); break;
-        default: st.template page<HM>(sp, probs, valid, p.scale_log2, lane); break;
+        case 1: st.template page<1>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+        case 2: st.template page<2>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+        case 3: st.template page<3>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+        case 4: st.template page<4>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+        default: st.template page<HM>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
       }
     } else if constexpr (KVT == kBF16) {
-      st.page(sp, min(kPage, L - j0 * kPage), lane);
+      st.page(sp, min(kPage, L - j0 * kPage), lo_t, lane);
     } else {
       int valid[PPI];
 #pragma unroll
       for (int q = 0; q < PPI; ++q) valid[q] = j0 + q < pe ? min(kPage, L - (j0 + q) * kPage) : 0;
-      st.pages(sp, valid, lane);
+      st.pages(sp, valid, lo_t, lane);
     }
     const int nxt = i + S;
     if (nxt < n_my) {
@@ -1254,9 +1273,9 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   if (tid == 0) *ticket = 0;  // leave the counter ready for the next call
 }
 
-template <int KVT, int D, bool STEP>
+template <int KVT, int D, bool STEP, bool WIN>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_kernel<KVT, D, STEP>);
+  return reinterpret_cast<const void*>(&decode_kernel<KVT, D, STEP, WIN>);
 }
 
 struct Variant {
@@ -1273,24 +1292,26 @@ constexpr int max_splits_of() {
   return Smem<KVT, D>::big / (2 * kMaxHeads * 4) - 1;
 }
 
-#define PKV_VARIANT(T, D, ST, I)                                                        \
-  {kernel_ptr<T, D, ST>(), Smem<T, D, ST>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>(), \
+#define PKV_VARIANT(T, D, ST, WN, I)                                                        \
+  {kernel_ptr<T, D, ST, WN>(), Smem<T, D, ST>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>(), \
    Tune<T, D>::W}
-// step: the fused decode-step kernels (indices 6 .. 11)
-Variant variant(int dtype, int D, bool step) {
-  switch (dtype * 1000 + D + (step ? 100000 : 0)) {
-    case kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, false, 0);
-    case kF32 * 1000 + 128: return PKV_VARIANT(kF32, 128, false, 1);
-    case kBF16 * 1000 + 64: return PKV_VARIANT(kBF16, 64, false, 2);
-    case kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, false, 3);
-    case kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, false, 4);
-    case kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, false, 5);
-    case 100000 + kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, true, 6);
-    case 100000 + kF32 * 1000 + 128: return PKV_VARIANT(kF32, 128, true, 7);
-    case 100000 + kBF16 * 1000 + 64: return PKV_VARIANT(kBF16, 64, true, 8);
-    case 100000 + kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, true, 9);
-    case 100000 + kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, true, 10);
-    case 100000 + kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, true, 11);
+// index: dtype-and-head-dim slot (0 .. 5), + 6 for the fused decode step, + 12 for the
+// sliding window
+constexpr int kVariants = 24;
+Variant variant(int dtype, int D, bool step, bool win) {
+  switch (dtype * 1000 + D + (step ? 100000 : 0) + (win ? 1000000 : 0)) {
+#define PKV_VARIANTS_OF(ST, WN, BASE, KEY)                                                 \
+    case KEY + kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, ST, WN, BASE + 0);          \
+    case KEY + kF32 * 1000 + 128: return PKV_VARIANT(kF32, 128, ST, WN, BASE + 1);        \
+    case KEY + kBF16 * 1000 + 64: return PKV_VARIANT(kBF16, 64, ST, WN, BASE + 2);        \
+    case KEY + kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, ST, WN, BASE + 3);      \
+    case KEY + kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, ST, WN, BASE + 4);        \
+    case KEY + kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, ST, WN, BASE + 5);
+    PKV_VARIANTS_OF(false, false, 0, 0)
+    PKV_VARIANTS_OF(true, false, 6, 100000)
+    PKV_VARIANTS_OF(false, true, 12, 1000000)
+    PKV_VARIANTS_OF(true, true, 18, 1100000)
+#undef PKV_VARIANTS_OF
     default: return {nullptr, 0, -1, 1, 1, 4};
   }
 }
@@ -1301,7 +1322,7 @@ Variant variant(int dtype, int D, bool step) {
 constexpr int kMaxDevices = 64;
 struct DevInfo {
   int sms = 0;
-  int occ[12] = {};
+  int occ[kVariants] = {};
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -1332,13 +1353,19 @@ bool device_facts(int device, const Variant& v, int* sms, int* occ) {
 bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int device,
                  int chunk_override, DecodePlan* plan, bool step) {
   (void)q_dtype;
-  const Variant v = variant(c.dtype, c.D, step);
+  const Variant v = variant(c.dtype, c.D, step, c.window > 0);
   if (!v.fn) return false;
   const int G = Hq / c.Hkv;
   const int cap = (c.dtype == kF32 && c.D == 128) ? f32_head_cap<128>() : kMaxHeads;
   plan->heads_per_cta = G < cap ? G : cap;
   plan->head_groups = (G + plan->heads_per_cta - 1) / plan->heads_per_cta;
-  const int mb = MB > 0 ? MB : 1;
+  // pages a sequence's keys can span: the table width, or under a sliding window of W
+  // tokens at most ceil((W - 1) / 16) + 1
+  int mb = MB > 0 ? MB : 1;
+  if (c.window > 0) {
+    const long long span = (static_cast<long long>(c.window) + kPage - 2) / kPage + 1;
+    if (span < mb) mb = static_cast<int>(span);
+  }
   int sms = 0, occ = 0;
   if (!device_facts(device, v, &sms, &occ)) return false;
   int chunk;
@@ -1376,7 +1403,7 @@ bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int dev
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st) {
-  const Variant v = variant(a.c.dtype, a.c.D, a.step);
+  const Variant v = variant(a.c.dtype, a.c.D, a.step, a.c.window > 0);
   if (!v.fn) return cudaErrorInvalidValue;
   DParams p{};
   p.k = static_cast<const uint8_t*>(a.c.k);
@@ -1398,6 +1425,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   p.B = a.B;
   p.num_pages = a.c.num_pages;
   p.chunk = plan.chunk_pages;
+  p.window = a.c.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   if (a.step) {
     p.kw = static_cast<uint8_t*>(a.kw);

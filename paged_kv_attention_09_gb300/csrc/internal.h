@@ -28,6 +28,7 @@ struct CacheView {
   const float* ks;
   const float* vs;
   int num_pages, Hkv, D, dtype;
+  int window;  // sliding-window length in tokens, 0 = none
 };
 
 // ---------------------------------------------------------------- append

@@ -338,6 +338,9 @@ bool plan_prefill(const CacheView& c, int B, int Hq, int max_q_len, int MB, int 
   (void)B; (void)MB; (void)device; (void)q_dtype;
   if (c.dtype != kBF16) return false;
   if (c.D != 64 && c.D != 128) return false;
+#if !PKV_PREFILL_TC
+  if (c.window > 0) return false;  // the warp-level MMA kernel has no window mask
+#endif
   const int G = Hq / c.Hkv;
 #if PKV_PREFILL_TC
   plan->rows_per_cta = prefill_tc_rows();

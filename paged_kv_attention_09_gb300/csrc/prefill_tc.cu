@@ -4,7 +4,9 @@
 // chunked-prefill SDPA path; BF16 KV with its own paged-attention kernel) and "tinyloop
 // Current Status" (chunked prefill, chunk 512; GQA; 16-token pages).  Row i of a chunk
 // of length Lq sits at position context_len - Lq + i and attends causally to positions
-// 0..that position (the chunk's own K/V are appended first).
+// 0..that position (the chunk's own K/V are appended first); under a sliding window of W
+// tokens ("tinyloop Current Status", KV cache modes table) to the last W of them only,
+// and the block's tiles start at the page of its lowest window start.
 //
 // One block computes 128 query rows — (chunk token, query head) pairs of one GQA group,
 // token-major — against the group's paged K/V in tiles of 64 keys (4 pages):
@@ -59,6 +61,7 @@ struct TParams {
   float* out;
   int32_t* dev_status;
   int q_dtype, Hkv, Hq, G, MB, num_pages;
+  int window;  // sliding window in tokens (0: none)
   float scale_log2;
 };
 
@@ -131,18 +134,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int p_first = L - Lq + row0 / p.G;
   const int p_last = L - Lq + last_row / p.G;
   const int n_keys0 = err ? 0 : p_last + 1;
+  // Sliding window of W tokens: row position pos sees keys pos - W + 1 .. pos.  Keys
+  // below lo_blk are seen by no row of the block, keys below lo_max by some rows only.
+  // The block's key range starts at kbase, the first key of the page holding lo_blk;
+  // tiles are counted from there.
+  const int win = p.window;
+  const int lo_blk = win > 0 ? max(0, p_first - win + 1) : 0;
+  const int lo_max = win > 0 ? p_last - win + 1 : 0;
+  const int kb0 = (lo_blk / kPage) * kPage;
   const int32_t* bt = p.bt + static_cast<size_t>(b) * p.MB;
   if (tid == 0) s_err = err;
   __syncthreads();
-  for (int j = tid; j < (n_keys0 + kPage - 1) / kPage; j += kThreadsTC) {
+  for (int j = kb0 / kPage + tid; j < (n_keys0 + kPage - 1) / kPage; j += kThreadsTC) {
     const int pg = bt[j];
     if (pg < 0 || pg >= p.num_pages) atomicOr(&s_err, 0x1);  // PKV_DEV_BAD_PAGE
   }
   __syncthreads();
   err = s_err;
   const int n_keys = err ? 0 : n_keys0;
-  const int n_pages = (n_keys + kPage - 1) / kPage;
-  const int n_tiles = (n_keys + kKeysTC - 1) / kKeysTC;
+  const int kbase = err ? 0 : kb0;
+  const int n_pages = (n_keys - kbase + kPage - 1) / kPage;  // pages from kbase on
+  const int n_tiles = (n_keys - kbase + kKeysTC - 1) / kKeysTC;
 
   // ---- set-up: TMEM, barriers, the query tile(s)
   if (warp == kSoftWarps) {
@@ -224,6 +236,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       uint64_t* empty = isK ? k_empty : v_empty;
       const uint8_t* src = isK ? p.k : p.v;
       uint8_t* ring = smem + (isK ? Sm::k0 : Sm::v0);
+      const int32_t* btw = bt + kbase / kPage;  // the block's first page
       int issued = 0;
       for (int j = 0; j < n_units; ++j) {
         const int st = j % RS, use = j / RS;
@@ -232,7 +245,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         if (*abort_flag) break;
         mbar_arrive_expect_tx(&full[st], np * Sm::kBlk);
         for (int q = 0; q < np; ++q) {
-          const size_t blk = static_cast<size_t>(bt[j * per + q]) * p.Hkv + g;
+          const size_t blk = static_cast<size_t>(btw[j * per + q]) * p.Hkv + g;
           bulk_g2s(ring + st * sbytes + q * Sm::kBlk, src + blk * Sm::kBlk, Sm::kBlk, &full[st], pol);
         }
         issued = j + 1;
@@ -311,6 +324,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // accumulator grp; thread = row r (TMEM lane 32 (warp % 4) + lane)
     const int grp = hf;
     const int pos = valid_row ? L - Lq + rho / p.G : p_first;
+    const int lo_row = win > 0 ? pos - win + 1 : 0;  // first key of the row's window
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tO = tmem + lane_base + D * grp;
     const float sl = p.scale_log2;
@@ -332,11 +346,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
       tc::fence_before_sync();
       mbar_arrive(&s_free[0]);
-      const int key0 = j * kKeysTC;
+      const int key0 = kbase + j * kKeysTC;
       // raw scores; the scale (> 0) is applied inside the exponent with one FMA
-      if (key0 + kKeysTC - 1 > p_first || key0 + kKeysTC > n_keys) {
+      if (key0 + kKeysTC - 1 > p_first || key0 + kKeysTC > n_keys || key0 < lo_max) {
 #pragma unroll
-        for (int u = 0; u < 64; ++u) s[u] = (key0 + u <= pos) ? s[u] : -CUDART_INF_F;
+        for (int u = 0; u < 64; ++u)
+          s[u] = (key0 + u <= pos && key0 + u >= lo_row) ? s[u] : -CUDART_INF_F;
       }
       float t[32];  // pairwise max tree (a flat chain would be 63 dependent steps)
 #pragma unroll
@@ -396,16 +411,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
       tc::st_wait();
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      if (key0 + kKeysTC > n_keys) {
-        // keys past the last one any row may see: pages not loaded, or page padding
-        // that may hold anything (even NaN); zero them in V so that 0 * V stays 0
-        // (after this tile's V copies have landed)
+      const int kz = min(kKeysTC, n_keys - key0);      // tile keys kz .. 63: past the end
+      const int hz = j == 0 ? lo_blk - kbase : 0;       // tile keys 0 .. hz - 1: before the window
+      if (kz < kKeysTC || hz > 0) {
+        // keys no row may see: pages not loaded, page padding, or keys of the first page
+        // before every row's window; they may hold anything (even NaN), so zero them in V
+        // so that 0 * V stays 0 (after this tile's V copies have landed)
         ok = mbar_wait(&v_full[j % Sm::KST], (j / Sm::KST) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         uint8_t* vst = smem + Sm::v0 + (j % Sm::KST) * Sm::stage;
-        const int kz = n_keys - key0;
-        for (int idx = r; idx < (kKeysTC - kz) * D; idx += kRowsTC) {
-          const int key = kz + idx / D, d = idx % D;
+        for (int idx = r; idx < (kKeysTC - kz + hz) * D; idx += kRowsTC) {
+          const int u = idx / D, d = idx % D;
+          const int key = u < hz ? u : kz + (u - hz);
           *reinterpret_cast<__nv_bfloat16*>(vst + (key >> 4) * Sm::kBlk + bf16_v_off(d, key & 15)) =
               __float2bfloat16_rn(0.f);
         }
@@ -504,6 +521,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, cudaStream_
   p.G = a.Hq / a.c.Hkv;
   p.MB = a.MB;
   p.num_pages = a.c.num_pages;
+  p.window = a.c.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   const bool split = a.q_dtype == kF32;
   const void* fn;

@@ -39,7 +39,7 @@ class pkv_cache(ctypes.Structure):
                 ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32), ("window", ctypes.c_int32)]
 
 
 _lib = None
@@ -102,10 +102,11 @@ class KVCache:
     include/pkv.h); the tensor shapes are containers of the right size.
     """
 
-    def __init__(self, k, v, k_scale=None, v_scale=None):
+    def __init__(self, k, v, k_scale=None, v_scale=None, window=0):
         self.k, self.v, self.k_scale, self.v_scale = k, v, k_scale, v_scale
         self.num_pages, self.num_kv_heads, self.page_size, self.head_dim = k.shape
         self.kv_dtype = _CODE[k.dtype]
+        self.window = int(window)  # sliding window in tokens (0: none), read by every call
 
     @classmethod
     def allocate(cls, num_pages, num_kv_heads, head_dim, kv_dtype, device="cuda",
@@ -124,7 +125,7 @@ class KVCache:
                          None if self.k_scale is None else self.k_scale.data_ptr(),
                          None if self.v_scale is None else self.v_scale.data_ptr(),
                          self.num_pages, self.page_size, self.num_kv_heads, self.head_dim,
-                         self.kv_dtype)
+                         self.kv_dtype, self.window)
 
 
 def pkv_status_string(code: int) -> str:

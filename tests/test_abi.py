@@ -58,6 +58,7 @@ def test_host_validation_codes(lib):
     assert _append(lib, _cache(page_size=8)) == 4                   # page size
     assert _append(lib, _cache(head_dim=96)) == 7                   # unsupported D
     assert _append(lib, _cache(num_pages=0)) == 2                   # shape
+    assert _append(lib, _cache(window=-1)) == 2                     # negative window
     assert _append(lib, _cache(k_cache=0x10008)) == 5               # alignment
     assert _append(lib, _cache(kv_dtype=pkv.INT8, k_scale=None)) == 1
     assert _append(lib, _cache(), new_dtype=pkv.INT8) == 3          # INT8 sources

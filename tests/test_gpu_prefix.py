@@ -41,6 +41,8 @@ def test_decode_with_shared_prefix_pages(kv):
     for chunk in (0, 2):  # automatic split, and a forced split so shared pages cross blocks
         pkv.pkv_set_decode_chunk_pages(chunk)
         try:
+            db.workspace = pkv.workspace_for(pkv.pkv_decode_workspace_size(
+                dw.cache, b.num_seqs, wl.num_q_heads, b.max_blocks), "cuda")
             runner.run_batch(dw, 0)
             torch.cuda.synchronize()
         finally:
