@@ -22,7 +22,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pkv_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
-F32, BF16, INT8 = 0, 1, 2
+F32, BF16, INT8, FP8, INT4 = 0, 1, 2, 3, 4
+QUANTISED = (INT8, FP8, INT4)
 
 
 def build(force: bool = False, defines=(), name: str = "liboracle.so") -> str:
@@ -52,6 +53,14 @@ def _bind(lib):
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
     lib.oracle_quantize_row_int8.argtypes = [p, i, p, p]
     lib.oracle_quantize_row_int8.restype = None
+    lib.oracle_quantize_row_fp8.argtypes = [p, i, p, p]
+    lib.oracle_quantize_row_fp8.restype = None
+    lib.oracle_quantize_row_int4.argtypes = [p, i, p, p]
+    lib.oracle_quantize_row_int4.restype = None
+    lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_value.restype = ctypes.c_double
     lib.oracle_append.argtypes = [i, i, i, i, i, p, p, p, p, p, p, i, p, i]
     lib.oracle_append.restype = i
     lib.oracle_decode.argtypes = [i, i, i, i, i, p, p, p, p, p, i, i, i, p, i, p, d, i, p, i, i]
@@ -89,20 +98,22 @@ def _c(a, dtype):
 
 
 _REAL = {F32: np.float32, BF16: np.uint16}
-_CACHE = {F32: np.float32, BF16: np.uint16, INT8: np.int8}
+_CACHE = {F32: np.float32, BF16: np.uint16, INT8: np.int8, FP8: np.uint8, INT4: np.uint8}
 
 
 class HostCache:
-    """The oracle's own KV cache: K [NP,Hkv,P,D], V [NP,Hkv,D,P], scales [NP,Hkv,P]."""
+    """The oracle's own KV cache: K [NP,Hkv,P,D], V [NP,Hkv,D,P], scales [NP,Hkv,P]
+    (INT4: K [NP,Hkv,P,D/2], V [NP,Hkv,D,P/2] bytes, two codes per byte)."""
 
     def __init__(self, kv_dtype, num_pages, page_size, num_kv_heads, head_dim, fill=0):
         self.kv_dtype, self.num_pages, self.page_size = kv_dtype, num_pages, page_size
         self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
         NP, H, P, D = num_pages, num_kv_heads, page_size, head_dim
         dt = _CACHE[kv_dtype]
-        self.k = np.full((NP, H, P, D), fill, dtype=dt)
-        self.v = np.full((NP, H, D, P), fill, dtype=dt)
-        if kv_dtype == INT8:
+        half = 2 if kv_dtype == INT4 else 1
+        self.k = np.full((NP, H, P, D // half), fill, dtype=dt)
+        self.v = np.full((NP, H, D, P // half), fill, dtype=dt)
+        if kv_dtype in QUANTISED:
             self.k_scale = np.zeros((NP, H, P), np.float32)
             self.v_scale = np.zeros((NP, H, P), np.float32)
         else:
@@ -128,6 +139,36 @@ def quantize_row_int8(x):
     s = np.zeros(1, np.float32)
     load().oracle_quantize_row_int8(_ptr(x), x.shape[0], _ptr(codes), _ptr(s))
     return codes, s[0]
+
+
+def quantize_row_fp8(x):
+    """Symmetric FP8 (E4M3) quantisation of one row; returns (codes uint8, scale float32)."""
+    x = _c(x, np.float32)
+    codes = np.zeros(x.shape[0], np.uint8)
+    s = np.zeros(1, np.float32)
+    load().oracle_quantize_row_fp8(_ptr(x), x.shape[0], _ptr(codes), _ptr(s))
+    return codes, s[0]
+
+
+def quantize_row_int4(x):
+    """Symmetric INT4 quantisation of one row; returns (codes int8 in [-7, 7], scale)."""
+    x = _c(x, np.float32)
+    codes = np.zeros(x.shape[0], np.int8)
+    s = np.zeros(1, np.float32)
+    load().oracle_quantize_row_int4(_ptr(x), x.shape[0], _ptr(codes), _ptr(s))
+    return codes, s[0]
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """Encode float32 values as FP8 E4M3 codes (nearest, ties to even, saturating)."""
+    lib = load()
+    return np.array([lib.oracle_f32_to_e4m3(float(v)) for v in np.asarray(x, np.float32).ravel()],
+                    np.uint8)
+
+
+def e4m3_value(codes) -> np.ndarray:
+    lib = load()
+    return np.array([lib.oracle_e4m3_value(int(c)) for c in np.asarray(codes).ravel()])
 
 
 def append(cache: HostCache, k_new, v_new, new_dtype, slot_mapping) -> int:

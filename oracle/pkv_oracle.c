@@ -56,7 +56,7 @@
 #define ORACLE_MUTANT 0
 #endif
 
-enum { ODT_F32 = 0, ODT_BF16 = 1, ODT_INT8 = 2 };
+enum { ODT_F32 = 0, ODT_BF16 = 1, ODT_INT8 = 2, ODT_FP8 = 3, ODT_INT4 = 4 };
 
 /* ---------------------------------------------------------------- scalar helpers */
 
@@ -121,7 +121,104 @@ void oracle_quantize_row_int8(const float* x, int n, int8_t* codes, float* scale
   *scale_out = s;
 }
 
+/*
+ * FP8 E4M3, the "fn" member of the OCP 8-bit floating-point formats (named as an option
+ * for the KV cache in the TinyInfer review, item 2 "Improve KV cache efficiency"): one
+ * sign bit, four exponent bits with bias 7, three mantissa bits; exponent field 0 holds
+ * the subnormals m/8 * 2^-6; there is no infinity and S.1111.111 is NaN, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_value(uint8_t c) {
+  int e = (c >> 3) & 15, m = c & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) mag = ldexp((double)m / 8.0, -6);
+  else mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return (c & 0x80) ? -mag : mag;
+}
+
+/* float -> E4M3 code: the nearest finite value, ties to the even code (even mantissa),
+ * magnitudes beyond 448 saturating to 448; the sign is kept (a negative value that
+ * rounds to zero gives the negative zero 0x80).  Written as a search over the 127
+ * finite non-negative codes, whose values increase with the code. */
+uint8_t oracle_f32_to_e4m3(float x) {
+  double a = fabs((double)x);
+  if (a > 448.0) a = 448.0;
+  int best = 0;
+  double bd = a;  /* distance to code 0 */
+  for (int c = 1; c <= 126; ++c) {
+    double d = fabs(oracle_e4m3_value((uint8_t)c) - a);
+#if ORACLE_MUTANT == 13 /* rounding toward zero */
+    if (oracle_e4m3_value((uint8_t)c) <= a) { best = c; bd = d; }
+#else
+    if (d < bd || (d == bd && (c & 1) == 0)) { best = c; bd = d; }
+#endif
+  }
+  return (uint8_t)(signbit(x) ? (best | 0x80) : best);
+}
+
+/* Symmetric per-row FP8 quantiser (the INT8 scheme with the E4M3 range): s = max|x| /
+ * 448 (float division), code = e4m3(x / s); a row of zeros gets s = 0 and codes 0. */
+void oracle_quantize_row_fp8(const float* x, int n, uint8_t* codes, float* scale_out) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  float s = amax / 448.0f;
+  for (int i = 0; i < n; ++i) codes[i] = s != 0.0f ? oracle_f32_to_e4m3(x[i] / s) : 0;
+  *scale_out = s;
+}
+
+/* Symmetric per-row INT4 quantiser ("tinyloop Current Status", KV cache modes table: an
+ * INT4 KV mode, format not given; read as the INT8 scheme with 4-bit codes): s = max|x| / 7
+ * (float division), code = clamp(round_half_even(x / s), -7, 7). */
+void oracle_quantize_row_int4(const float* x, int n, int8_t* codes, float* scale_out) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  float s = amax / 7.0f;
+  for (int i = 0; i < n; ++i) {
+    float r = s != 0.0f ? rintf(x[i] / s) : 0.0f;
+    if (r > 7.0f) r = 7.0f;
+    if (r < -7.0f) r = -7.0f;
+    codes[i] = (int8_t)r;
+  }
+  *scale_out = s;
+}
+
 /* ---------------------------------------------------------------- cache addressing */
+
+/*
+ * INT4 blocks hold two codes per byte: K [16 tokens][D/2 bytes], V [D][8 bytes] per
+ * (page, kv head).  Along a row (d for K, the token for V) every 8 consecutive elements
+ * form one little-endian 32-bit word, in which element e (0..7) occupies the 4 bits from
+ * bit 4 * ((e >> 1) + 4 * (e & 1)): even elements in the low 16 bits, odd ones in the
+ * high 16 bits.  Codes are 4-bit two's complement.
+ */
+static void int4_place(size_t row_byte0, int e_in_row, size_t* byte, int* shift) {
+  int w = e_in_row / 8, e = e_in_row % 8;
+#if ORACLE_MUTANT == 14 /* nibbles in plain element order */
+  int nib = e;
+#else
+  int nib = (e >> 1) + 4 * (e & 1);
+#endif
+  *byte = row_byte0 + 4 * (size_t)w + nib / 2;
+  *shift = 4 * (nib % 2);
+}
+static void int4_k_place(int page, int h, int off, int d, int Hkv, int P, int D, size_t* byte,
+                         int* shift) {
+  size_t blk = ((size_t)page * Hkv + h) * (size_t)P * D / 2;
+  int4_place(blk + (size_t)off * D / 2, d, byte, shift);
+}
+static void int4_v_place(int page, int h, int off, int d, int Hkv, int P, int D, size_t* byte,
+                         int* shift) {
+  size_t blk = ((size_t)page * Hkv + h) * (size_t)P * D / 2;
+  int4_place(blk + (size_t)d * P / 2, off, byte, shift);
+}
+
 
 static size_t k_index(int kv_dtype, int page, int h, int off, int d, int Hkv, int P, int D) {
   size_t blk = ((size_t)page * Hkv + h) * (size_t)P * D;
@@ -147,11 +244,24 @@ static size_t s_index(int page, int h, int off, int Hkv, int P) {
 /* Stored K or V element as a double (after dequantisation). */
 static double cache_value(const void* cache, const float* scales, int kv_dtype, int is_v,
                           int page, int h, int off, int d, int Hkv, int P, int D) {
+  if (kv_dtype == ODT_INT4) {
+    size_t byte;
+    int shift;
+    if (is_v) int4_v_place(page, h, off, d, Hkv, P, D, &byte, &shift);
+    else int4_k_place(page, h, off, d, Hkv, P, D, &byte, &shift);
+    int c = (((const uint8_t*)cache)[byte] >> shift) & 15;
+    if (c >= 8) c -= 16;
+    return (double)c * (double)scales[s_index(page, h, off, Hkv, P)];
+  }
   size_t i = is_v ? v_index(kv_dtype, page, h, off, d, Hkv, P, D)
                   : k_index(kv_dtype, page, h, off, d, Hkv, P, D);
   if (kv_dtype == ODT_INT8) {
     int8_t c = ((const int8_t*)cache)[i];
     return (double)c * (double)scales[s_index(page, h, off, Hkv, P)];
+  }
+  if (kv_dtype == ODT_FP8) {
+    uint8_t c = ((const uint8_t*)cache)[i];
+    return oracle_e4m3_value(c) * (double)scales[s_index(page, h, off, Hkv, P)];
   }
   return read_real(cache, kv_dtype, i);
 }
@@ -163,7 +273,8 @@ static double cache_value(const void* cache, const float* scales, int kv_dtype, 
  * slot = slot_mapping[i] (page = slot / P, off = slot % P) for every kv head;
  * slot < 0 means "skip this token" (padding).  The source rows are float32 or
  * bfloat16 [T][Hkv][D].  FP32 cache: stored as the float value; BF16 cache: rounded to
- * nearest even; INT8 cache: quantised per (token, head) with the quantiser above.
+ * nearest even; INT8, FP8 and INT4 caches: quantised per (token, head) with the
+ * quantisers above (INT4 codes written into their 4 bits, the rest of the byte kept).
  * Returns the number of tokens whose slot was >= num_pages * P (those are skipped).
  */
 int oracle_append(int kv_dtype, int num_pages, int P, int Hkv, int D, void* k_cache,
@@ -183,13 +294,26 @@ int oracle_append(int kv_dtype, int num_pages, int P, int Hkv, int D, void* k_ca
         void* dst = is_v ? v_cache : k_cache;
         for (int d = 0; d < D; ++d)
           row[d] = read_real_f(src, new_dtype, ((size_t)i * Hkv + h) * D + d);
-        if (kv_dtype == ODT_INT8) {
+        if (kv_dtype == ODT_INT8 || kv_dtype == ODT_FP8) {
           float s;
-          oracle_quantize_row_int8(row, D, codes, &s);
+          if (kv_dtype == ODT_INT8) oracle_quantize_row_int8(row, D, codes, &s);
+          else oracle_quantize_row_fp8(row, D, (uint8_t*)codes, &s);
           for (int d = 0; d < D; ++d) {
             size_t j = is_v ? v_index(kv_dtype, page, h, off, d, Hkv, P, D)
                             : k_index(kv_dtype, page, h, off, d, Hkv, P, D);
             ((int8_t*)dst)[j] = codes[d];
+          }
+          (is_v ? v_scale : k_scale)[s_index(page, h, off, Hkv, P)] = s;
+        } else if (kv_dtype == ODT_INT4) {
+          float s;
+          oracle_quantize_row_int4(row, D, codes, &s);
+          for (int d = 0; d < D; ++d) {
+            size_t byte;
+            int shift;
+            if (is_v) int4_v_place(page, h, off, d, Hkv, P, D, &byte, &shift);
+            else int4_k_place(page, h, off, d, Hkv, P, D, &byte, &shift);
+            uint8_t* bp = (uint8_t*)dst + byte;
+            *bp = (uint8_t)((*bp & ~(15 << shift)) | ((codes[d] & 15) << shift));
           }
           (is_v ? v_scale : k_scale)[s_index(page, h, off, Hkv, P)] = s;
         } else {

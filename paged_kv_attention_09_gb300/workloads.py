@@ -24,8 +24,8 @@ from typing import Optional
 import numpy as np
 import torch
 
-F32, BF16, INT8 = 0, 1, 2
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", INT8: "int8"}
+F32, BF16, INT8, FP8, INT4 = 0, 1, 2, 3, 4
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", INT8: "int8", FP8: "fp8", INT4: "int4"}
 PAGE_SIZE = 16
 
 

@@ -19,7 +19,7 @@ import pytest
 import torch
 
 import oracle
-from oracle import BF16, F32, INT8, HostCache
+from oracle import BF16, F32, FP8, INT4, INT8, QUANTISED, HostCache
 from paged_kv_attention_09_gb300 import workloads as W
 
 P = 16
@@ -45,21 +45,54 @@ def v_elem(dtype, t, d, D):
     return d * P + t
 
 
+def e4m3_torch(x):
+    """float32 -> FP8 E4M3 codes by the library cast (round to nearest even)."""
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def e4m3_decode_torch(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def int4_codes(rows):
+    """Unpack INT4 rows (uint8 [..., n/2]) into codes [..., n] by the documented layout:
+    every 8 consecutive elements form a little-endian 32-bit word in which element e sits
+    at bit 4 * ((e >> 1) + 4 * (e & 1)); 4-bit two's complement."""
+    b = rows.reshape(*rows.shape[:-1], -1, 4).astype(np.uint32)
+    word = b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24)
+    e = np.arange(8, dtype=np.uint32)
+    nib = ((word[..., None] >> (4 * ((e >> 1) + 4 * (e & 1)))) & 15).astype(np.int64)
+    return np.where(nib >= 8, nib - 16, nib).reshape(*rows.shape[:-1], -1)
+
+
+def stored_codes(cache: HostCache):
+    """K [NP,Hkv,P,D] and V [NP,Hkv,D,P] element arrays as stored (codes for FP8/INT4
+    decoded to their E4M3 values / integers, before the per-token scale)."""
+    if cache.kv_dtype == FP8:
+        return e4m3_decode_torch(cache.k), e4m3_decode_torch(cache.v)
+    if cache.kv_dtype == INT4:
+        return int4_codes(cache.k), int4_codes(cache.v)
+    return cache.k, cache.v
+
+
 def logical_kv(cache: HostCache, bt_row, L, g):
     """Reassemble logical K/V [L, D] (float64, dequantised) from the documented layout."""
     t = np.arange(L)
     pages, offs = bt_row[t // P], t % P
     D = cache.head_dim
     dd = np.arange(D)[None, :]
-    kf = cache.k.reshape(cache.num_pages, cache.num_kv_heads, -1)
-    vf = cache.v.reshape(cache.num_pages, cache.num_kv_heads, -1)
+    ks, vs = stored_codes(cache)
+    kf = ks.reshape(cache.num_pages, cache.num_kv_heads, -1)
+    vf = vs.reshape(cache.num_pages, cache.num_kv_heads, -1)
     k = kf[pages[:, None], g, k_elem(cache.kv_dtype, offs[:, None], dd, D)]
     v = vf[pages[:, None], g, v_elem(cache.kv_dtype, offs[:, None], dd, D)]
     if cache.kv_dtype == BF16:
         k, v = bf16_to_f32(k), bf16_to_f32(v)
     k = k.astype(np.float64)
     v = v.astype(np.float64)
-    if cache.kv_dtype == INT8:
+    if cache.kv_dtype in QUANTISED:
         k = k * cache.k_scale[pages, g, offs].astype(np.float64)[:, None]
         v = v * cache.v_scale[pages, g, offs].astype(np.float64)[:, None]
     return k, v
@@ -183,6 +216,92 @@ def test_int8_quantiser_nearest_code_and_ties():
     assert check_quantiser()
 
 
+# --------------------------------------------------------------------------- FP8 / INT4
+
+def check_e4m3():
+    """The E4M3 decoder against the library's float8 type for all 256 codes, and the
+    encoder against the library cast on random values, every tie and the subnormals."""
+    codes = np.arange(256, dtype=np.uint8)
+    ours, ref = oracle.e4m3_value(codes), e4m3_decode_torch(codes)
+    nan = np.isnan(ref)
+    if not (np.array_equal(np.isnan(ours), nan) and np.array_equal(ours[~nan], ref[~nan])):
+        return False
+    rng = np.random.default_rng(21)
+    fin = np.array([oracle.e4m3_value(c)[0] for c in range(127)])
+    mids = ((fin[:-1] + fin[1:]) / 2).astype(np.float32)  # exact ties
+    x = np.concatenate([
+        (rng.standard_normal(3000) * 10.0 ** rng.uniform(-4, 2.3, 3000)).astype(np.float32),
+        mids, -mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(500)),
+        (rng.uniform(0, 2.0 ** -6, 300)).astype(np.float32),  # subnormal range
+        np.array([0.0, -0.0, 448.0, -448.0, 2.0 ** -10, -(2.0 ** -10)], np.float32),
+    ])
+    x = x[np.abs(x) <= 448]
+    if not np.array_equal(oracle.f32_to_e4m3(x), e4m3_torch(x)):
+        return False
+    # saturation beyond the largest finite value (the encoder's choice; the library cast
+    # gives NaN there)
+    return list(oracle.f32_to_e4m3([449.0, 1e6, -3e4])) == [0x7E, 0x7E, 0xFE]
+
+
+def test_e4m3_codec_matches_library_float8():
+    assert check_e4m3()
+
+
+def check_quantisers_fp8_int4():
+    rng = np.random.default_rng(13)
+    cand = np.arange(-7, 8, dtype=np.float64)
+    for trial in range(200):
+        n = 64 if trial % 2 == 0 else 128
+        x = (rng.standard_normal(n) * (10.0 ** rng.uniform(-3, 3))).astype(np.float32)
+        amax = np.max(np.abs(x))
+        c4, s4 = oracle.quantize_row_int4(x)
+        if s4 != np.float32(amax) / np.float32(7.0) or np.abs(c4[np.argmax(np.abs(x))]) != 7:
+            return False
+        r = x.astype(np.float64) / np.float64(s4)
+        best = np.abs(r[:, None] - cand[None, :]).min(axis=1)
+        if np.any(np.abs(r - c4) > best + 1e-5) or np.any(np.abs(c4) > 7):
+            return False
+        c8, s8 = oracle.quantize_row_fp8(x)
+        if s8 != np.float32(amax) / np.float32(448.0):
+            return False
+        q = np.clip(x / s8, np.float32(-448), np.float32(448))  # float32 division
+        if not np.array_equal(c8, e4m3_torch(q)):
+            return False
+    x = np.zeros(64, np.float32)
+    x[:7] = [7.0, 2.5, 3.5, -2.5, -0.5, 0.5, 1.5]  # s = 1: halves go to the even code
+    c4, s4 = oracle.quantize_row_int4(x)
+    if s4 != 1.0 or list(c4[:7]) != [7, 2, 4, -2, 0, 0, 2]:
+        return False
+    c4, s4 = oracle.quantize_row_int4(np.zeros(64, np.float32))
+    c8, s8 = oracle.quantize_row_fp8(np.zeros(64, np.float32))
+    return s4 == 0 and s8 == 0 and not c4.any() and not c8.any()
+
+
+def test_fp8_int4_quantisers():
+    assert check_quantisers_fp8_int4()
+
+
+def test_append_fp8_int4_stored_values():
+    """Stored codes and scales of every appended row, read back through the documented
+    layout (INT4: two codes per byte, the other element of each byte untouched)."""
+    for kv in (FP8, INT4):
+        wl = W.small_workload(7 + kv, num_q_heads=2, num_kv_heads=2, head_dim=64, kv_dtype=kv,
+                              q_dtype=F32, decode_lens=[33, 20])
+        c = oracle.cache_from_workload(wl)
+        qz = oracle.quantize_row_fp8 if kv == FP8 else oracle.quantize_row_int4
+        if kv == FP8:
+            ks, vs = c.k, c.v
+        else:
+            ks, vs = int4_codes(c.k), int4_codes(c.v)
+        for i in range(wl.slots.shape[0]):
+            pg, off = divmod(int(wl.slots[i]), P)
+            for h in range(2):
+                codes, s = qz(wl.k_src[i, h])
+                assert np.array_equal(ks[pg, h, off], codes) and c.k_scale[pg, h, off] == s
+                codes, s = qz(wl.v_src[i, h])
+                assert np.array_equal(vs[pg, h, :, off], codes) and c.v_scale[pg, h, off] == s
+
+
 # --------------------------------------------------------------------------- append
 
 def test_append_places_rows_at_documented_positions():
@@ -240,6 +359,10 @@ CASES = [
     (BF16, F32, 8, 8, 64, [3, 48]),
     (INT8, F32, 32, 4, 64, [2, 16, 40]),
     (INT8, BF16, 6, 1, 128, [19, 50]),
+    (FP8, F32, 8, 2, 64, [1, 17, 40]),
+    (FP8, BF16, 6, 1, 128, [19, 33]),
+    (INT4, F32, 32, 4, 64, [2, 16, 41]),
+    (INT4, BF16, 6, 1, 128, [18, 50]),
 ]
 
 
@@ -262,7 +385,8 @@ def test_decode_matches_dense_sdpa():
 
 def check_prefill_bruteforce():
     for i, (kv, qd, Hq, Hkv, D) in enumerate([(BF16, BF16, 12, 2, 128), (F32, F32, 4, 2, 64),
-                                              (INT8, F32, 8, 2, 64)]):
+                                              (INT8, F32, 8, 2, 64), (FP8, F32, 8, 2, 64),
+                                              (INT4, BF16, 4, 1, 128)]):
         wl = W.small_workload(200 + i, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                               kv_dtype=kv, q_dtype=qd, prefill=[(20, 13), (0, 17), (33, 1)])
         c = oracle.cache_from_workload(wl)
@@ -666,10 +790,11 @@ def test_window_step_is_store_then_windowed_decode():
 PINS = [check_bf16_rounding, check_quantiser, check_decode_bruteforce,
         check_prefill_bruteforce, check_closed_forms, check_page_permutation_invariance,
         check_gqa_equals_replicated_mha, check_causality, check_rope, check_decode_step,
-        check_window_decode, check_window_prefill, check_window_step]
+        check_window_decode, check_window_prefill, check_window_step, check_e4m3,
+        check_quantisers_fp8_int4]
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14])
 def test_planted_mistake_is_caught(mutant, monkeypatch):
     path = oracle.build(defines=[f"ORACLE_MUTANT={mutant}"], name=f"liboracle_m{mutant}.so")
     monkeypatch.setattr(oracle, "_lib", oracle.load(path))
