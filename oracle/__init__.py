@@ -103,16 +103,19 @@ _CACHE = {F32: np.float32, BF16: np.uint16, INT8: np.int8, FP8: np.uint8, INT4: 
 
 class HostCache:
     """The oracle's own KV cache: K [NP,Hkv,P,D], V [NP,Hkv,D,P], scales [NP,Hkv,P]
-    (INT4: K [NP,Hkv,P,D/2], V [NP,Hkv,D,P/2] bytes, two codes per byte)."""
+    (INT4: K [NP,Hkv,P,D/2] and V [NP,Hkv,D/2,P] bytes, two codes per byte)."""
 
     def __init__(self, kv_dtype, num_pages, page_size, num_kv_heads, head_dim, fill=0):
         self.kv_dtype, self.num_pages, self.page_size = kv_dtype, num_pages, page_size
         self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
         NP, H, P, D = num_pages, num_kv_heads, page_size, head_dim
         dt = _CACHE[kv_dtype]
-        half = 2 if kv_dtype == INT4 else 1
-        self.k = np.full((NP, H, P, D // half), fill, dtype=dt)
-        self.v = np.full((NP, H, D, P // half), fill, dtype=dt)
+        if kv_dtype == INT4:  # two codes per byte: K rows of D/2, V row pairs of P bytes
+            self.k = np.full((NP, H, P, D // 2), fill, dtype=dt)
+            self.v = np.full((NP, H, D // 2, P), fill, dtype=dt)
+        else:
+            self.k = np.full((NP, H, P, D), fill, dtype=dt)
+            self.v = np.full((NP, H, D, P), fill, dtype=dt)
         if kv_dtype in QUANTISED:
             self.k_scale = np.zeros((NP, H, P), np.float32)
             self.v_scale = np.zeros((NP, H, P), np.float32)

@@ -192,11 +192,15 @@ void oracle_quantize_row_int4(const float* x, int n, int8_t* codes, float* scale
 /* ---------------------------------------------------------------- cache addressing */
 
 /*
- * INT4 blocks hold two codes per byte: K [16 tokens][D/2 bytes], V [D][8 bytes] per
- * (page, kv head).  Along a row (d for K, the token for V) every 8 consecutive elements
- * form one little-endian 32-bit word, in which element e (0..7) occupies the 4 bits from
- * bit 4 * ((e >> 1) + 4 * (e & 1)): even elements in the low 16 bits, odd ones in the
- * high 16 bits.  Codes are 4-bit two's complement.
+ * INT4 blocks hold two 4-bit two's-complement codes per byte, D * 8 bytes per block for
+ * K and for V of each (page, kv head).
+ *   K [16 tokens][D/2 bytes]: along a token's row every 8 consecutive head-dim elements
+ *     form one little-endian 32-bit word, in which element e (0..7) occupies the 4 bits
+ *     from bit 4 * ((e >> 1) + 4 * (e & 1)): even elements in the low 16 bits, odd ones
+ *     in the high 16 bits.
+ *   V [D/2 row pairs][16 bytes]: row pair p holds head-dim rows d = 16 (p / 8) + p % 8
+ *     (low 4 bits) and d + 8 (high 4 bits); token t sits at byte 4 (t / 4) +
+ *     {0, 2, 1, 3}[t % 4] of the pair's 16 bytes.  A token's bytes hold only its codes.
  */
 static void int4_place(size_t row_byte0, int e_in_row, size_t* byte, int* shift) {
   int w = e_in_row / 8, e = e_in_row % 8;
@@ -215,8 +219,15 @@ static void int4_k_place(int page, int h, int off, int d, int Hkv, int P, int D,
 }
 static void int4_v_place(int page, int h, int off, int d, int Hkv, int P, int D, size_t* byte,
                          int* shift) {
+  static const int tpos[4] = {0, 2, 1, 3};
   size_t blk = ((size_t)page * Hkv + h) * (size_t)P * D / 2;
-  int4_place(blk + (size_t)d * P / 2, off, byte, shift);
+#if ORACLE_MUTANT == 15 /* row pairs (d, d + 1) instead of (d, d + 8) */
+  int pair = d / 2, high = d % 2;
+#else
+  int pair = 8 * (d / 16) + d % 8, high = (d % 16) >= 8;
+#endif
+  *byte = blk + (size_t)pair * P + 4 * (off / 4) + tpos[off % 4];
+  *shift = 4 * high;
 }
 
 

@@ -57,7 +57,7 @@ def e4m3_decode_torch(codes):
 
 
 def int4_codes(rows):
-    """Unpack INT4 rows (uint8 [..., n/2]) into codes [..., n] by the documented layout:
+    """Unpack INT4 K rows (uint8 [..., n/2]) into codes [..., n] by the documented layout:
     every 8 consecutive elements form a little-endian 32-bit word in which element e sits
     at bit 4 * ((e >> 1) + 4 * (e & 1)); 4-bit two's complement."""
     b = rows.reshape(*rows.shape[:-1], -1, 4).astype(np.uint32)
@@ -67,13 +67,29 @@ def int4_codes(rows):
     return np.where(nib >= 8, nib - 16, nib).reshape(*rows.shape[:-1], -1)
 
 
+def int4_v_codes(v):
+    """Unpack an INT4 V cache (uint8 [NP, Hkv, D/2, 16]) into codes [NP, Hkv, D, 16]: row
+    pair p holds head-dim rows 16 (p // 8) + p % 8 (low 4 bits) and that + 8 (high 4
+    bits); token t at byte 4 (t // 4) + (0, 2, 1, 3)[t % 4]."""
+    NP, H, D2, T = v.shape
+    t = np.arange(T)
+    byt = v[..., 4 * (t // 4) + np.array([0, 2, 1, 3])[t % 4]].astype(np.int64)  # [.., p, t]
+    lo, hi = byt & 15, byt >> 4
+    out = np.empty((NP, H, 2 * D2, T), np.int64)
+    p = np.arange(D2)
+    d0 = 16 * (p // 8) + p % 8
+    out[:, :, d0, :] = lo
+    out[:, :, d0 + 8, :] = hi
+    return np.where(out >= 8, out - 16, out)
+
+
 def stored_codes(cache: HostCache):
     """K [NP,Hkv,P,D] and V [NP,Hkv,D,P] element arrays as stored (codes for FP8/INT4
     decoded to their E4M3 values / integers, before the per-token scale)."""
     if cache.kv_dtype == FP8:
         return e4m3_decode_torch(cache.k), e4m3_decode_torch(cache.v)
     if cache.kv_dtype == INT4:
-        return int4_codes(cache.k), int4_codes(cache.v)
+        return int4_codes(cache.k), int4_v_codes(cache.v)
     return cache.k, cache.v
 
 
@@ -292,7 +308,7 @@ def test_append_fp8_int4_stored_values():
         if kv == FP8:
             ks, vs = c.k, c.v
         else:
-            ks, vs = int4_codes(c.k), int4_codes(c.v)
+            ks, vs = int4_codes(c.k), int4_v_codes(c.v)
         for i in range(wl.slots.shape[0]):
             pg, off = divmod(int(wl.slots[i]), P)
             for h in range(2):
@@ -794,7 +810,7 @@ PINS = [check_bf16_rounding, check_quantiser, check_decode_bruteforce,
         check_quantisers_fp8_int4]
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15])
 def test_planted_mistake_is_caught(mutant, monkeypatch):
     path = oracle.build(defines=[f"ORACLE_MUTANT={mutant}"], name=f"liboracle_m{mutant}.so")
     monkeypatch.setattr(oracle, "_lib", oracle.load(path))
