@@ -59,14 +59,23 @@ def parse():
 # ----------------------------------------------------------------------------- bytes
 
 def esz(code):
-    return {0: 4, 1: 2, 2: 1}[code]
+    """Bytes per element of a source (new-row) dtype: float32 or bfloat16."""
+    return {0: 4, 1: 2}[code]
+
+
+def kv_token_bytes(wl):
+    """Cache bytes of one token over all kv heads: its K and V rows, plus the two FP32
+    scales of the coded formats (INT8, FP8 one byte per element; INT4 half a byte)."""
+    D = wl.head_dim
+    row = {0: 4 * D, 1: 2 * D, 2: D, 3: D, 4: D // 2}[wl.kv_dtype]
+    return wl.num_kv_heads * (2 * row + (8 if wl.kv_dtype in (2, 3, 4) else 0))
 
 
 def decode_bytes(wl, b):
-    """Algorithmic HBM bytes of one decode call: every cached token's K and V (and INT8
-    scales) once, q, out, the used block-table entries and the lengths."""
+    """Algorithmic HBM bytes of one decode call: every cached token's K and V (and the
+    coded formats' scales) once, q, out, the used block-table entries and the lengths."""
     Hkv, D, Hq = wl.num_kv_heads, wl.head_dim, wl.num_q_heads
-    per_tok = Hkv * D * esz(wl.kv_dtype) * 2 + (Hkv * 8 if wl.kv_dtype == 2 else 0)
+    per_tok = kv_token_bytes(wl)
     toks = int(b.context_lens.sum())
     pages = int(sum(math.ceil(int(L) / 16) for L in b.context_lens))
     qb = b.q.size * (2 if b.q.dtype == np.uint16 else 4)
@@ -75,7 +84,7 @@ def decode_bytes(wl, b):
 
 def prefill_bytes(wl, b):
     Hkv, D, Hq = wl.num_kv_heads, wl.head_dim, wl.num_q_heads
-    per_tok = Hkv * D * esz(wl.kv_dtype) * 2
+    per_tok = kv_token_bytes(wl)
     toks = int(b.context_lens.sum())
     pages = int(sum(math.ceil(int(L) / 16) for L in b.context_lens))
     qb = b.q.size * (2 if b.q.dtype == np.uint16 else 4)
@@ -95,7 +104,7 @@ def append_bytes(wl):
     T = int(wl.step_rows.shape[0])
     Hkv, D = wl.num_kv_heads, wl.head_dim
     src = T * Hkv * D * esz(wl.new_dtype) * 2
-    dst = T * Hkv * D * esz(wl.kv_dtype) * 2 + (T * Hkv * 8 if wl.kv_dtype == 2 else 0)
+    dst = T * kv_token_bytes(wl)
     return src + dst + T * 4
 
 
@@ -234,8 +243,7 @@ def cpu_oracle_rate(wl, seconds, threads, fused=True, rope=False):
                 break
             n = max(n + 1, min(B, int(n * max(2.0, 0.8 * seconds / len(wl.batches) / max(dt, 1e-3)))))
         toks = int(sum(int(b.context_lens[s]) for s in seqs))
-        per_tok = wl.num_kv_heads * wl.head_dim * esz(wl.kv_dtype) * 2 + \
-            (wl.num_kv_heads * 8 if wl.kv_dtype == 2 else 0)
+        per_tok = kv_token_bytes(wl)
         done_bytes += toks * per_tok
         done_tok += toks
         t_total += dt
@@ -272,9 +280,7 @@ def run_ours(args, rank, world):
     reps = [base]
     for _ in range(R - 1):
         c = base.cache
-        cache = pkv.KVCache(c.k.clone(), c.v.clone(),
-                            None if c.k_scale is None else c.k_scale.clone(),
-                            None if c.v_scale is None else c.v_scale.clone())
+        cache = c.clone()
         batches = [runner.DeviceBatch(b.kind, b.q.clone(), b.block_tables.clone(),
                                       b.context_lens.clone(),
                                       None if b.q_start_loc is None else b.q_start_loc.clone(),
@@ -427,13 +433,14 @@ def main():
     K = args.steps
     names = (["append"] if n_append else []) + [b.kind for b in wl.batches]
     avg = {n: statistics.fmean(v) for n, v in zip(names, kern_ms)}
+    from paged_kv_attention_09_gb300 import workloads as W
     peak, peak_kind = measured_hbm()
     value = acc["total"] * world / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {0: "f32", 1: "bf16", 2: "int8"}[wl.kv_dtype] + "-kv/f32-acc",
+        "dtype": W.DTYPE_NAMES[wl.kv_dtype] + "-kv/f32-acc",
         "data": "synthetic (seeded N(0,1) values, shapes of the named model family)",
         "config": {
             "workload": wl.name, "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
@@ -505,7 +512,7 @@ def main_reference(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "impl": "reference",
-            "dtype": {0: "f64", 1: "f64", 2: "f64"}[wl.kv_dtype],
+            "dtype": "f64",
             "data": "synthetic (seeded N(0,1) values, shapes of the named model family)",
             "config": {"workload": wl.name, "num_q_heads": wl.num_q_heads,
                        "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim},

@@ -39,17 +39,30 @@
  * Cache layout (struct pkv_cache).  Each (page, kv head) pair owns one K block and one
  * V block of page_size * head_dim elements; block (page, h) starts at element
  * (page * num_kv_heads + h) * page_size * head_dim of k_cache / v_cache.
- *   FP32, INT8:  K element (token t, column d) at t * head_dim + d        (row per token)
+ *   FP32, INT8, FP8:
+ *                K element (token t, column d) at t * head_dim + d        (row per token)
  *                V element (token t, column d) at d * page_size + t       (transposed)
+ *   INT4 (two codes per byte; a block is page_size * head_dim / 2 bytes):
+ *                K: token t's row is head_dim / 2 bytes at t * head_dim / 2; every 8
+ *                   consecutive columns form a little-endian 32-bit word in which column
+ *                   8w + e sits at bit 4 * ((e >> 1) + 4 * (e & 1)) (even columns in the
+ *                   low half-word, odd ones in the high half-word)
+ *                V: row pair p (16 bytes at p * 16) holds columns d = 16 (p / 8) + p % 8
+ *                   (low 4 bits) and d + 8 (high 4 bits); token t at byte 4 (t / 4) +
+ *                   {0, 2, 1, 3}[t % 4] of the pair (a token's bytes hold only its codes)
  *   BF16 (tensor-core tiles: 8 x 8 core matrices of 64 contiguous elements, so a block
  *         is directly an MMA operand tile):
  *                K element (t, d) at ((t/8) * (head_dim/8) + d/8) * 64 + (t%8) * 8 + d%8
  *                V element (t, d) at ((d/8) * 2 + t/8) * 64 + (d%8) * 8 + t%8
- *   k_scale, v_scale  float32 [num_pages][num_kv_heads][page_size]   INT8 only
+ *   k_scale, v_scale  float32 [num_pages][num_kv_heads][page_size]   INT8, FP8, INT4
  *   Token t of a sequence lives in page block_tables[b][t / page_size] at offset
  *   t % page_size; its slot number is page * page_size + offset.
- *   Element types: PKV_F32 float32, PKV_BF16 bfloat16, PKV_INT8 int8 code c whose value
- *   is c * scale, scale = max|x| / 127 per (token, kv head).
+ *   Element types: PKV_F32 float32, PKV_BF16 bfloat16, and three coded formats whose
+ *   value is code * scale with one scale per (token, kv head): PKV_INT8 int8 codes,
+ *   scale = max|x| / 127; PKV_FP8 E4M3 codes (OCP "fn": bias 7, no infinity, largest
+ *   finite 448), scale = max|x| / 448; PKV_INT4 4-bit two's-complement codes in
+ *   [-7, 7], scale = max|x| / 7 ("tinyloop Current Status", KV cache modes table: INT8
+ *   and INT4 KV caches; the TinyInfer review, item 2: INT8 or FP8 KV cache).
  *   All cache pointers must be 16-byte aligned.
  *
  * Sliding window (pkv_cache.window; "tinyloop Current Status", KV cache modes table: a
@@ -71,7 +84,7 @@
 extern "C" {
 #endif
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_INT8 = 2 } pkv_dtype;
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_INT8 = 2, PKV_FP8 = 3, PKV_INT4 = 4 } pkv_dtype;
 
 typedef enum {
   PKV_OK = 0,
@@ -96,8 +109,8 @@ typedef enum {
 typedef struct pkv_cache {
   void* k_cache;
   void* v_cache;
-  float* k_scale; /* INT8 only, else NULL */
-  float* v_scale; /* INT8 only, else NULL */
+  float* k_scale; /* INT8, FP8, INT4 only, else NULL */
+  float* v_scale; /* INT8, FP8, INT4 only, else NULL */
   int32_t num_pages;
   int32_t page_size;
   int32_t num_kv_heads;
@@ -111,10 +124,11 @@ typedef struct pkv_cache {
  * Status": INT8 KV cache).
  *   k_new, v_new   [num_tokens][num_kv_heads][head_dim], element type new_dtype
  *                  (PKV_F32 or PKV_BF16).  FP32 cache: stored as is (BF16 widened
- *                  exactly).  BF16 cache: rounded to nearest even.  INT8 cache: per
- *                  (token, kv head) s = max|x| / 127 (IEEE division), code =
- *                  clamp(rint(x / s), -127, 127), s and codes stored; an all-zero row
- *                  stores s = 0 and zero codes.
+ *                  exactly).  BF16 cache: rounded to nearest even.  INT8 / INT4 cache:
+ *                  per (token, kv head) s = max|x| / R (IEEE division, R = 127 / 7),
+ *                  code = clamp(rint(x / s), -R, R), s and codes stored.  FP8 cache:
+ *                  s = max|x| / 448, code = E4M3(x / s) rounded to nearest even,
+ *                  saturating at +-448.  An all-zero row stores s = 0 and zero codes.
  *   slot_mapping   int32 [num_tokens]; slot < 0 skips that token (padding);
  *                  slot >= num_pages * page_size sets PKV_DEV_BAD_SLOT and is skipped.
  *   Slots within one call must be distinct.  num_tokens == 0 is a no-op.

@@ -18,14 +18,14 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 pkv_status check_cache(const pkv_cache* c) {
   if (!c || !c->k_cache || !c->v_cache) return PKV_ERR_NULL;
-  if (c->kv_dtype < PKV_F32 || c->kv_dtype > PKV_INT8) return PKV_ERR_DTYPE;
+  if (c->kv_dtype < PKV_F32 || c->kv_dtype > PKV_INT4) return PKV_ERR_DTYPE;
   if (c->page_size != 16) return PKV_ERR_PAGE_SIZE;
   if (c->num_pages < 1 || c->num_kv_heads < 1 || c->head_dim < 1) return PKV_ERR_SHAPE;
   if (c->window < 0) return PKV_ERR_SHAPE;
   if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (c->kv_dtype == PKV_INT8 && (!c->k_scale || !c->v_scale)) return PKV_ERR_NULL;
+  if (pkv::quantised(c->kv_dtype) && (!c->k_scale || !c->v_scale)) return PKV_ERR_NULL;
   if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PKV_ERR_ALIGN;
-  if (c->kv_dtype == PKV_INT8 && (!aligned16(c->k_scale) || !aligned16(c->v_scale)))
+  if (pkv::quantised(c->kv_dtype) && (!aligned16(c->k_scale) || !aligned16(c->v_scale)))
     return PKV_ERR_ALIGN;
   // every page block must stay addressable with 32-bit slot numbers
   if (static_cast<long long>(c->num_pages) * c->page_size > 0x7fffffffLL) return PKV_ERR_SHAPE;

@@ -1,9 +1,11 @@
 // append.cu — KV append: scatter new tokens' K/V rows into their cache slots.
 //
 // "Tiny-LLM-Inference Project_Status" (feature list: paged KV cache; dtype contract:
-// FP32 or BF16 KV) and "tinyloop Current Status" (KV cache modes table: INT8 KV cache).
-// One warp per (token, kv head) writes both the K row and the V column of that slot;
-// INT8 rows go through the shared quantiser (kvrow.cuh).
+// FP32 or BF16 KV), "tinyloop Current Status" (KV cache modes table: INT8 and INT4 KV
+// caches) and the TinyInfer review (item 2: INT8 or FP8 KV cache).  One warp per (token,
+// kv head) writes both the K row and the V column of that slot; quantised rows go through
+// the shared quantisers (kvrow.cuh).  INT4 K rows are written as whole 32-bit words and
+// INT4 V bytes belong to one token each, so tokens of one call never share a byte.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -46,6 +48,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const size_t blk = static_cast<size_t>(page) * Hkv + h;  // (page, head) block index
   const size_t k_row = (blk * kPage + off) * D;            // K: [P][D] inside the block
   const size_t v_base = blk * D * kPage + off;             // V: [D][P] inside the block
+  // (INT4: D/2 bytes per K row and D/2 row pairs of 16 bytes per V block)
 
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
@@ -54,10 +57,35 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int e = 0; e < E; ++e) x[e] = load_src<NEW_DT>(src, src_row + lane * E + e);
 
-    if constexpr (KV_DT == kINT8) {
+    if constexpr (KV_DT == kINT4) {
       int8_t code[E];
-      const float s = quantize_row_int8<E>(x, code);
-      int8_t* dst = static_cast<int8_t*>(which ? v_cache : k_cache);
+      const float s = quantize_row_int4<E>(x, code);
+      uint8_t* dst = static_cast<uint8_t*>(which ? v_cache : k_cache) + blk * kPage * (D / 2);
+      if (which == 0) {
+        const uint32_t w = int4_k_word<E>(code, lane);
+        if ((lane & (8 / E - 1)) == 0)
+          reinterpret_cast<uint32_t*>(dst + off * (D / 2))[lane * E / 8] = w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int d = lane * E + e;
+          const uint8_t b = int4_v_byte<E>(code, e);
+          if ((d & 15) < 8) dst[int4_v_pair(d) * kPage + int4_v_tpos(off)] = b;
+        }
+      }
+      if (lane == 0) (which ? v_scale : k_scale)[blk * kPage + off] = s;
+    } else if constexpr (KV_DT == kINT8 || KV_DT == kFP8) {
+      uint8_t code[E];
+      float s;
+      if constexpr (KV_DT == kINT8) {
+        int8_t c8[E];
+        s = quantize_row_int8<E>(x, c8);
+#pragma unroll
+        for (int e = 0; e < E; ++e) code[e] = static_cast<uint8_t>(c8[e]);
+      } else {
+        s = quantize_row_fp8<E>(x, code);
+      }
+      uint8_t* dst = static_cast<uint8_t*>(which ? v_cache : k_cache);
       if (which == 0) {
 #pragma unroll
         for (int e = 0; e < E; ++e) dst[k_row + lane * E + e] = code[e];
@@ -119,11 +147,23 @@ cudaError_t launch_append(const CacheView& c, void* k_cache, void* v_cache, floa
                                          slots, T, c.Hkv, c.num_pages, dev_status)
                 : launch_t<kBF16, kF32>(c.D, grid, st, k_cache, v_cache, ks, vs, k_new, v_new,
                                         slots, T, c.Hkv, c.num_pages, dev_status);
-    default:
+    case kINT8:
       return nb ? launch_t<kINT8, kBF16>(c.D, grid, st, k_cache, v_cache, ks, vs, k_new, v_new,
                                          slots, T, c.Hkv, c.num_pages, dev_status)
                 : launch_t<kINT8, kF32>(c.D, grid, st, k_cache, v_cache, ks, vs, k_new, v_new,
                                         slots, T, c.Hkv, c.num_pages, dev_status);
+    case kFP8:
+      return nb ? launch_t<kFP8, kBF16>(c.D, grid, st, k_cache, v_cache, ks, vs, k_new, v_new,
+                                        slots, T, c.Hkv, c.num_pages, dev_status)
+                : launch_t<kFP8, kF32>(c.D, grid, st, k_cache, v_cache, ks, vs, k_new, v_new,
+                                       slots, T, c.Hkv, c.num_pages, dev_status);
+    case kINT4:
+      return nb ? launch_t<kINT4, kBF16>(c.D, grid, st, k_cache, v_cache, ks, vs, k_new, v_new,
+                                         slots, T, c.Hkv, c.num_pages, dev_status)
+                : launch_t<kINT4, kF32>(c.D, grid, st, k_cache, v_cache, ks, vs, k_new, v_new,
+                                        slots, T, c.Hkv, c.num_pages, dev_status);
+    default:
+      return cudaErrorInvalidValue;
   }
 }
 

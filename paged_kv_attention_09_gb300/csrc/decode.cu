@@ -27,6 +27,10 @@
 //   INT8 KV — f16 MMA for both products.  Codes become the exact f16 values 1152 + code
 //             with one xor and two byte permutes (no subtraction); the bias is removed
 //             afterwards: 1152 * sum(q) from each score, 1152 * sum(P) from the output.
+//             FP8 (E4M3) and INT4 KV take the same path: E4M3 codes convert to their exact
+//             f16 values (no bias), INT4 codes to 1032 + code with one mask-and-xor per
+//             pair (the TinyInfer review, item 2; "tinyloop Current Status", KV cache modes
+//             table).
 //             Queries are scaled by a power of two into [0.5, 1) and split hi/lo in f16
 //             (rows 0-7 / 8-15); per-token K scales multiply the scores and V scales the
 //             probabilities (split hi/lo) in FP32.  (The s8 MMA path is far slower on
@@ -82,9 +86,10 @@ struct DParams {
   double inv_freq[kMaxHeadDim / 2];
 };
 
-template <int KVT>
-struct ElemSize {
-  static constexpr int value = KVT == kF32 ? 4 : (KVT == kBF16 ? 2 : 1);
+// Bytes of one stored K row (one token, one kv head); a V block has as many per token.
+template <int KVT, int D>
+struct RowBytes {
+  static constexpr int value = KVT == kF32 ? 4 * D : KVT == kBF16 ? 2 * D : KVT == kINT4 ? D / 2 : D;
 };
 
 // Pages per iteration of a warp, stages (iterations in flight) per warp, and the
@@ -102,22 +107,21 @@ struct ElemSize {
 #endif
 template <int KVT, int D>
 struct Tune {
-  static constexpr int PPI = KVT == kINT8 ? PKV_INT8_PPI : 1;
-  static constexpr int S = KVT == kINT8 ? PKV_INT8_STAGES
+  static constexpr int PPI = quantised(KVT) ? PKV_INT8_PPI : 1;
+  static constexpr int S = quantised(KVT) ? PKV_INT8_STAGES
                          : KVT == kBF16 ? (D == 64 ? 3 : PKV_BF16_STAGES)
                                         : (D == 64 ? 3 : 2);
   // Warps per block.  (Three-warp INT8 blocks, which leave 96 registers at 7 blocks per
   // SM, measured slower than four warps at 72 registers.)
   static constexpr int W = 4;
-  static constexpr int minBlocks = (KVT == kINT8 && D == 64) ? 7 : (KVT == kBF16 && D == 128) ? 3 : 1;
+  static constexpr int minBlocks = (quantised(KVT) && D == 64) ? 7 : (KVT == kBF16 && D == 128) ? 3 : 1;
 };
 
 template <int KVT, int D>
 struct Layout {
-  static constexpr int esz = ElemSize<KVT>::value;
-  static constexpr int kBytes = kPage * D * esz;               // K block of one (page, head)
-  static constexpr int vBytes = kPage * D * esz;               // V block of one (page, head)
-  static constexpr int sBytes = KVT == kINT8 ? kPage * 4 : 0;  // one scale vector
+  static constexpr int kBytes = kPage * RowBytes<KVT, D>::value;   // K block of one (page, head)
+  static constexpr int vBytes = kBytes;                            // V block of one (page, head)
+  static constexpr int sBytes = quantised(KVT) ? kPage * 4 : 0;  // one scale vector
   static constexpr int pageBytes = kBytes + vBytes + 2 * sBytes;
   static constexpr int PPI = Tune<KVT, D>::PPI;
   static constexpr int S = Tune<KVT, D>::S;
@@ -135,13 +139,13 @@ struct Smem {
   static constexpr int probs = KVT == kF32 ? kW * kMaxHeads * kPage * 4 : 0;
   // INT8: the query fragments (one uint4 per k-step and lane) and per-row constants,
   // built once by warp 0 and read by every warp
-  static constexpr int aux = KVT == kINT8 ? (D / 16) * 32 * 16 + 2 * kMaxHeads * 4 : 0;
+  static constexpr int aux = quantised(KVT) ? (D / 16) * 32 * 16 + 2 * kMaxHeads * 4 : 0;
   static constexpr int bars = kW * Lo::S * 8;
   // fused step: the block's rotated query rows (float), cos and sin of the rotation
   // angles, the new token's K and V rows in storage format (+ their scales)
   static constexpr int stepQ = STEP ? kMaxHeads * D * 4 : 0;
   static constexpr int stepRope = STEP ? D * 4 : 0;
-  static constexpr int stepRow = STEP ? 2 * (D * ElemSize<KVT>::value + 16) : 0;
+  static constexpr int stepRow = STEP ? 2 * (RowBytes<KVT, D>::value + 16) : 0;
   static constexpr int step0 = big + probs + aux + bars;
   static constexpr int total = step0 + stepQ + stepRope + stepRow;
 };
@@ -179,6 +183,28 @@ __device__ __forceinline__ void s8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, u
   const uint32_t biased = w ^ 0x80808080u;
   asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(biased), "r"(0x64646464u));
   asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(biased), "r"(0x64646464u));
+}
+
+// Four E4M3 codes (a 32-bit word) -> two f16x2 words holding their exact values (every
+// E4M3 value is an f16 value); byte b lands in half b % 2 of word b / 2.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const __half2_raw a =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+  const __half2_raw b =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
+  lo = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
+  hi = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+}
+
+// The INT4 codes at bits 4k .. 4k+3 and 16+4k .. 19+4k of w -> an f16x2 word holding
+// (24 + code) / 16 exactly: the nibble, its sign bit flipped (code + 8), becomes the top
+// four mantissa bits of 1.0.  (Placing it in the low mantissa bits of 1024 would cost no
+// shift, but its bias of 1032 would dominate the FP32 accumulator of P.V over long
+// contexts: a bias of 24 code units keeps the accumulator within ~7x of the signal.)
+template <int K>
+__device__ __forceinline__ uint32_t s4x2_to_f16x2_biased(uint32_t w) {
+  const uint32_t x = K <= 1 ? (w << (6 - 4 * K)) : (w >> (4 * K - 6));
+  return (x & 0x03C003C0u) ^ 0x3E003E00u;
 }
 
 // ------------------------------------------------------------------ FP32 (CUDA cores)
@@ -475,13 +501,21 @@ struct Bf16Warp {
   }
 };
 
-// ------------------------------------------------------------------ INT8 (f16 MMA)
+// ------------------------------------------------------------------ INT8 / FP8 / INT4 (f16 MMA)
 
-template <int D>
-struct Int8Warp {
+// One path for the three coded formats: the codes become exact f16 MMA operands.
+//   INT8  1152 + code (xor + two byte permutes per 4 codes); bias removed afterwards
+//   INT4  (24 + code) / 16 (one shift and one mask-and-xor per 2 codes); the factor 16
+//         goes into the score scale and the probabilities, the bias is removed afterwards
+//   FP8   the E4M3 value itself (hardware conversion, 2 codes per instruction), no bias
+template <int KVT, int D>
+struct QuantWarp {
   static constexpr int KS = D / 16;  // k-steps of the q.k product
   static constexpr int MT = D / 16;  // m-tiles (16 head-dim rows) of O^T = V^T P^T
-  static constexpr int PPI = Tune<kINT8, D>::PPI;  // pages per iteration
+  static constexpr int PPI = Tune<KVT, D>::PPI;  // pages per iteration
+  // the operands are 2^kMulLog2 (kBias + code)
+  static constexpr float kBias = KVT == kINT8 ? 1152.f : KVT == kINT4 ? 24.f : 0.f;
+  static constexpr int kMulLog2 = KVT == kINT4 ? -4 : 0;
   const uint4* qs;                   // [k-step][lane] f16 A fragments of the query rows
                                      // (hi 0-7, lo 8-15), in shared memory
   // O^T accumulators: lane (r, c) holds head-dim rows 16 mt + r and 16 mt + r + 8 of
@@ -541,8 +575,8 @@ struct Int8Warp {
       qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
       qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
       if (c == 0) {
-        rowc[r] = ldexpf(p.scale_log2, e);
-        rowc[kMaxHeads + r] = 1152.f * qsum;  // K entered the MMA as 1152 + code
+        rowc[r] = ldexpf(p.scale_log2, e - kMulLog2);
+        rowc[kMaxHeads + r] = ldexpf(kBias, kMulLog2) * qsum;  // K entered as 2^m (kBias + code)
       }
     }
     m = -CUDART_INF_F;
@@ -562,7 +596,7 @@ struct Int8Warp {
   // valid 0 was not loaded and its stage memory is stale); the first lo tokens of page 0
   // are before a sliding window and are not attended.
   __device__ void pages(const uint8_t* st, const int (&valid)[PPI], int lo, int lane) {
-    using Lo = Layout<kINT8, D>;
+    using Lo = Layout<KVT, D>;
     const int r = lane >> 2, c = lane & 3;
     float x[PPI][4];
     float ksc[PPI][4], vsc[PPI][4];
@@ -575,7 +609,7 @@ struct Int8Warp {
       vsc[pg][0] = v4.x; vsc[pg][1] = v4.y; vsc[pg][2] = v4.z; vsc[pg][3] = v4.w;
       // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
       // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3 of head r.
-      // The accumulators of the hi rows start at -1152 sum(q): the code bias cancels
+      // The accumulators of the hi rows start at -kBias sum(q): the code bias cancels
       // inside the FP32 accumulation.
       // Each query fragment is read once per page and serves both n-tiles.
       float sacc[2][4];
@@ -586,19 +620,42 @@ struct Int8Warp {
       }
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk) {
-        uint4 kw[2];
+        // this lane's 16 codes of head-dim columns 64 blk + 16 c .. + 15 for the tokens of
+        // n-tiles 0 and 1: 16 bytes (INT8, FP8) or 8 bytes (INT4) each
+        uint32_t kw[2][4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-          kw[j] = *reinterpret_cast<const uint4*>(Ks + (4 * (r >> 1) + (r & 1) + 2 * j) * D + blk * 64 + c * 16);
+        for (int j = 0; j < 2; ++j) {
+          const int tok = 4 * (r >> 1) + (r & 1) + 2 * j;
+          if constexpr (KVT == kINT4) {
+            const uint2 v2 = *reinterpret_cast<const uint2*>(Ks + tok * (D / 2) + blk * 32 + c * 8);
+            kw[j][0] = v2.x; kw[j][1] = v2.y; kw[j][2] = kw[j][3] = 0u;
+          } else {
+            const uint4 v4 = *reinterpret_cast<const uint4*>(Ks + tok * D + blk * 64 + c * 16);
+            kw[j][0] = v4.x; kw[j][1] = v4.y; kw[j][2] = v4.z; kw[j][3] = v4.w;
+          }
+        }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           const uint4 f = qs[(4 * blk + s) * 32 + lane];
           const uint32_t a[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const uint32_t wsj = s == 0 ? kw[j].x : s == 1 ? kw[j].y : s == 2 ? kw[j].z : kw[j].w;
             uint32_t b0, b1;
-            s8x4_to_f16x4_biased(wsj, b0, b1);
+            if constexpr (KVT == kINT4) {
+              // columns 4s .. 4s+3: nibbles 2 (s % 2) and 2 (s % 2) + 1 of word s / 2
+              const uint32_t w = kw[j][s >> 1];
+              if (s & 1) {
+                b0 = s4x2_to_f16x2_biased<2>(w);
+                b1 = s4x2_to_f16x2_biased<3>(w);
+              } else {
+                b0 = s4x2_to_f16x2_biased<0>(w);
+                b1 = s4x2_to_f16x2_biased<1>(w);
+              }
+            } else if constexpr (KVT == kFP8) {
+              e4m3x4_to_f16x4(kw[j][s], b0, b1);
+            } else {
+              s8x4_to_f16x4_biased(kw[j][s], b0, b1);
+            }
             mma_f16(sacc[j], a, b0, b1);
           }
         }
@@ -612,6 +669,11 @@ struct Int8Warp {
     bool partial = lo > 0;
 #pragma unroll
     for (int pg = 0; pg < PPI; ++pg) partial |= valid[pg] < kPage;
+    // (FP8 only: tokens not attended may hold NaN codes, which the zeroed probability
+    // would not cancel in the MMA; their V operands are masked to zero below)
+    uint32_t vmask[PPI][2];
+#pragma unroll
+    for (int pg = 0; pg < PPI; ++pg) vmask[pg][0] = vmask[pg][1] = 0xffffffffu;
     if (partial) {  // padding may hold NaN scales: mask by select
 #pragma unroll
       for (int pg = 0; pg < PPI; ++pg)
@@ -620,6 +682,9 @@ struct Int8Warp {
           const bool ok = (4 * c + i) < valid[pg] && (pg > 0 || (4 * c + i) >= lo);
           x[pg][i] = ok ? x[pg][i] : -CUDART_INF_F;
           vsc[pg][i] = ok ? vsc[pg][i] : 0.f;
+          if constexpr (KVT == kFP8) {
+            if (!ok) vmask[pg][i >> 1] &= (i & 1) ? 0x0000ffffu : 0xffff0000u;
+          }
         }
     }
     float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
@@ -659,17 +724,37 @@ struct Int8Warp {
       // k-slot order {2c, 2c+1 | 2c+8, 2c+9} -> tokens {4c, 4c+1 | 4c+2, 4c+3} makes a
       // ready-made fragment; the hi and lo parts accumulate into the same C.
       uint32_t bh[2], bl[2];
-      split_h2(pv[pg][0], pv[pg][1], bh[0], bl[0]);
-      split_h2(pv[pg][2], pv[pg][3], bh[1], bl[1]);
+      // (scaled by 2^-kMulLog2, exactly, so that the products carry kBias + code)
+      constexpr float vm = kMulLog2 == 0 ? 1.f : 16.f;
+      static_assert(kMulLog2 == 0 || kMulLog2 == -4, "probability factor");
+      split_h2(pv[pg][0] * vm, pv[pg][1] * vm, bh[0], bl[0]);
+      split_h2(pv[pg][2] * vm, pv[pg][3] * vm, bh[1], bl[1]);
       // A = V^T rows 16 j + r and 16 j + r + 8, tokens 4c .. 4c+3 (same k-slot order)
       const uint8_t* Vs = st + pg * Lo::pageBytes + Lo::kBytes;
 #pragma unroll
       for (int j = 0; j < MT; ++j) {
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r) * kPage + 4 * c);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r + 8) * kPage + 4 * c);
         uint32_t a[4];
-        s8x4_to_f16x4_biased(w0, a[0], a[2]);
-        s8x4_to_f16x4_biased(w1, a[1], a[3]);
+        if constexpr (KVT == kINT4) {
+          // one word: row pair 8 j + r, tokens 4c .. 4c+3 stored in the order 0, 2, 1, 3;
+          // low nibbles row 16 j + r, high nibbles row 16 j + r + 8
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + (8 * j + r) * kPage + 4 * c);
+          a[0] = s4x2_to_f16x2_biased<0>(w);
+          a[1] = s4x2_to_f16x2_biased<1>(w);
+          a[2] = s4x2_to_f16x2_biased<2>(w);
+          a[3] = s4x2_to_f16x2_biased<3>(w);
+        } else {
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r) * kPage + 4 * c);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r + 8) * kPage + 4 * c);
+          if constexpr (KVT == kFP8) {
+            e4m3x4_to_f16x4(w0, a[0], a[2]);
+            e4m3x4_to_f16x4(w1, a[1], a[3]);
+            a[0] &= vmask[pg][0]; a[1] &= vmask[pg][0];
+            a[2] &= vmask[pg][1]; a[3] &= vmask[pg][1];
+          } else {
+            s8x4_to_f16x4_biased(w0, a[0], a[2]);
+            s8x4_to_f16x4_biased(w1, a[1], a[3]);
+          }
+        }
         mma_f16(o[j], a, bh[0], bh[1]);
         mma_f16(o[j], a, bl[0], bl[1]);
       }
@@ -687,9 +772,9 @@ struct Int8Warp {
       cm[r] = m;
       cl[r] = lt;
     }
-    // V entered the MMA as 1152 + code: remove 1152 * sum(P) of heads 2c and 2c + 1
-    const float ba = 1152.f * __shfl_sync(0xffffffffu, st, 8 * c);
-    const float bb = 1152.f * __shfl_sync(0xffffffffu, st, 8 * c + 4);
+    // V entered the MMA as kBias + code: remove kBias * sum(P) of heads 2c and 2c + 1
+    const float ba = kBias * __shfl_sync(0xffffffffu, st, 8 * c);
+    const float bb = kBias * __shfl_sync(0xffffffffu, st, 8 * c + 4);
     float* oa = cO + (2 * c) * (D + 2);
     float* ob = oa + (D + 2);
 #pragma unroll
@@ -714,7 +799,15 @@ struct WarpOf<kBF16, D> {
 };
 template <int D>
 struct WarpOf<kINT8, D> {
-  using type = Int8Warp<D>;
+  using type = QuantWarp<kINT8, D>;
+};
+template <int D>
+struct WarpOf<kFP8, D> {
+  using type = QuantWarp<kFP8, D>;
+};
+template <int D>
+struct WarpOf<kINT4, D> {
+  using type = QuantWarp<kINT4, D>;
 };
 
 // ------------------------------------------------------------------ the kernel
@@ -841,7 +934,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
 
   // ---- copy issue: lane l < NK PPI issues one copy (kind l % NK of page l / NK of the
   // iteration), so a whole stage costs one warp instruction; lane 0 posts the byte count.
-  constexpr int NK = KVT == kINT8 ? 4 : 2;  // K, V (and the two scale vectors)
+  constexpr int NK = quantised(KVT) ? 4 : 2;  // K, V (and the two scale vectors)
   const int cq = lane / NK, ck = lane % NK;
   // this lane's copy: size, and destination inside stage 0 (the source is selected per
   // issue from the kernel parameters, which costs no registers across the loop)
@@ -880,7 +973,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   int t_new = 0;
   uint8_t* const nrow = smem + Sm::step0 + Sm::stepQ + Sm::stepRope;
   if constexpr (STEP) {
-    constexpr int esz = ElemSize<KVT>::value;
+    constexpr int RB = RowBytes<KVT, D>::value;
     float* sqw = reinterpret_cast<float*>(smem + Sm::step0);
     float* rc = reinterpret_cast<float*>(smem + Sm::step0 + Sm::stepQ);
     float* rs = rc + D / 2;
@@ -949,22 +1042,57 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const float(&x)[E] = which ? vx : kx;
-        uint8_t* nr = nrow + which * (D * esz + 16);
+        uint8_t* nr = nrow + which * (RB + 16);
         uint8_t* cache = which ? p.vw : p.kw;
-        if constexpr (KVT == kINT8) {
+        if constexpr (KVT == kINT4) {
+          // K: the row's words; V: one byte per row pair (the block's V rows 8j + r hold
+          // head-dim rows 16j + r and 16j + r + 8) at the token's position
           int8_t code[E];
-          const float sc = quantize_row_int8<E>(x, code);
+          const float sc = quantize_row_int4<E>(x, code);
+          uint8_t* cb = cache + blk * kPage * (D / 2);
+          if (which == 0) {
+            const uint32_t wd = int4_k_word<E>(code, lane);
+            if ((lane & (8 / E - 1)) == 0) {
+              reinterpret_cast<uint32_t*>(nr)[lane * E / 8] = wd;
+              if (hg == 0) reinterpret_cast<uint32_t*>(cb + off * (D / 2))[lane * E / 8] = wd;
+            }
+          } else {
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const int d = lane * E + e;
-            nr[d] = static_cast<uint8_t>(code[e]);
-            if (hg == 0) {
-              if (which == 0) cache[(blk * kPage + off) * D + d] = static_cast<uint8_t>(code[e]);
-              else cache[blk * D * kPage + static_cast<size_t>(d) * kPage + off] = static_cast<uint8_t>(code[e]);
+            for (int e = 0; e < E; ++e) {
+              const int d = lane * E + e;
+              const uint8_t by = int4_v_byte<E>(code, e);
+              if ((d & 15) < 8) {
+                nr[int4_v_pair(d)] = by;
+                if (hg == 0) cb[int4_v_pair(d) * kPage + int4_v_tpos(off)] = by;
+              }
             }
           }
           if (lane == 0) {
-            *reinterpret_cast<float*>(nr + D) = sc;
+            *reinterpret_cast<float*>(nr + RB) = sc;
+            if (hg == 0) (which ? p.vsw : p.ksw)[blk * kPage + off] = sc;
+          }
+        } else if constexpr (KVT == kINT8 || KVT == kFP8) {
+          uint8_t code[E];
+          float sc;
+          if constexpr (KVT == kINT8) {
+            int8_t c8[E];
+            sc = quantize_row_int8<E>(x, c8);
+#pragma unroll
+            for (int e = 0; e < E; ++e) code[e] = static_cast<uint8_t>(c8[e]);
+          } else {
+            sc = quantize_row_fp8<E>(x, code);
+          }
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            nr[d] = code[e];
+            if (hg == 0) {
+              if (which == 0) cache[(blk * kPage + off) * D + d] = code[e];
+              else cache[blk * D * kPage + static_cast<size_t>(d) * kPage + off] = code[e];
+            }
+          }
+          if (lane == 0) {
+            *reinterpret_cast<float*>(nr + RB) = sc;
             if (hg == 0) (which ? p.vsw : p.ksw)[blk * kPage + off] = sc;
           }
         } else if constexpr (KVT == kBF16) {
@@ -997,7 +1125,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   }
 
   st.init(p, b, h0, nh, lane, aux, w, sq);
-  if constexpr (KVT == kINT8) __syncthreads();  // warp 0 built the shared query fragments
+  if constexpr (quantised(KVT)) __syncthreads();  // warp 0 built the shared query fragments
   st.finish(aux, lane);
   __syncwarp();
 
@@ -1015,30 +1143,36 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     if constexpr (STEP) {
       // the fused step: the new token replaces whatever the cache held at its slot
       if (patch && j0 <= np - 1 && np - 1 < j0 + PPI) {
-        constexpr int esz = ElemSize<KVT>::value;
+        constexpr int RB = RowBytes<KVT, D>::value;
         uint8_t* pg = my_stages + stage * Lo::stageBytes + (np - 1 - j0) * Lo::pageBytes;
         const uint8_t* nk = nrow;
-        const uint8_t* nv = nrow + D * esz + 16;
-        for (int d = lane; d < D; d += 32) {
-          if constexpr (KVT == kINT8) {
-            pg[t_new * D + d] = nk[d];
-            pg[Lo::kBytes + d * kPage + t_new] = nv[d];
-          } else if constexpr (KVT == kBF16) {
-            *reinterpret_cast<__nv_bfloat16*>(pg + bf16_k_off(t_new, d, D)) =
-                reinterpret_cast<const __nv_bfloat16*>(nk)[d];
-            *reinterpret_cast<__nv_bfloat16*>(pg + Lo::kBytes + bf16_v_off(d, t_new)) =
-                reinterpret_cast<const __nv_bfloat16*>(nv)[d];
-          } else {
-            reinterpret_cast<float*>(pg)[t_new * D + d] = reinterpret_cast<const float*>(nk)[d];
-            reinterpret_cast<float*>(pg + Lo::kBytes)[d * kPage + t_new] =
-                reinterpret_cast<const float*>(nv)[d];
+        const uint8_t* nv = nrow + RB + 16;
+        if constexpr (KVT == kINT4) {
+          if (lane < D / 8)
+            reinterpret_cast<uint32_t*>(pg + t_new * (D / 2))[lane] = reinterpret_cast<const uint32_t*>(nk)[lane];
+          for (int q = lane; q < D / 2; q += 32) pg[Lo::kBytes + q * kPage + int4_v_tpos(t_new)] = nv[q];
+        } else {
+          for (int d = lane; d < D; d += 32) {
+            if constexpr (KVT == kINT8 || KVT == kFP8) {
+              pg[t_new * D + d] = nk[d];
+              pg[Lo::kBytes + d * kPage + t_new] = nv[d];
+            } else if constexpr (KVT == kBF16) {
+              *reinterpret_cast<__nv_bfloat16*>(pg + bf16_k_off(t_new, d, D)) =
+                  reinterpret_cast<const __nv_bfloat16*>(nk)[d];
+              *reinterpret_cast<__nv_bfloat16*>(pg + Lo::kBytes + bf16_v_off(d, t_new)) =
+                  reinterpret_cast<const __nv_bfloat16*>(nv)[d];
+            } else {
+              reinterpret_cast<float*>(pg)[t_new * D + d] = reinterpret_cast<const float*>(nk)[d];
+              reinterpret_cast<float*>(pg + Lo::kBytes)[d * kPage + t_new] =
+                  reinterpret_cast<const float*>(nv)[d];
+            }
           }
         }
-        if constexpr (KVT == kINT8) {
+        if constexpr (quantised(KVT)) {
           if (lane == 0) {
-            reinterpret_cast<float*>(pg + 2 * Lo::kBytes)[t_new] = *reinterpret_cast<const float*>(nk + D);
+            reinterpret_cast<float*>(pg + 2 * Lo::kBytes)[t_new] = *reinterpret_cast<const float*>(nk + RB);
             reinterpret_cast<float*>(pg + 2 * Lo::kBytes + Lo::sBytes)[t_new] =
-                *reinterpret_cast<const float*>(nv + D);
+                *reinterpret_cast<const float*>(nv + RB);
           }
         }
         fence_proxy_async_smem();  // ordered before the stage's next bulk copy
@@ -1295,22 +1429,26 @@ constexpr int max_splits_of() {
 #define PKV_VARIANT(T, D, ST, WN, I)                                                        \
   {kernel_ptr<T, D, ST, WN>(), Smem<T, D, ST>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>(), \
    Tune<T, D>::W}
-// index: dtype-and-head-dim slot (0 .. 5), + 6 for the fused decode step, + 12 for the
+// index: dtype-and-head-dim slot (0 .. 9), + 10 for the fused decode step, + 20 for the
 // sliding window
-constexpr int kVariants = 24;
+constexpr int kVariants = 40;
 Variant variant(int dtype, int D, bool step, bool win) {
   switch (dtype * 1000 + D + (step ? 100000 : 0) + (win ? 1000000 : 0)) {
-#define PKV_VARIANTS_OF(ST, WN, BASE, KEY)                                                 \
+#define PKV_VARIANTS_OF(ST, WN, BASE, KEY)                                                \
     case KEY + kF32 * 1000 + 64: return PKV_VARIANT(kF32, 64, ST, WN, BASE + 0);          \
     case KEY + kF32 * 1000 + 128: return PKV_VARIANT(kF32, 128, ST, WN, BASE + 1);        \
     case KEY + kBF16 * 1000 + 64: return PKV_VARIANT(kBF16, 64, ST, WN, BASE + 2);        \
     case KEY + kBF16 * 1000 + 128: return PKV_VARIANT(kBF16, 128, ST, WN, BASE + 3);      \
     case KEY + kINT8 * 1000 + 64: return PKV_VARIANT(kINT8, 64, ST, WN, BASE + 4);        \
-    case KEY + kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, ST, WN, BASE + 5);
+    case KEY + kINT8 * 1000 + 128: return PKV_VARIANT(kINT8, 128, ST, WN, BASE + 5);      \
+    case KEY + kFP8 * 1000 + 64: return PKV_VARIANT(kFP8, 64, ST, WN, BASE + 6);          \
+    case KEY + kFP8 * 1000 + 128: return PKV_VARIANT(kFP8, 128, ST, WN, BASE + 7);        \
+    case KEY + kINT4 * 1000 + 64: return PKV_VARIANT(kINT4, 64, ST, WN, BASE + 8);        \
+    case KEY + kINT4 * 1000 + 128: return PKV_VARIANT(kINT4, 128, ST, WN, BASE + 9);
     PKV_VARIANTS_OF(false, false, 0, 0)
-    PKV_VARIANTS_OF(true, false, 6, 100000)
-    PKV_VARIANTS_OF(false, true, 12, 1000000)
-    PKV_VARIANTS_OF(true, true, 18, 1100000)
+    PKV_VARIANTS_OF(true, false, 10, 100000)
+    PKV_VARIANTS_OF(false, true, 20, 1000000)
+    PKV_VARIANTS_OF(true, true, 30, 1100000)
 #undef PKV_VARIANTS_OF
     default: return {nullptr, 0, -1, 1, 1, 4};
   }

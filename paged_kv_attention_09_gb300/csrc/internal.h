@@ -8,7 +8,12 @@ namespace pkv {
 
 constexpr int kPage = 16;  // tokens per page (the only supported page size)
 
-enum : int { kF32 = 0, kBF16 = 1, kINT8 = 2 };
+enum : int { kF32 = 0, kBF16 = 1, kINT8 = 2, kFP8 = 3, kINT4 = 4 };
+
+// Formats stored as codes with one FP32 scale per (token, kv head).
+__host__ __device__ constexpr bool quantised(int dtype) {
+  return dtype == kINT8 || dtype == kFP8 || dtype == kINT4;
+}
 
 // BF16 page blocks are stored as tensor-core tiles: 8 x 8 "core matrices" of 16-byte
 // rows, each matrix 128 contiguous bytes, so one bulk copy of a block lands a valid

@@ -52,14 +52,14 @@ extern "C" pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void
                                               const int32_t* context_lens, float scale,
                                               float* out, int32_t* dev_status, void* stream) {
   if (!cache || !cache->k_cache || !cache->v_cache) return PKV_ERR_NULL;
-  if (cache->kv_dtype < PKV_F32 || cache->kv_dtype > PKV_INT8) return PKV_ERR_DTYPE;
+  if (cache->kv_dtype < PKV_F32 || cache->kv_dtype > PKV_INT4) return PKV_ERR_DTYPE;
   if (cache->page_size != 16) return PKV_ERR_PAGE_SIZE;
-  if (cache->num_pages < 1 || cache->num_kv_heads < 1) return PKV_ERR_SHAPE;
+  if (cache->num_pages < 1 || cache->num_kv_heads < 1 || cache->window < 0) return PKV_ERR_SHAPE;
   if (cache->head_dim != 64 && cache->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (cache->kv_dtype == PKV_INT8 && (!cache->k_scale || !cache->v_scale)) return PKV_ERR_NULL;
+  const bool coded = pkv::quantised(cache->kv_dtype);
+  if (coded && (!cache->k_scale || !cache->v_scale)) return PKV_ERR_NULL;
   if (!aligned16(cache->k_cache) || !aligned16(cache->v_cache)) return PKV_ERR_ALIGN;
-  if (cache->kv_dtype == PKV_INT8 && (!aligned16(cache->k_scale) || !aligned16(cache->v_scale)))
-    return PKV_ERR_ALIGN;
+  if (coded && (!aligned16(cache->k_scale) || !aligned16(cache->v_scale))) return PKV_ERR_ALIGN;
   if (num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1) return PKV_ERR_SHAPE;
   if (num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_SHAPE;
   if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
@@ -74,7 +74,7 @@ extern "C" pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_DEVICE;
   const pkv::CacheView view{cache->k_cache,  cache->v_cache,     cache->k_scale,
                             cache->v_scale,  cache->num_pages,   cache->num_kv_heads,
-                            cache->head_dim, cache->kv_dtype};
+                            cache->head_dim, cache->kv_dtype,   cache->window};
   pkv::DecodePlan plan{};
   if (!pkv::plan_decode(view, num_seqs, num_q_heads, max_blocks_per_seq, q_dtype, dev,
                         pkv::decode_chunk_override(), &plan))

@@ -14,8 +14,11 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpkv.so")
 
-F32, BF16, INT8 = 0, 1, 2
-_TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16, INT8: torch.int8}
+F32, BF16, INT8, FP8, INT4 = 0, 1, 2, 3, 4
+CODED = (INT8, FP8, INT4)  # stored as codes with one FP32 scale per (token, kv head)
+# element containers of the cache tensors (FP8 codes and INT4 code pairs as raw bytes)
+_TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16, INT8: torch.int8, FP8: torch.uint8,
+                INT4: torch.uint8}
 _CODE = {torch.float32: F32, torch.bfloat16: BF16, torch.int8: INT8}
 
 DEV_BAD_PAGE, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_BAD_CHUNK, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
@@ -97,28 +100,43 @@ class KVCache:
     """Device tensors of one paged cache in the library's layout.
 
     k: [num_pages, Hkv, 16, D]; v: [num_pages, Hkv, D, 16] (page blocks transposed);
-    k_scale, v_scale: float32 [num_pages, Hkv, 16] for INT8 caches.  For BF16 caches the
-    elements inside each (page, kv head) block are in tensor-core tile order (see
-    include/pkv.h); the tensor shapes are containers of the right size.
+    k_scale, v_scale: float32 [num_pages, Hkv, 16] for INT8, FP8 and INT4 caches.  For
+    BF16 caches the elements inside each (page, kv head) block are in tensor-core tile
+    order, FP8 codes are bytes, and INT4 blocks hold two codes per byte (k: [.., 16, D/2],
+    v: [.., D/2, 16] bytes); see include/pkv.h.  The tensor shapes are containers of the
+    right size.
     """
 
-    def __init__(self, k, v, k_scale=None, v_scale=None, window=0):
+    def __init__(self, k, v, k_scale=None, v_scale=None, window=0, kv_dtype=None):
         self.k, self.v, self.k_scale, self.v_scale = k, v, k_scale, v_scale
+        self.kv_dtype = _CODE[k.dtype] if kv_dtype is None else int(kv_dtype)
         self.num_pages, self.num_kv_heads, self.page_size, self.head_dim = k.shape
-        self.kv_dtype = _CODE[k.dtype]
+        if self.kv_dtype == INT4:
+            self.head_dim *= 2
         self.window = int(window)  # sliding window in tokens (0: none), read by every call
 
     @classmethod
     def allocate(cls, num_pages, num_kv_heads, head_dim, kv_dtype, device="cuda",
                  page_size=16):
         dt = _TORCH_DTYPE[kv_dtype]
-        k = torch.zeros(num_pages, num_kv_heads, page_size, head_dim, dtype=dt, device=device)
-        v = torch.zeros(num_pages, num_kv_heads, head_dim, page_size, dtype=dt, device=device)
+        if kv_dtype == INT4:
+            k = torch.zeros(num_pages, num_kv_heads, page_size, head_dim // 2, dtype=dt, device=device)
+            v = torch.zeros(num_pages, num_kv_heads, head_dim // 2, page_size, dtype=dt, device=device)
+        else:
+            k = torch.zeros(num_pages, num_kv_heads, page_size, head_dim, dtype=dt, device=device)
+            v = torch.zeros(num_pages, num_kv_heads, head_dim, page_size, dtype=dt, device=device)
         ks = vs = None
-        if kv_dtype == INT8:
+        if kv_dtype in CODED:
             ks = torch.zeros(num_pages, num_kv_heads, page_size, dtype=torch.float32, device=device)
             vs = torch.zeros_like(ks)
-        return cls(k, v, ks, vs)
+        return cls(k, v, ks, vs, kv_dtype=kv_dtype)
+
+    def clone(self) -> "KVCache":
+        """A copy in fresh device memory (same format and window)."""
+        return KVCache(self.k.clone(), self.v.clone(),
+                       None if self.k_scale is None else self.k_scale.clone(),
+                       None if self.v_scale is None else self.v_scale.clone(),
+                       window=self.window, kv_dtype=self.kv_dtype)
 
     def struct(self) -> pkv_cache:
         return pkv_cache(self.k.data_ptr(), self.v.data_ptr(),

@@ -51,9 +51,12 @@ def upload(wl: Workload, device="cuda", cache_fill: Optional[float] = None,
     """Allocate the cache and batch tensors; optionally append the history rows."""
     cache = pkv.KVCache.allocate(wl.num_pages, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, device)
     if cache_fill is not None:  # sentinel for never-written slots (NaN poisons padding)
-        if wl.kv_dtype == pkv.INT8:
+        if wl.kv_dtype in pkv.CODED:
             cache.k_scale.fill_(cache_fill)
             cache.v_scale.fill_(cache_fill)
+            if wl.kv_dtype == pkv.FP8 and cache_fill != cache_fill:  # NaN: the E4M3 NaN code
+                cache.k.fill_(0x7F)
+                cache.v.fill_(0x7F)
         else:
             cache.k.fill_(cache_fill)
             cache.v.fill_(cache_fill)

@@ -179,8 +179,10 @@ def _uniform_lens(seed: int, n: int, lo: int, hi: int):
     return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
 
 
-# The five named workloads.  Index i uses seed 1000 + i (lengths use 2000 + i).
-WORKLOADS = ("tiny", "smollm2-f32", "qwen-bf16", "tinyllama-int8", "mixed")
+# The named workloads.  Index i uses seed 1000 + i (lengths use 2000 + i).  The last two
+# are the batch-256 TinyLlama-shaped decode with the cache in FP8 and in INT4.
+WORKLOADS = ("tiny", "smollm2-f32", "qwen-bf16", "tinyllama-int8", "mixed", "tinyllama-fp8",
+             "tinyllama-int4")
 
 
 def workload(name: str) -> Workload:
@@ -204,6 +206,12 @@ def workload(name: str) -> Workload:
         return make_workload(name, seed=1003, num_q_heads=32, num_kv_heads=4, head_dim=64,
                              num_pages=16384, kv_dtype=INT8, q_dtype=F32, new_dtype=F32,
                              decode_lens=[1024] * 256, max_decode_len=1024)
+    if name in ("tinyllama-fp8", "tinyllama-int4"):
+        fp8 = name == "tinyllama-fp8"
+        return make_workload(name, seed=1005 if fp8 else 1006, num_q_heads=32, num_kv_heads=4,
+                             head_dim=64, num_pages=16384, kv_dtype=FP8 if fp8 else INT4,
+                             q_dtype=F32, new_dtype=F32, decode_lens=[1024] * 256,
+                             max_decode_len=1024)
     if name == "mixed":
         return make_workload(name, seed=1004, num_q_heads=12, num_kv_heads=2, head_dim=128,
                              num_pages=16384, kv_dtype=BF16, q_dtype=BF16, new_dtype=BF16,

@@ -6,7 +6,7 @@ import oracle
 from paged_kv_attention_09_gb300 import pkv, runner
 from paged_kv_attention_09_gb300 import workloads as W
 
-TOL = {W.F32: 1e-4, W.BF16: 2e-3, W.INT8: 2e-3}
+TOL = {W.F32: 1e-4, W.BF16: 2e-3, W.INT8: 2e-3, W.FP8: 2e-3, W.INT4: 2e-3}
 
 
 def oracle_outputs(wl, oc=None, seqs=None):

@@ -4,7 +4,7 @@ Element-by-element parity on small workloads spanning several pages, ragged tail
 every dtype combination and head layout; sampled parity at the full workload sizes in
 the benchmark's launch configuration; NaN-poisoned padding; page-permutation
 bit-identity; split-count invariance and determinism; device-side error reporting.
-Tolerances (max abs error): 1e-4 for FP32 KV, 2e-3 for BF16 / INT8 KV.
+Tolerances (max abs error): 1e-4 for FP32 KV, 2e-3 for BF16 / INT8 / FP8 / INT4 KV.
 """
 import numpy as np
 import pytest
@@ -32,6 +32,12 @@ SMALL = [
     (W.INT8, W.F32, 32, 4, 64),
     (W.INT8, W.BF16, 6, 2, 128),
     (W.INT8, W.F32, 4, 4, 64),
+    (W.FP8, W.F32, 32, 4, 64),
+    (W.FP8, W.BF16, 6, 2, 128),
+    (W.FP8, W.F32, 12, 1, 64),     # two head groups
+    (W.INT4, W.F32, 32, 4, 64),
+    (W.INT4, W.BF16, 6, 2, 128),
+    (W.INT4, W.F32, 12, 1, 128),   # two head groups
 ]
 
 
@@ -45,9 +51,10 @@ def test_decode_small_parity(kv, qd, Hq, Hkv, D):
     assert max_err(got[0], ref) <= TOL[kv]
 
 
-@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8])
+@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8, W.FP8, W.INT4])
 def test_decode_poisoned_padding_is_never_read(kv):
-    """Unwritten slots hold NaN (NaN scales for INT8); table entries past the context
+    """Unwritten slots hold NaN (NaN scales for the coded formats, and NaN codes for FP8);
+    table entries past the context
     hold -1.  Any read of either would show up as NaN or a bad-page status."""
     wl = W.small_workload(77 + kv, num_q_heads=8, num_kv_heads=2, head_dim=64, kv_dtype=kv,
                           q_dtype=W.F32, decode_lens=[1, 17, 30, 47], max_decode_len=80)
@@ -67,7 +74,7 @@ def test_decode_zero_length_gives_zero_rows():
     assert max_err(got[0], oracle_outputs(wl)[0]) <= 2e-3
 
 
-@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8])
+@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8, W.FP8, W.INT4])
 def test_page_permutation_bit_identical(kv):
     wl = W.small_workload(91 + kv, num_q_heads=8, num_kv_heads=2, head_dim=64, kv_dtype=kv,
                           q_dtype=W.F32, decode_lens=[70, 33, 129])
@@ -81,7 +88,7 @@ def test_page_permutation_bit_identical(kv):
     assert np.array_equal(got1[0], got2[0])
 
 
-@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8])
+@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8, W.FP8, W.INT4])
 def test_split_count_invariance_and_determinism(kv):
     wl = W.small_workload(95 + kv, num_q_heads=12, num_kv_heads=2, head_dim=128 if kv else 64,
                           kv_dtype=kv, q_dtype=W.BF16 if kv == W.BF16 else W.F32,
@@ -132,7 +139,8 @@ def test_workspace_is_left_zero_for_the_next_call():
 # Full-size workloads in the benchmark's launch configuration (automatic split); the
 # oracle computes a sample of sequences one by one.
 FULL = [("tiny", None), ("smollm2-f32", [0, 1, 17, 40, 63]), ("qwen-bf16", [0, 5, 11, 31]),
-        ("tinyllama-int8", [0, 1, 100, 255]), ("mixed", [0, 3])]
+        ("tinyllama-int8", [0, 1, 100, 255]), ("mixed", [0, 3]),
+        ("tinyllama-fp8", [0, 7, 128, 255]), ("tinyllama-int4", [0, 9, 200, 255])]
 
 
 @pytest.mark.parametrize("name,seqs", FULL)
@@ -150,7 +158,7 @@ def test_full_size_sampled_parity(name, seqs):
     assert np.all(np.isfinite(got[i]))
 
 
-@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8])
+@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8, W.FP8, W.INT4])
 @pytest.mark.parametrize("chunk", [0, 1000])
 def test_long_context_many_iterations_per_warp(kv, chunk):
     """A single block streaming ~300 pages gives each warp more than two batches of 32

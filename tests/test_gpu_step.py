@@ -52,6 +52,10 @@ CASES = [
     (W.INT8, W.BF16, W.F32, 6, 1, 128, [48, 17]),
     (W.INT8, W.F32, W.BF16, 32, 2, 64, [9, 81]),  # two head groups of 8
     (W.BF16, W.BF16, W.BF16, 32, 2, 128, [77, 3]),  # two head groups of 8
+    (W.FP8, W.F32, W.F32, 32, 4, 64, [20, 1, 33, 300]),
+    (W.FP8, W.BF16, W.BF16, 6, 1, 128, [48, 17]),
+    (W.INT4, W.F32, W.F32, 32, 4, 64, [20, 1, 33, 300]),
+    (W.INT4, W.BF16, W.F32, 12, 2, 128, [48, 17, 5]),
 ]
 
 
@@ -65,7 +69,7 @@ def test_step_matches_oracle(case, rope):
     assert cache_bytes_equal(dw, oc)  # the new rows stored exactly as the oracle stores them
 
 
-@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8])
+@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8, W.FP8, W.INT4])
 def test_step_with_splits(kv):
     """Long contexts split over several blocks: the block of the last split patches the
     new token; the automatic split and a forced small chunk."""
@@ -78,7 +82,7 @@ def test_step_with_splits(kv):
         assert cache_bytes_equal(dw, oc)
 
 
-@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8])
+@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8, W.FP8, W.INT4])
 def test_step_bad_slot_and_no_new_token(kv):
     """Sequence 0's slot is not its last position's slot: NaN rows, status bit, nothing
     stored for it; sequence 1 has no new token (slot -1) and attends over the cache as is;

@@ -47,7 +47,8 @@ def decode_gpu(wl, window, bt=None, chunk=0, poison_rows=None):
 
 @pytest.mark.parametrize("kv,qd,Hq,Hkv,D", [(W.F32, W.F32, 9, 3, 64), (W.F32, W.BF16, 8, 2, 128),
                                             (W.BF16, W.BF16, 12, 2, 128), (W.BF16, W.F32, 8, 8, 64),
-                                            (W.INT8, W.F32, 32, 4, 64), (W.INT8, W.BF16, 6, 1, 128)])
+                                            (W.INT8, W.F32, 32, 4, 64), (W.INT8, W.BF16, 6, 1, 128),
+                                            (W.FP8, W.F32, 8, 2, 64), (W.INT4, W.F32, 8, 2, 128)])
 @pytest.mark.parametrize("window", [1, 5, 16, 17, 100, 1000])
 def test_window_decode_matches_oracle(kv, qd, Hq, Hkv, D, window):
     wl = W.small_workload(8000 + kv * 10 + D + qd, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
@@ -61,7 +62,7 @@ def test_window_decode_matches_oracle(kv, qd, Hq, Hkv, D, window):
         assert max_err(got, ref) <= TOL[kv], (chunk, max_err(got, ref))
 
 
-@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8])
+@pytest.mark.parametrize("kv", [W.F32, W.BF16, W.INT8, W.FP8, W.INT4])
 def test_window_released_pages_and_stale_nan_rows(kv):
     """Pages wholly before the window hold -1 in the table; the rows before the window in
     its first page are NaN: neither is read into the result."""
