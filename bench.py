@@ -53,6 +53,9 @@ def parse():
                     help="the decode batch as one pkv_decode_step launch")
     ap.add_argument("--rope", action="store_true",
                     help="with --fused: the step also applies the rotary embedding")
+    ap.add_argument("--graphs", action="store_true",
+                    help="end-to-end leg: the step's launches through the bucketed "
+                         "CUDA-graph executor (decode-only workloads)")
     return ap.parse_args()
 
 
@@ -377,6 +380,18 @@ def run_ours(args, rank, world):
         host_out = [b.out.cpu().pin_memory() for b in base.batches]
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
+        graphs = None
+        if args.graphs:
+            if n_batches != 1 or wl.batches[0].kind != "decode":
+                raise SystemExit("--graphs: decode-only workloads")
+            gk, gv, gs, gp = dec_in if fused else (step_k, step_v, step_s, None)
+            graphs = []
+            for dw in reps:
+                b = dw.batches[0]
+                graphs.append(pkv.DecodeGraph(
+                    [pkv.GraphLayer(dw.cache, b.q, b.out, gk, gv)], b.block_tables,
+                    b.context_lens, wl.scale, [b.q.shape[0]], slot_mapping=gs, fused=fused,
+                    positions=gp, rope_theta=ROPE_THETA, dev_status=dw.dev_status))
 
         def e2e_step(i):
             dw = reps[i % R]
@@ -387,10 +402,13 @@ def run_ours(args, rank, world):
                     dev_in.append(b.q_start_loc)
             for d, h in zip(dev_in, host_in):
                 d.copy_(h, non_blocking=True)  # on `stream` (the current stream here)
-            if n_append:
-                pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
-            for j in range(n_batches):
-                run_j(dw, j)
+            if graphs is not None:
+                graphs[i % R].launch(dw.batches[0].q.shape[0], stream)
+            else:
+                if n_append:
+                    pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
+                for j in range(n_batches):
+                    run_j(dw, j)
             for b, h in zip(dw.batches, host_out):
                 h.copy_(b.out, non_blocking=True)
 
@@ -411,7 +429,11 @@ def run_ours(args, rank, world):
             e2e_ms = float(t.item())
         e2e = {"value": round(acc["total"] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_ms, 5)}
+               "ms_per_step": round(e2e_ms, 5),
+               "launches": "one CUDA graph per step" if graphs is not None else "direct"}
+        if graphs is not None:
+            for g in graphs:
+                g.close()
     status = int(base.dev_status.item())
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed steps")

@@ -258,6 +258,87 @@ pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void* q, int32_
                                    int32_t* dev_status, void* stream);
 
 /*
+ * Bucketed CUDA-graph executor for small-batch decode steps ("mini-llm-inference-engine"
+ * README, architecture overview, core design principles: CUDA Graph multi-bucket
+ * capture; no mechanism is given).  At small batch the kernels of a decode step take a
+ * few microseconds each and their launches dominate; this object captures the whole step
+ * once per batch-size bucket and replays it with one graph launch.
+ *
+ * A step runs, for every layer l in order, either
+ *     pkv_append(layer l's new rows) then pkv_decode_attn        (fused == 0), or
+ *     pkv_decode_step                                            (fused != 0),
+ * over the first B sequences of the caller's buffers, B the bucket.  Every pointer is
+ * caller-owned device memory captured by address: the caller rewrites the buffers'
+ * contents between launches, never their addresses.  Rows num_seqs .. B - 1 of a launch
+ * are padding the caller keeps inert: context_lens 0 and slot_mapping -1 (their outputs
+ * are zero rows, nothing is stored).  Layers share block_tables, context_lens,
+ * slot_mapping, positions, the workspace and dev_status (all layers of a model index the
+ * same pages); each layer has its own cache, queries, new rows and output.
+ *   layers[l].q      [B_max][num_q_heads][head_dim] (q_dtype)
+ *   layers[l].k_new, v_new  [B_max][num_kv_heads][head_dim] (new_dtype); NULL: no append
+ *                    (fused == 0 only)
+ *   layers[l].out    [B_max][num_q_heads][head_dim] float32
+ *   buckets          ascending batch sizes >= 1 (at most PKV_GRAPH_MAX_BUCKETS); B_max is
+ *                    the last one
+ *   workspace        at least pkv_decode_graph_workspace_size bytes, zero-filled before
+ *                    the first launch (the kernels leave it zero)
+ * Creation captures and instantiates one graph per bucket on an internal stream of the
+ * current device (host objects only; no device memory is allocated by the library).
+ * Launches of one executor are ordered on their stream; executors sharing buffers must
+ * not run concurrently.  Errors of the captured calls are returned by create.
+ */
+#define PKV_GRAPH_MAX_BUCKETS 16
+
+typedef struct pkv_graph_layer {
+  pkv_cache cache;
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  float* out;
+} pkv_graph_layer;
+
+typedef struct pkv_decode_graph_desc {
+  int32_t num_layers;
+  const pkv_graph_layer* layers; /* host array of num_layers */
+  int32_t num_q_heads;
+  int32_t q_dtype;
+  int32_t new_dtype;
+  int32_t fused;                 /* 0: append + decode; else the fused decode step */
+  const int32_t* block_tables;   /* [B_max][max_blocks_per_seq] */
+  int32_t max_blocks_per_seq;
+  const int32_t* context_lens;   /* [B_max] */
+  const int32_t* slot_mapping;   /* [B_max]; NULL only when no layer appends */
+  const int32_t* positions;      /* fused only: [B_max] or NULL (no rotation) */
+  double rope_theta;
+  float scale;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;           /* may be NULL */
+  int32_t num_buckets;
+  const int32_t* buckets;        /* host array of num_buckets */
+} pkv_decode_graph_desc;
+
+typedef struct pkv_decode_graph pkv_decode_graph;
+
+/* Scratch bytes the executor needs (the largest decode workspace over buckets and
+ * layers); host call. */
+pkv_status pkv_decode_graph_workspace_size(const pkv_decode_graph_desc* desc, size_t* bytes);
+
+/* Validates desc, captures and instantiates one graph per bucket; *out receives the
+ * executor (NULL on error). */
+pkv_status pkv_decode_graph_create(const pkv_decode_graph_desc* desc, pkv_decode_graph** out);
+
+/* One step for num_seqs sequences (0 <= num_seqs <= B_max; 0 is a no-op): replays the
+ * smallest bucket >= num_seqs on `stream` (a stream of the executor's device). */
+pkv_status pkv_decode_graph_launch(pkv_decode_graph* graph, int32_t num_seqs, void* stream);
+
+/* The bucket a launch of num_seqs sequences replays (0 if none). */
+int32_t pkv_decode_graph_bucket(const pkv_decode_graph* graph, int32_t num_seqs);
+
+/* Releases the executor's graphs (after its launches have completed); NULL is a no-op. */
+void pkv_decode_graph_destroy(pkv_decode_graph* graph);
+
+/*
  * Tuning override: pages per thread block for the decode split (0 = automatic, the
  * default).  Process-wide; affects pkv_decode_workspace_size.  Meant for tests and
  * sweeps, not for changing results (splits only reorder floating-point sums).

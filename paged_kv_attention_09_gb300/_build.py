@@ -14,7 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
-SOURCES = ("api.cu", "append.cu", "decode.cu", "prefill.cu", "prefill_tc.cu", "noalloc.cu")
+SOURCES = ("api.cu", "append.cu", "decode.cu", "prefill.cu", "prefill_tc.cu", "noalloc.cu",
+           "graph.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", INCLUDE, "-I", CSRC]

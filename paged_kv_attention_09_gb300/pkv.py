@@ -27,7 +27,10 @@ STATUS = {0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_DTYPE"
           7: "PKV_ERR_UNSUPPORTED", 8: "PKV_ERR_LAUNCH", 9: "PKV_ERR_DEVICE"}
 EXPORTS = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn", "pkv_decode_step",
            "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn",
-           "pkv_decode_attn_noalloc", "pkv_set_decode_chunk_pages", "pkv_status_string")
+           "pkv_decode_attn_noalloc", "pkv_set_decode_chunk_pages", "pkv_status_string",
+           "pkv_decode_graph_workspace_size", "pkv_decode_graph_create",
+           "pkv_decode_graph_launch", "pkv_decode_graph_bucket", "pkv_decode_graph_destroy")
+GRAPH_MAX_BUCKETS = 16
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -43,6 +46,23 @@ class pkv_cache(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("window", ctypes.c_int32)]
+
+
+class pkv_graph_layer(ctypes.Structure):
+    _fields_ = [("cache", pkv_cache), ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p),
+                ("v_new", ctypes.c_void_p), ("out", ctypes.c_void_p)]
+
+
+class pkv_decode_graph_desc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("layers", ctypes.POINTER(pkv_graph_layer)),
+                ("num_q_heads", ctypes.c_int32), ("q_dtype", ctypes.c_int32),
+                ("new_dtype", ctypes.c_int32), ("fused", ctypes.c_int32),
+                ("block_tables", ctypes.c_void_p), ("max_blocks_per_seq", ctypes.c_int32),
+                ("context_lens", ctypes.c_void_p), ("slot_mapping", ctypes.c_void_p),
+                ("positions", ctypes.c_void_p), ("rope_theta", ctypes.c_double),
+                ("scale", ctypes.c_float), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("dev_status", ctypes.c_void_p),
+                ("num_buckets", ctypes.c_int32), ("buckets", ctypes.POINTER(ctypes.c_int32))]
 
 
 _lib = None
@@ -75,6 +95,16 @@ def load(path: str = LIB_PATH):
     lib.pkv_set_decode_chunk_pages.restype = None
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
+    GD = ctypes.POINTER(pkv_decode_graph_desc)
+    lib.pkv_decode_graph_workspace_size.argtypes = [GD, ctypes.POINTER(SZ)]
+    lib.pkv_decode_graph_create.argtypes = [GD, ctypes.POINTER(ctypes.c_void_p)]
+    lib.pkv_decode_graph_launch.argtypes = [P, I32, P]
+    lib.pkv_decode_graph_bucket.argtypes = [P, I32]
+    lib.pkv_decode_graph_destroy.argtypes = [P]
+    lib.pkv_decode_graph_destroy.restype = None
+    for fn in ("pkv_decode_graph_workspace_size", "pkv_decode_graph_create",
+               "pkv_decode_graph_launch", "pkv_decode_graph_bucket"):
+        getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -201,6 +231,85 @@ def pkv_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new:
                                   int(block_tables.shape[1]), _ptr(context_lens), float(scale),
                                   _ptr(out), _ptr(workspace), wb, _ptr(dev_status),
                                   _stream(stream)), "pkv_decode_step")
+
+
+class GraphLayer:
+    """One layer of a decode-graph step: its cache, query rows, new K/V rows (or None: no
+    append) and output, all sized for the largest bucket."""
+
+    def __init__(self, cache: KVCache, q: torch.Tensor, out: torch.Tensor,
+                 k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None):
+        self.cache, self.q, self.out, self.k_new, self.v_new = cache, q, out, k_new, v_new
+
+
+class DecodeGraph:
+    """pkv_decode_graph: one captured CUDA graph per batch-size bucket (see include/pkv.h).
+
+    The tensors are captured by address and must stay alive (and in place) for the
+    executor's lifetime; rows past a launch's num_seqs up to its bucket must be inert
+    (context_lens 0, slot_mapping -1).  The workspace is allocated here, zero-filled."""
+
+    def __init__(self, layers, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                 scale: float, buckets, slot_mapping: Optional[torch.Tensor] = None,
+                 fused: bool = False, positions: Optional[torch.Tensor] = None,
+                 rope_theta: float = 10000.0, dev_status: Optional[torch.Tensor] = None):
+        lib = load()
+        self.layers = list(layers)
+        self._keep = (block_tables, context_lens, slot_mapping, positions, dev_status)
+        arr = (pkv_graph_layer * len(self.layers))()
+        for i, L in enumerate(self.layers):
+            arr[i] = pkv_graph_layer(L.cache.struct(), _ptr(L.q), _ptr(L.k_new), _ptr(L.v_new),
+                                     _ptr(L.out))
+        self._arr = arr
+        self._buckets = (ctypes.c_int32 * len(buckets))(*[int(b) for b in buckets])
+        q0 = self.layers[0].q
+        k0 = next((L.k_new for L in self.layers if L.k_new is not None), None)
+        d = pkv_decode_graph_desc()
+        d.num_layers = len(self.layers)
+        d.layers = ctypes.cast(arr, ctypes.POINTER(pkv_graph_layer))
+        d.num_q_heads = int(q0.shape[1])
+        d.q_dtype = _CODE[q0.dtype]
+        d.new_dtype = _CODE[k0.dtype] if k0 is not None else F32
+        d.fused = 1 if fused else 0
+        d.block_tables = _ptr(block_tables)
+        d.max_blocks_per_seq = int(block_tables.shape[1])
+        d.context_lens = _ptr(context_lens)
+        d.slot_mapping = _ptr(slot_mapping)
+        d.positions = _ptr(positions)
+        d.rope_theta = float(rope_theta)
+        d.scale = float(scale)
+        d.dev_status = _ptr(dev_status)
+        d.num_buckets = len(buckets)
+        d.buckets = ctypes.cast(self._buckets, ctypes.POINTER(ctypes.c_int32))
+        n = ctypes.c_size_t(0)
+        _check(lib.pkv_decode_graph_workspace_size(ctypes.byref(d), ctypes.byref(n)),
+               "pkv_decode_graph_workspace_size")
+        self.workspace = workspace_for(int(n.value), q0.device)
+        d.workspace = _ptr(self.workspace)
+        d.workspace_bytes = int(n.value)
+        self._desc = d
+        h = ctypes.c_void_p(None)
+        _check(lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)),
+               "pkv_decode_graph_create")
+        self._h = h
+
+    def bucket(self, num_seqs: int) -> int:
+        return int(load().pkv_decode_graph_bucket(self._h, int(num_seqs)))
+
+    def launch(self, num_seqs: int, stream=None) -> None:
+        _check(load().pkv_decode_graph_launch(self._h, int(num_seqs), _stream(stream)),
+               "pkv_decode_graph_launch")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().pkv_decode_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def pkv_decode_attn_noalloc(cache: KVCache, q: torch.Tensor, block_tables: torch.Tensor,

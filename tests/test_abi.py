@@ -102,3 +102,40 @@ def test_no_device_is_reported_not_crashed(lib):
     c = _cache()
     n = ctypes.c_size_t(0)
     assert lib.pkv_decode_workspace_size(ctypes.byref(c), 2, 4, 4, ctypes.byref(n)) == 9
+
+
+def test_graph_descriptor_validation(lib):
+    """The decode-graph executor rejects bad descriptors on the host."""
+    n = ctypes.c_size_t(0)
+    h = ctypes.c_void_p(None)
+    assert lib.pkv_decode_graph_workspace_size(None, ctypes.byref(n)) == 1
+    assert lib.pkv_decode_graph_create(None, ctypes.byref(h)) == 1 and not h.value
+    layer = (pkv.pkv_graph_layer * 1)(pkv.pkv_graph_layer(_cache(), 0x80000, 0x90000,
+                                                           0x90000, 0xB0000))
+
+    def desc(**kw):
+        d = pkv.pkv_decode_graph_desc()
+        d.num_layers, d.layers = 1, ctypes.cast(layer, ctypes.POINTER(pkv.pkv_graph_layer))
+        d.num_q_heads, d.q_dtype, d.new_dtype = 4, pkv.F32, pkv.F32
+        d.block_tables, d.max_blocks_per_seq, d.context_lens = 0xA0000, 4, 0xA1000
+        d.slot_mapping = 0xA2000
+        b = (ctypes.c_int32 * 3)(1, 2, 4)
+        d.num_buckets, d.buckets = 3, ctypes.cast(b, ctypes.POINTER(ctypes.c_int32))
+        d._b = b
+        for k, v in kw.items():
+            setattr(d, k, v)
+        return d
+    for bad, code in [(dict(num_layers=0), 2), (dict(num_buckets=0), 2),
+                      (dict(num_buckets=17), 2), (dict(slot_mapping=None), 1)]:
+        d = desc(**bad)
+        assert lib.pkv_decode_graph_workspace_size(ctypes.byref(d), ctypes.byref(n)) == code, bad
+        assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == code, bad
+    d = desc()
+    unordered = (ctypes.c_int32 * 3)(1, 4, 2)
+    d.buckets = ctypes.cast(unordered, ctypes.POINTER(ctypes.c_int32))
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == 2
+    layer[0].cache.kv_dtype = 9  # a layer's cache is validated like any call's
+    assert lib.pkv_decode_graph_create(ctypes.byref(desc()), ctypes.byref(h)) == 3
+    assert lib.pkv_decode_graph_launch(None, 1, None) == 1
+    assert lib.pkv_decode_graph_bucket(None, 3) == 0
+    lib.pkv_decode_graph_destroy(None)  # a no-op
