@@ -53,6 +53,9 @@ def parse():
                     help="the decode batch as one pkv_decode_step launch")
     ap.add_argument("--rope", action="store_true",
                     help="with --fused: the step also applies the rotary embedding")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="a step runs the hot path over this many layers (one cache each, "
+                         "shared tables and lengths), as a model's decode step does")
     ap.add_argument("--graphs", action="store_true",
                     help="end-to-end leg: the step's launches through the bucketed "
                          "CUDA-graph executor (decode-only workloads)")
@@ -267,8 +270,9 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     pkv.load()
     wl = W.workload(args.workload)
-    acc = step_accounting(wl)
-    ws_bytes = acc["total"]
+    acc = step_accounting(wl)  # per layer
+    NL = max(1, args.layers)
+    ws_bytes = acc["total"] * NL
     R = args.replicas or max(2, math.ceil(4 * L2_BYTES / max(ws_bytes, 1)))
     base = runner.upload(wl, f"cuda:{dev}")
     fused = args.fused and wl.batches[0].kind == "decode"
@@ -292,14 +296,19 @@ def run_ours(args, rank, world):
                    for b in base.batches]
         reps.append(runner.DeviceWorkload(wl, cache, base.k_src, base.v_src, base.slots,
                                           base.step_rows, batches, base.dev_status))
+    # every replica's layers: the replica itself, then copies of its cache that share its
+    # tables, lengths, queries and outputs
+    layered = [[dw] + [runner.DeviceWorkload(wl, dw.cache.clone(), dw.k_src, dw.v_src, dw.slots,
+                                             dw.step_rows, dw.batches, dw.dev_status)
+                       for _ in range(NL - 1)] for dw in reps]
     stream = torch.cuda.Stream(device=f"cuda:{dev}")
     stream.wait_stream(torch.cuda.current_stream())
     n_batches = len(wl.batches)
 
     def append_only(i):
-        dw = reps[i % R]
         if n_append:
-            pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
+            for dw in layered[i % R]:
+                pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
 
     def run_j(dw, j):
         if fused and j == 0:
@@ -308,12 +317,17 @@ def run_ours(args, rank, world):
             runner.run_batch(dw, j, stream)
 
     def batch_only(j):
-        return lambda i: run_j(reps[i % R], j)
+        def run(i):
+            for dw in layered[i % R]:
+                run_j(dw, j)
+        return run
 
     def step(i):
-        append_only(i)
-        for j in range(n_batches):
-            run_j(reps[i % R], j)
+        for dw in layered[i % R]:
+            if n_append:
+                pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
+            for j in range(n_batches):
+                run_j(dw, j)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -358,7 +372,7 @@ def run_ours(args, rank, world):
         total_ms = replay_ms(g_step)
     if world > 1:
         dist.barrier()
-    kern_ms = [[replay_ms(g) / K] for g in g_kern]
+    kern_ms = [[replay_ms(g) / (K * NL)] for g in g_kern]
     if world > 1:
         t = torch.tensor([total_ms], device=f"cuda:{dev}")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -386,12 +400,12 @@ def run_ours(args, rank, world):
                 raise SystemExit("--graphs: decode-only workloads")
             gk, gv, gs, gp = dec_in if fused else (step_k, step_v, step_s, None)
             graphs = []
-            for dw in reps:
-                b = dw.batches[0]
+            for dws in layered:
+                b = dws[0].batches[0]
                 graphs.append(pkv.DecodeGraph(
-                    [pkv.GraphLayer(dw.cache, b.q, b.out, gk, gv)], b.block_tables,
+                    [pkv.GraphLayer(dw.cache, b.q, b.out, gk, gv) for dw in dws], b.block_tables,
                     b.context_lens, wl.scale, [b.q.shape[0]], slot_mapping=gs, fused=fused,
-                    positions=gp, rope_theta=ROPE_THETA, dev_status=dw.dev_status))
+                    positions=gp, rope_theta=ROPE_THETA, dev_status=dws[0].dev_status))
 
         def e2e_step(i):
             dw = reps[i % R]
@@ -405,10 +419,11 @@ def run_ours(args, rank, world):
             if graphs is not None:
                 graphs[i % R].launch(dw.batches[0].q.shape[0], stream)
             else:
-                if n_append:
-                    pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
-                for j in range(n_batches):
-                    run_j(dw, j)
+                for dwl in layered[i % R]:
+                    if n_append:
+                        pkv.pkv_append(dwl.cache, step_k, step_v, step_s, dwl.dev_status, stream)
+                    for j in range(n_batches):
+                        run_j(dwl, j)
             for b, h in zip(dw.batches, host_out):
                 h.copy_(b.out, non_blocking=True)
 
@@ -427,7 +442,7 @@ def run_ours(args, rank, world):
             t = torch.tensor([e2e_ms], device=f"cuda:{dev}")
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        e2e = {"value": round(acc["total"] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(acc["total"] * NL * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 5),
                "launches": "one CUDA graph per step" if graphs is not None else "direct"}
@@ -457,7 +472,8 @@ def main():
     avg = {n: statistics.fmean(v) for n, v in zip(names, kern_ms)}
     from paged_kv_attention_09_gb300 import workloads as W
     peak, peak_kind = measured_hbm()
-    value = acc["total"] * world / (ms * 1e-3) / 1e9
+    NL = max(1, args.layers)
+    value = acc["total"] * NL * world / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -475,16 +491,17 @@ def main():
                      ("; prefill chunk rows appended, then prefill attention"
                       if len(wl.batches) > 1 else "") if fused else
                      "append new K/V rows, then attention over every batch"),
+            "layers": NL,
             "timing": "CUDA events around one CUDA-graph replay of the K steps",
-            "bytes_per_step": acc["total"], "replicas": R,
-            "l2": f"rotating {R} replicas of every input ({R} x {acc['total'] / 1e6:.1f} MB "
+            "bytes_per_step": acc["total"] * NL, "replicas": R,
+            "l2": f"rotating {R} replicas of every input ({R} x {acc['total'] * NL / 1e6:.1f} MB "
                   f"per cycle > {L2_BYTES / 2**20:.0f} MiB L2)",
             "parallelism": "replicas" if world > 1 else "single",
         },
-        "seq_tokens_per_s": round(acc["kv_tokens"] * world / (ms * 1e-3), 1),
+        "seq_tokens_per_s": round(acc["kv_tokens"] * NL * world / (ms * 1e-3), 1),
         "decode_steps_per_s": round(acc["seqs"] * world / (ms * 1e-3), 1),
         "kernel_ms": {n: round(v, 5) for n, v in avg.items()},
-        "gpu_launches": K * ((1 if n_append else 0) + len(wl.batches)),
+        "gpu_launches": K * NL * ((1 if n_append else 0) + len(wl.batches)),
     }
     dec = avg.get("decode")
     if dec:
