@@ -98,7 +98,9 @@ def _c(a, dtype):
 
 
 _REAL = {F32: np.float32, BF16: np.uint16}
-_CACHE = {F32: np.float32, BF16: np.uint16, INT8: np.int8, FP8: np.uint8, INT4: np.uint8}
+# element containers: INT8 bytes hold code + 128 (offset binary), FP8 bytes E4M3 codes,
+# INT4 bytes two codes each
+_CACHE = {F32: np.float32, BF16: np.uint16, INT8: np.uint8, FP8: np.uint8, INT4: np.uint8}
 
 
 class HostCache:

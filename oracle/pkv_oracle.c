@@ -29,7 +29,8 @@
  *   BF16 (tensor-core tiles of 8x8 "core matrices", each 64 contiguous elements):
  *                 K element (t, d) at ((t/8)*(D/8) + d/8)*64 + (t%8)*8 + d%8
  *                 V element (d, t) at ((d/8)*2  + t/8)*64 + (d%8)*8 + t%8
- *   scales   [num_pages][Hkv][16]  float32     (INT8 only; one per token and kv head)
+ *   scales   [num_pages][Hkv][16]  float32     (coded formats; one per token and kv head)
+ *   INT8 codes are stored in offset binary: the byte holds code + 128.
  *   slot = page * 16 + offset
  *
  * The INT8 quantiser and the BF16 rounding run in C `float` exactly as specified
@@ -267,7 +268,12 @@ static double cache_value(const void* cache, const float* scales, int kv_dtype, 
   size_t i = is_v ? v_index(kv_dtype, page, h, off, d, Hkv, P, D)
                   : k_index(kv_dtype, page, h, off, d, Hkv, P, D);
   if (kv_dtype == ODT_INT8) {
-    int8_t c = ((const int8_t*)cache)[i];
+    /* stored in offset binary: the byte holds code + 128 */
+#if ORACLE_MUTANT == 16 /* the byte read as a two's-complement code */
+    int c = ((const int8_t*)cache)[i];
+#else
+    int c = (int)((const uint8_t*)cache)[i] - 128;
+#endif
     return (double)c * (double)scales[s_index(page, h, off, Hkv, P)];
   }
   if (kv_dtype == ODT_FP8) {
@@ -312,7 +318,9 @@ int oracle_append(int kv_dtype, int num_pages, int P, int Hkv, int D, void* k_ca
           for (int d = 0; d < D; ++d) {
             size_t j = is_v ? v_index(kv_dtype, page, h, off, d, Hkv, P, D)
                             : k_index(kv_dtype, page, h, off, d, Hkv, P, D);
-            ((int8_t*)dst)[j] = codes[d];
+            /* INT8 codes in offset binary (code + 128); E4M3 codes as they are */
+            ((uint8_t*)dst)[j] = kv_dtype == ODT_INT8 ? (uint8_t)(codes[d] + 128)
+                                                     : (uint8_t)codes[d];
           }
           (is_v ? v_scale : k_scale)[s_index(page, h, off, Hkv, P)] = s;
         } else if (kv_dtype == ODT_INT4) {

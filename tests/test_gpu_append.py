@@ -23,7 +23,7 @@ COMBOS = [(kv, new, D) for kv, new in [(W.F32, W.F32), (W.F32, W.BF16), (W.BF16,
 def _sentinel_caches(wl, value):
     oc = oracle.HostCache(wl.kv_dtype, wl.num_pages, 16, wl.num_kv_heads, wl.head_dim)
     gc = pkv.KVCache.allocate(wl.num_pages, wl.num_kv_heads, wl.head_dim, wl.kv_dtype)
-    if wl.kv_dtype in (W.FP8, W.INT4):  # raw bytes: a fixed sentinel pattern
+    if wl.kv_dtype in (W.INT8, W.FP8, W.INT4):  # raw bytes: a fixed sentinel pattern
         oc.k[...] = 0xA5
         oc.v[...] = 0xA5
         oc.k_scale[...] = 0.5

@@ -90,6 +90,8 @@ def stored_codes(cache: HostCache):
         return e4m3_decode_torch(cache.k), e4m3_decode_torch(cache.v)
     if cache.kv_dtype == INT4:
         return int4_codes(cache.k), int4_v_codes(cache.v)
+    if cache.kv_dtype == INT8:  # offset binary: the byte holds code + 128
+        return cache.k.astype(np.int64) - 128, cache.v.astype(np.int64) - 128
     return cache.k, cache.v
 
 
@@ -352,10 +354,13 @@ def test_append_bf16_and_int8_stored_values():
     for i in range(wl.slots.shape[0]):
         pg, off = divmod(int(wl.slots[i]), P)
         for h in range(2):
+            # INT8 bytes hold code + 128 (offset binary)
             codes, s = oracle.quantize_row_int8(wl.k_src[i, h])
-            assert np.array_equal(ci.k[pg, h, off], codes) and ci.k_scale[pg, h, off] == s
+            assert np.array_equal(ci.k[pg, h, off].astype(np.int64) - 128, codes)
+            assert ci.k_scale[pg, h, off] == s
             codes, s = oracle.quantize_row_int8(wl.v_src[i, h])
-            assert np.array_equal(ci.v[pg, h, :, off], codes) and ci.v_scale[pg, h, off] == s
+            assert np.array_equal(ci.v[pg, h, :, off].astype(np.int64) - 128, codes)
+            assert ci.v_scale[pg, h, off] == s
             ref = torch.from_numpy(wl.k_src[i, h]).to(torch.bfloat16).view(torch.int16)
             idx = k_elem(BF16, off, np.arange(64), 64)
             assert np.array_equal(cb.k.reshape(wl.num_pages, 2, -1)[pg, h, idx],
@@ -810,7 +815,7 @@ PINS = [check_bf16_rounding, check_quantiser, check_decode_bruteforce,
         check_quantisers_fp8_int4]
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16])
 def test_planted_mistake_is_caught(mutant, monkeypatch):
     path = oracle.build(defines=[f"ORACLE_MUTANT={mutant}"], name=f"liboracle_m{mutant}.so")
     monkeypatch.setattr(oracle, "_lib", oracle.load(path))
