@@ -58,8 +58,8 @@
  *   Token t of a sequence lives in page block_tables[b][t / page_size] at offset
  *   t % page_size; its slot number is page * page_size + offset.
  *   Element types: PKV_F32 float32, PKV_BF16 bfloat16, and three coded formats whose
- *   value is code * scale with one scale per (token, kv head): PKV_INT8 int8 codes,
- *   scale = max|x| / 127; PKV_FP8 E4M3 codes (OCP "fn": bias 7, no infinity, largest
+ *   value is code * scale with one scale per (token, kv head): PKV_INT8 codes in
+ *   [-127, 127] stored in offset binary (the byte holds code + 128), scale = max|x| / 127; PKV_FP8 E4M3 codes (OCP "fn": bias 7, no infinity, largest
  *   finite 448), scale = max|x| / 448; PKV_INT4 4-bit two's-complement codes in
  *   [-7, 7], scale = max|x| / 7 ("tinyloop Current Status", KV cache modes table: INT8
  *   and INT4 KV caches; the TinyInfer review, item 2: INT8 or FP8 KV cache).

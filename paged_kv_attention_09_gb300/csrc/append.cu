@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         int8_t c8[E];
         s = quantize_row_int8<E>(x, c8);
 #pragma unroll
-        for (int e = 0; e < E; ++e) code[e] = static_cast<uint8_t>(c8[e]);
+        for (int e = 0; e < E; ++e) code[e] = int8_stored(c8[e]);
       } else {
         s = quantize_row_fp8<E>(x, code);
       }

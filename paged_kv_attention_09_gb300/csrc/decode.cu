@@ -24,8 +24,8 @@
 //             form the A rows: the BF16 high part in rows 0-7, the rounding remainder in
 //             rows 8-15, so FP32 queries keep ~16 bits; the probabilities use the same
 //             hi/lo split for P.V.
-//   INT8 KV — f16 MMA for both products.  Codes become the exact f16 values 1152 + code
-//             with one xor and two byte permutes (no subtraction); the bias is removed
+//   INT8 KV — f16 MMA for both products.  Codes (stored as code + 128) become the exact
+//             f16 values 1152 + code with two byte permutes per 4 codes; the bias is removed
 //             afterwards: 1152 * sum(q) from each score, 1152 * sum(P) from the output.
 //             FP8 (E4M3) and INT4 KV take the same path: E4M3 codes convert to their exact
 //             f16 values (no bias), INT4 codes to 1032 + code with one mask-and-xor per
@@ -177,12 +177,11 @@ __device__ __forceinline__ void split_b2(float a, float b, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// Four int8 codes (a 32-bit word) -> two f16x2 words holding 1152 + code exactly:
-// byte b (biased by ^0x80) becomes the low byte of the f16 0x64XX = 1024 + (b ^ 0x80).
-__device__ __forceinline__ void s8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t biased = w ^ 0x80808080u;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(biased), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(biased), "r"(0x64646464u));
+// Four stored INT8 bytes (code + 128, a 32-bit word) -> two f16x2 words holding
+// 1152 + code exactly: each byte becomes the low byte of the f16 0x64XX = 1024 + byte.
+__device__ __forceinline__ void u8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(w), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(w), "r"(0x64646464u));
 }
 
 // Four E4M3 codes (a 32-bit word) -> two f16x2 words holding their exact values (every
@@ -504,7 +503,7 @@ struct Bf16Warp {
 // ------------------------------------------------------------------ INT8 / FP8 / INT4 (f16 MMA)
 
 // One path for the three coded formats: the codes become exact f16 MMA operands.
-//   INT8  1152 + code (xor + two byte permutes per 4 codes); bias removed afterwards
+//   INT8  1152 + code (two byte permutes per 4 stored codes); bias removed afterwards
 //   INT4  (24 + code) / 16 (one shift and one mask-and-xor per 2 codes); the factor 16
 //         goes into the score scale and the probabilities, the bias is removed afterwards
 //   FP8   the E4M3 value itself (hardware conversion, 2 codes per instruction), no bias
@@ -654,7 +653,7 @@ struct QuantWarp {
             } else if constexpr (KVT == kFP8) {
               e4m3x4_to_f16x4(kw[j][s], b0, b1);
             } else {
-              s8x4_to_f16x4_biased(kw[j][s], b0, b1);
+              u8x4_to_f16x4_biased(kw[j][s], b0, b1);
             }
             mma_f16(sacc[j], a, b0, b1);
           }
@@ -751,8 +750,8 @@ struct QuantWarp {
             a[0] &= vmask[pg][0]; a[1] &= vmask[pg][0];
             a[2] &= vmask[pg][1]; a[3] &= vmask[pg][1];
           } else {
-            s8x4_to_f16x4_biased(w0, a[0], a[2]);
-            s8x4_to_f16x4_biased(w1, a[1], a[3]);
+            u8x4_to_f16x4_biased(w0, a[0], a[2]);
+            u8x4_to_f16x4_biased(w1, a[1], a[3]);
           }
         }
         mma_f16(o[j], a, bh[0], bh[1]);
@@ -1078,7 +1077,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
             int8_t c8[E];
             sc = quantize_row_int8<E>(x, c8);
 #pragma unroll
-            for (int e = 0; e < E; ++e) code[e] = static_cast<uint8_t>(c8[e]);
+            for (int e = 0; e < E; ++e) code[e] = int8_stored(c8[e]);
           } else {
             sc = quantize_row_fp8<E>(x, code);
           }

@@ -26,6 +26,12 @@ __device__ __forceinline__ float row_scale(const float (&x)[E], float range) {
   return __fdiv_rn(amax, range);
 }
 
+// The stored byte of an INT8 code: offset binary, code + 128 (so that the decode kernel
+// widens a code to the f16 value 1024 + byte with a byte permute alone).
+__device__ __forceinline__ uint8_t int8_stored(int8_t code) {
+  return static_cast<uint8_t>(static_cast<uint8_t>(code) ^ 0x80u);
+}
+
 // Returns the row's scale and writes its codes; every lane of the warp must call it.
 template <int E>
 __device__ __forceinline__ float quantize_row_int8(const float (&x)[E], int8_t (&code)[E]) {

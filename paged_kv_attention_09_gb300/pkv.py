@@ -17,9 +17,10 @@ LIB_PATH = os.path.join(_PKG, "libpkv.so")
 F32, BF16, INT8, FP8, INT4 = 0, 1, 2, 3, 4
 CODED = (INT8, FP8, INT4)  # stored as codes with one FP32 scale per (token, kv head)
 # element containers of the cache tensors (FP8 codes and INT4 code pairs as raw bytes)
-_TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16, INT8: torch.int8, FP8: torch.uint8,
+# (INT8 bytes hold code + 128, offset binary)
+_TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16, INT8: torch.uint8, FP8: torch.uint8,
                 INT4: torch.uint8}
-_CODE = {torch.float32: F32, torch.bfloat16: BF16, torch.int8: INT8}
+_CODE = {torch.float32: F32, torch.bfloat16: BF16}
 
 DEV_BAD_PAGE, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_BAD_CHUNK, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_DTYPE",
