@@ -507,6 +507,8 @@ struct Bf16Warp {
 //   INT4  (24 + code) / 16 (one shift and one mask-and-xor per 2 codes); the factor 16
 //         goes into the score scale and the probabilities, the bias is removed afterwards
 //   FP8   the E4M3 value itself (hardware conversion, 2 codes per instruction), no bias
+constexpr float kRescaleLog2 = 8.f;  // lazy rescale margin of the coded formats' softmax
+
 template <int KVT, int D>
 struct QuantWarp {
   static constexpr int KS = D / 16;  // k-steps of the q.k product
@@ -520,7 +522,9 @@ struct QuantWarp {
   // O^T accumulators: lane (r, c) holds head-dim rows 16 mt + r and 16 mt + r + 8 of
   // heads 2c and 2c + 1 (the C layout of the transposed product)
   float o[MT][4];
-  float m, l, sp, row_scale, kbias;  // per query head r = lane / 4
+  // per query head r = lane / 4: nm = -(running max in log2 units); scores stay in raw
+  // units and the head's log2 scale row_scale applies inside the exponent
+  float nm, l, sp, row_scale, kbias;
 
   // k-slot pair {2c, 2c+1} of k-step ks <-> head_dim 64(ks/4) + 16c + 4(ks%4): each lane's
   // K operand is then one contiguous 16-byte shared-memory load per n-tile.
@@ -578,7 +582,7 @@ struct QuantWarp {
         rowc[kMaxHeads + r] = ldexpf(kBias, kMulLog2) * qsum;  // K entered as 2^m (kBias + code)
       }
     }
-    m = -CUDART_INF_F;
+    nm = CUDART_INF_F;
     l = 0.f;
     sp = 0.f;
 #pragma unroll
@@ -663,7 +667,7 @@ struct QuantWarp {
       for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e)
-          x[pg][2 * j + e] = (sacc[j][e] + sacc[j][2 + e]) * (row_scale * ksc[pg][2 * j + e]);
+          x[pg][2 * j + e] = (sacc[j][e] + sacc[j][2 + e]) * ksc[pg][2 * j + e];
     }
     bool partial = lo > 0;
 #pragma unroll
@@ -692,23 +696,16 @@ struct QuantWarp {
       mx = fmaxf(mx, fmaxf(fmaxf(x[pg][0], x[pg][1]), fmaxf(x[pg][2], x[pg][3])));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float mn = fmaxf(m, mx);
-    const float corr = fast_exp2(m - mn);
-    m = mn;
-    float pv[PPI][4];
-    float ls = 0.f, ps = 0.f;
-#pragma unroll
-    for (int pg = 0; pg < PPI; ++pg)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float pr = fast_exp2(x[pg][i] - mn);
-        pv[pg][i] = pr * vsc[pg][i];
-        ls += pr;
-        ps += pv[pg][i];
-      }
-    l = l * corr + ls;
-    sp = sp * corr + ps;
-    if (__any_sync(0xffffffffu, corr != 1.f)) {
+    // The running max is raised only when a score exceeds it by more than 2^8 in the
+    // exponent (probabilities then stay below 256, well inside f16 and FP32), so most
+    // pages skip the rescale entirely.
+    const bool need = fmaf(row_scale, mx, nm) > kRescaleLog2;
+    if (__any_sync(0xffffffffu, need)) {
+      const float nn = need ? -row_scale * mx : nm;
+      const float corr = fast_exp2(nn - nm);  // 0 on the first page (nm = +inf)
+      nm = nn;
+      l *= corr;
+      sp *= corr;
       // this lane's accumulators belong to heads 2c and 2c + 1
       const float ca = __shfl_sync(0xffffffffu, corr, 8 * c);
       const float cb = __shfl_sync(0xffffffffu, corr, 8 * c + 4);
@@ -717,6 +714,19 @@ struct QuantWarp {
         o[j][0] *= ca; o[j][1] *= cb; o[j][2] *= ca; o[j][3] *= cb;
       }
     }
+    float pv[PPI][4];
+    float ls = 0.f, ps = 0.f;
+#pragma unroll
+    for (int pg = 0; pg < PPI; ++pg)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float pr = fast_exp2(fmaf(row_scale, x[pg][i], nm));
+        pv[pg][i] = pr * vsc[pg][i];
+        ls += pr;
+        ps += pv[pg][i];
+      }
+    l += ls;
+    sp += ps;
 #pragma unroll
     for (int pg = 0; pg < PPI; ++pg) {
       // B = P^T (tokens x heads): lane (r, c) holds head r, tokens 4c .. 4c+3, which the
@@ -768,7 +778,7 @@ struct QuantWarp {
     st += __shfl_xor_sync(0xffffffffu, st, 1);
     st += __shfl_xor_sync(0xffffffffu, st, 2);
     if (c == 0) {
-      cm[r] = m;
+      cm[r] = -nm;  // the running max in log2 units, as the merge expects
       cl[r] = lt;
     }
     // V entered the MMA as kBias + code: remove kBias * sum(P) of heads 2c and 2c + 1
