@@ -1327,16 +1327,40 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // The merge.  Warp w handles heads w and w + 4: its lanes read the (max, sum) of every
-  // split in one round trip and reduce them by shuffles; the weights go to shared memory.
-  // Then each thread owns 4 consecutive outputs of one or two heads and reads the
-  // partial outputs of 8 or 16 splits at a time as 16-byte loads, all in flight together,
-  // adding them in split order.
+  // The merge.  Each thread owns 4 consecutive outputs of one or two heads; it issues the
+  // 16-byte loads of its first 8 splits' partial outputs first, so that they are in
+  // flight together with the (max, sum) loads: warp w reads the (max, sum) of every split
+  // for heads w and w + 4 in one round trip and reduces them by shuffles into weights in
+  // shared memory.  Further splits follow in batches of 8, added in split order.
   {
     float* wts = reinterpret_cast<float*>(stages);  // [nsplit][8] weights, then [8] 1/L
     float* lsm = wts + (nsplit + 1) * kMaxHeads;    // [nsplit][8] partial sums
     const size_t stride = static_cast<size_t>(p.B) * p.Hq;
     const size_t row0 = static_cast<size_t>(b) * p.Hq + h0;
+    constexpr int D4 = D / 4;
+    constexpr int CPT = (kMaxHeads * D4 + kThreads - 1) / kThreads;  // chunks per thread
+    constexpr int SB = 8;                                             // splits per batch
+    const size_t sstride = stride * D4;  // float4s from one split's partial to the next
+    const float4* src[CPT];
+    int rr[CPT];
+    bool act[CPT];
+    float4 acc[CPT];
+    float4 v[CPT][SB];
+    // (the register-bound coded kernels with head_dim 64 issue them after the weights)
+    constexpr bool kEarly = !(quantised(KVT) && D == 64);
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+      const int cidx = tid + c * kThreads;
+      act[c] = cidx < nh * D4;
+      rr[c] = act[c] ? cidx / D4 : 0;
+      src[c] = reinterpret_cast<const float4*>(p.ws_o + (row0 + rr[c]) * D) + (act[c] ? cidx % D4 : 0);
+      acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (kEarly) {
+#pragma unroll
+        for (int k = 0; k < SB; ++k)
+          v[c][k] = act[c] && k < nsplit ? __ldcg(src[c] + k * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     __syncthreads();
     for (int r = w; r < nh; r += kW) {
       float M = -CUDART_INF_F;
@@ -1364,30 +1388,15 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
       if (lane == 0) wts[nsplit * kMaxHeads + r] = poisoned ? CUDART_NAN_F : (Ls > 0.f ? 1.f / Ls : 0.f);
     }
     __syncthreads();
-    constexpr int D4 = D / 4;
-    constexpr int CPT = (kMaxHeads * D4 + kThreads - 1) / kThreads;  // chunks per thread
-    constexpr int SB = 8;                                             // splits per batch
-    const size_t sstride = stride * D4;  // float4s from one split's partial to the next
-    const float4* src[CPT];
-    int rr[CPT];
-    bool act[CPT];
-    float4 acc[CPT];
-#pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      const int cidx = tid + c * kThreads;
-      act[c] = cidx < nh * D4;
-      rr[c] = act[c] ? cidx / D4 : 0;
-      src[c] = reinterpret_cast<const float4*>(p.ws_o + (row0 + rr[c]) * D) + (act[c] ? cidx % D4 : 0);
-      acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     for (int s0 = 0; s0 < nsplit; s0 += SB) {
-      float4 v[CPT][SB];
+      if (s0 > 0 || !kEarly) {
 #pragma unroll
-      for (int c = 0; c < CPT; ++c)
+        for (int c = 0; c < CPT; ++c)
 #pragma unroll
-        for (int k = 0; k < SB; ++k)
-          v[c][k] = act[c] && s0 + k < nsplit ? __ldcg(src[c] + (s0 + k) * sstride)
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k = 0; k < SB; ++k)
+            v[c][k] = act[c] && s0 + k < nsplit ? __ldcg(src[c] + (s0 + k) * sstride)
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
       for (int c = 0; c < CPT; ++c)
 #pragma unroll
