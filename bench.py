@@ -129,6 +129,24 @@ def step_accounting(wl):
     return acc
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value over the ranks of the default process group (the job's time is
+    its slowest rank's); every rank gets it."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time
+    (each rank runs the same workload: weak scaling)."""
+    return units_per_rank * world / seconds
+
+
 # ----------------------------------------------------------------------------- peaks, clocks
 
 def measured_hbm():
@@ -374,9 +392,7 @@ def run_ours(args, rank, world):
         dist.barrier()
     kern_ms = [[replay_ms(g) / (K * NL)] for g in g_kern]
     if world > 1:
-        t = torch.tensor([total_ms], device=f"cuda:{dev}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, f"cuda:{dev}")
     ms = total_ms / K
     del g_step, g_kern
 
@@ -439,10 +455,9 @@ def run_ours(args, rank, world):
             torch.cuda.synchronize()
         e2e_ms = s2.elapsed_time(e2) / K
         if world > 1:
-            t = torch.tensor([e2e_ms], device=f"cuda:{dev}")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(acc["total"] * NL * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            e2e_ms = max_over_ranks(e2e_ms, f"cuda:{dev}")
+        e2e = {"value": round(job_rate(acc["total"] * NL, world, e2e_ms * 1e-3) / 1e9, 2),
+               "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 5),
                "launches": "one CUDA graph per step" if graphs is not None else "direct"}
@@ -473,7 +488,7 @@ def main():
     from paged_kv_attention_09_gb300 import workloads as W
     peak, peak_kind = measured_hbm()
     NL = max(1, args.layers)
-    value = acc["total"] * NL * world / (ms * 1e-3) / 1e9
+    value = job_rate(acc["total"] * NL, world, ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
