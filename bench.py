@@ -214,17 +214,31 @@ class ClockSampler:
                 "reasons": reasons}
 
 
+def code_digest(kernel_tag):
+    """sha256 of the code a kernel is built from: its .cu file and every header of the
+    package's CUDA sources, with comments and blank space removed (a comment-only edit
+    leaves the kernel, and so its profile, unchanged)."""
+    csrc = os.path.join(ROOT, "paged_kv_attention_09_gb300", "csrc")
+    names = [f"{kernel_tag}.cu"] + sorted(f for f in os.listdir(csrc) if f.endswith((".h", ".cuh")))
+    h = hashlib.sha256()
+    for name in names:
+        text = open(os.path.join(csrc, name)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [" ".join(line.split()) for line in text.splitlines()]
+        h.update(("\n".join(l for l in lines if l) + "\n").encode())
+    return h.hexdigest()
+
+
 def traffic_from_profiles(kernel_tag, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source (its sha256 is recorded in the summary)."""
+    current kernel code (its code digest is recorded in the summary)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
-    src = os.path.join(ROOT, "paged_kv_attention_09_gb300", "csrc", f"{kernel_tag}.cu")
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-        s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-        if m and s and s.group(1) == sha:
+        s = re.search(r"code_sha256:\s*([0-9a-f]{64})", text)
+        if m and s and s.group(1) == code_digest(kernel_tag):
             return float(m.group(1))
     except Exception:
         pass

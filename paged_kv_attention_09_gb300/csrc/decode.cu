@@ -28,9 +28,9 @@
 //             f16 values 1152 + code with two byte permutes per 4 codes; the bias is removed
 //             afterwards: 1152 * sum(q) from each score, 1152 * sum(P) from the output.
 //             FP8 (E4M3) and INT4 KV take the same path: E4M3 codes convert to their exact
-//             f16 values (no bias), INT4 codes to 1032 + code with one mask-and-xor per
-//             pair (the TinyInfer review, item 2; "tinyloop Current Status", KV cache modes
-//             table).
+//             f16 values (no bias), INT4 codes to (24 + code) / 16 with a shift and a
+//             mask-and-xor per pair (the TinyInfer review, item 2; "tinyloop Current
+//             Status", KV cache modes table).
 //             Queries are scaled by a power of two into [0.5, 1) and split hi/lo in f16
 //             (rows 0-7 / 8-15); per-token K scales multiply the scores and V scales the
 //             probabilities (split hi/lo) in FP32.  (The s8 MMA path is far slower on
