@@ -129,6 +129,16 @@ def step_accounting(wl):
     return acc
 
 
+def workload_config(wl, layers=1):
+    """The keys of the JSON line's config that identify the workload (both arms)."""
+    return {"workload": wl.name, "num_q_heads": wl.num_q_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+            "page_size": wl.page_size, "num_pages": wl.num_pages,
+            "batches": [{"kind": b.kind, "num_seqs": b.num_seqs,
+                         "context_tokens": int(b.context_lens.sum())} for b in wl.batches],
+            "layers": layers}
+
+
 # ----------------------------------------------------------------------------- ranks
 
 def max_over_ranks(x: float, device) -> float:
@@ -510,17 +520,13 @@ def main():
         "dtype": W.DTYPE_NAMES[wl.kv_dtype] + "-kv/f32-acc",
         "data": "synthetic (seeded N(0,1) values, shapes of the named model family)",
         "config": {
-            "workload": wl.name, "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
-            "head_dim": wl.head_dim, "page_size": wl.page_size, "num_pages": wl.num_pages,
-            "batches": [{"kind": b.kind, "num_seqs": b.num_seqs,
-                         "context_tokens": int(b.context_lens.sum())} for b in wl.batches],
+            **workload_config(wl, NL),
             "step": ((("decode batch as one fused launch (rotary embedding of the new query and "
                        "key, append of the new row, attention)") if args.rope else
                       "decode batch as one fused launch (append of the new row, attention)") +
                      ("; prefill chunk rows appended, then prefill attention"
                       if len(wl.batches) > 1 else "") if fused else
                      "append new K/V rows, then attention over every batch"),
-            "layers": NL,
             "timing": "CUDA events around one CUDA-graph replay of the K steps",
             "bytes_per_step": acc["total"] * NL, "replicas": R,
             "l2": f"rotating {R} replicas of every input ({R} x {acc['total'] * NL / 1e6:.1f} MB "
@@ -582,8 +588,8 @@ def main_reference(args):
             "scaling": "weak", "vs_baseline": None, "impl": "reference",
             "dtype": "f64",
             "data": "synthetic (seeded N(0,1) values, shapes of the named model family)",
-            "config": {"workload": wl.name, "num_q_heads": wl.num_q_heads,
-                       "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim},
+            "config": {**workload_config(wl, max(1, args.layers)),
+                       "timing": "host wall clock around the oracle's bounded sample"},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -1,0 +1,96 @@
+"""The benchmark's byte and FLOP accounting (the numerators of every roofline figure),
+checked against hand counts, and the reference arm's JSON line."""
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from paged_kv_attention_09_gb300 import workloads as W  # noqa: E402
+
+
+def test_cache_bytes_per_token_of_every_format():
+    # K and V rows of every kv head, plus two FP32 scales per kv head for coded formats
+    assert bench.kv_token_bytes(W.workload("tinyllama-int8")) == 4 * (2 * 64 + 8)
+    assert bench.kv_token_bytes(W.workload("tinyllama-fp8")) == 4 * (2 * 64 + 8)
+    assert bench.kv_token_bytes(W.workload("tinyllama-int4")) == 4 * (2 * 32 + 8)
+    assert bench.kv_token_bytes(W.workload("smollm2-f32")) == 3 * 2 * 64 * 4
+    assert bench.kv_token_bytes(W.workload("qwen-bf16")) == 2 * 2 * 128 * 2
+
+
+def test_decode_bytes_of_the_benchmark_workload():
+    wl = W.workload("tinyllama-int8")
+    b = wl.batches[0]
+    kv = 256 * 1024 * 4 * (2 * 64 + 8)       # every cached token's K, V and scales once
+    q = out = 256 * 32 * 64 * 4              # FP32 queries in, FP32 outputs out
+    tables = 256 * (1024 // 16) * 4          # the table entries that are read
+    lens = 256 * 4
+    assert bench.decode_bytes(wl, b) == kv + q + out + tables + lens == 146867200
+
+
+def test_append_and_prefill_accounting():
+    wl = W.workload("mixed")
+    T = 4 + 2 * 512                          # one new token per decode sequence + 2 chunks
+    assert bench.append_bytes(wl) == T * 2 * 128 * 2 * 2 + T * 2 * (2 * 128 * 2) + T * 4
+    pb = [b for b in wl.batches if b.kind == "prefill"][0]
+    keys = sum(2048 + i + 1 for i in range(512))  # causal: row i sees prior + i + 1 keys
+    assert bench.prefill_flops(wl, pb) == 2 * keys * 4 * 128 * 12
+
+
+def test_job_rate_is_all_ranks_work_over_the_slowest_time():
+    assert bench.job_rate(10.0, 4, 2.0) == 20.0
+
+
+def test_reference_arm_line(capsys, monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--workload", "tiny",
+                                      "--steps", "3", "--warmup", "3"])
+    bench.main()
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["value"] > 0
+    ident = bench.workload_config(W.workload("tiny"))
+    assert all(d["config"][k] == v for k, v in ident.items())
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+
+
+def test_our_arm_line_assembly(capsys, monkeypatch):
+    """The JSON line of our arm, assembled from fixed measurements (the GPU measurement
+    itself is replaced): every contract key, the roofline from the decode bytes and time,
+    the whole-job value from all bytes of the step."""
+    wl = W.workload("tinyllama-int8")
+    acc = bench.step_accounting(wl)
+    ms = 0.034  # per step
+    kern = [[0.0026], [0.0308]]  # append, decode (per launch)
+    e2e = {"value": 1.0, "unit": "GB/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 1,
+           "ms_per_step": 0.08, "launches": "direct"}
+    clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 5, "reasons": []}
+    monkeypatch.setattr(bench, "run_ours",
+                        lambda args, rank, world: (wl, acc, 4, ms, kern, clocks, e2e, False, 256))
+    monkeypatch.setattr(bench, "measured_hbm", lambda: (6794.5, "measured"))
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--no-cpu-baseline", "--steps", "7",
+                                      "--warmup", "3"])
+    bench.main()
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "clocks", "gpu_launches"):
+        assert key in d, key
+    assert d["n_gpus"] == 1 and d["steps"] == 7 and d["gpu_launches"] == 7 * 2
+    assert abs(d["value"] - acc["total"] / (ms * 1e-3) / 1e9) < 0.01
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["peak"] == 6794.5 and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - acc["decode"] / (0.0308e-3) / 1e9) < 0.1
+    assert abs(r["frac"] - r["achieved"] / 6794.5) < 1e-3
+    assert r["algorithmic_bytes_per_launch"] == acc["decode"]
+    assert d["config"]["workload"] == "tinyllama-int8" and d["config"]["layers"] == 1
+    assert d["dtype"] == "int8-kv/f32-acc"
