@@ -34,7 +34,7 @@ def _ranks(rank, world, port, out):
 
 def test_max_over_ranks_and_job_rate_gloo():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork: CUDA may be initialised
         out = m.dict()
         mp.spawn(_ranks, args=(world, free_port(), out), nprocs=world, join=True)
         res = dict(out)
