@@ -24,7 +24,9 @@
  *
  * Conventions shared by every call
  *   - Every pointer argument is caller-owned DEVICE memory unless stated otherwise.
- *     The library allocates nothing and frees nothing.
+ *     The library allocates no device memory and frees none; the only objects it
+ *     creates are the host-side CUDA graphs of a pkv_decode_graph, which the caller
+ *     destroys with pkv_decode_graph_destroy.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
  *   - Host-checkable errors (null pointers, shapes, dtypes, alignment, workspace size)
  *     return a status synchronously and launch nothing.
