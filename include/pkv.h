@@ -221,9 +221,12 @@ pkv_status pkv_prefill_workspace_size(const pkv_cache* cache, int32_t num_seqs,
  *   max_q_len      an upper bound of the chunk lengths (sizes the launch).
  *   context_lens   int32 [num_seqs]: cached tokens INCLUDING the chunk (append the
  *                  chunk first).  Chunk row i (chunk length Lq) sits at position
- *                  context_lens[b] - Lq + i and attends to positions 0..that position.
+ *                  context_lens[b] - Lq + i and attends to positions 0..that position
+ *                  (with a cache window W: position - W + 1 .. position).
  *   out            float32 [total_q][num_q_heads][head_dim].
  *   workspace      as for decode (pkv_prefill_workspace_size bytes; may be 0).
+ * The cache must be PKV_BF16 (other formats return PKV_ERR_UNSUPPORTED); the query tile
+ * products run on the tcgen05 tensor cores.
  */
 pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t q_dtype,
                                   int32_t num_seqs, int32_t num_q_heads,
