@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: oracle time over all warm-up and timed steps "
+                         "(each step samples at least one sequence per batch)")
     ap.add_argument("--fused", action="store_true",
                     help="the decode batch as one pkv_decode_step launch")
     ap.add_argument("--rope", action="store_true",
@@ -257,19 +260,24 @@ def traffic_from_profiles(kernel_tag, workload):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_rate(wl, seconds, threads, fused=True, rope=False):
+def cpu_oracle_rate(wl, seconds, threads, fused=True, rope=False, oc=None, counts=None):
     """Time the oracle (as it stands) on a bounded sample of the workload: whole
     sequences of the decode batch (as the same fused step when ``fused``) and of the
-    prefill batch, taken in order until about ``seconds`` of wall time.  Returns (GB/s,
-    tokens/s, sample description)."""
+    prefill batch, taken in order until about ``seconds`` of wall time (at least one
+    sequence of each batch).  ``oc``: the oracle's cache of the workload, built here when
+    not given (outside the timed calls).  ``counts``: run exactly that many sequences of
+    each batch once, instead of searching for the sample size.  Returns (GB/s, tokens/s,
+    sample description, timed seconds, sequences per batch)."""
     import oracle
-    oc = oracle.cache_from_workload(wl)
+    if oc is None:
+        oc = oracle.cache_from_workload(wl)
     d0 = wl.batches[0]
     new_rows = wl.step_rows[:d0.num_seqs]
-    done_bytes, done_tok, t_total, sample = 0, 0, 0.0, []
-    for b in wl.batches:
+    done_bytes, done_tok, t_total, sample, used = 0, 0, 0.0, [], []
+    for bi, b in enumerate(wl.batches):
         B = b.num_seqs
-        n = 1
+        # at least one sequence per host thread, so that every core the baseline reports works
+        n = min(B, max(1, threads)) if counts is None else counts[bi]
         while True:
             seqs = list(range(min(B, n)))
             t0 = time.perf_counter()
@@ -287,7 +295,7 @@ def cpu_oracle_rate(wl, seconds, threads, fused=True, rope=False):
                 oracle.prefill(oc, b.q, b.q_dtype, b.q_start_loc, b.block_tables,
                                b.context_lens, wl.scale, seqs=seqs, threads=threads)
             dt = time.perf_counter() - t0
-            if dt >= seconds / len(wl.batches) or len(seqs) == B:
+            if counts is not None or dt >= seconds / len(wl.batches) or len(seqs) == B:
                 break
             n = max(n + 1, min(B, int(n * max(2.0, 0.8 * seconds / len(wl.batches) / max(dt, 1e-3)))))
         toks = int(sum(int(b.context_lens[s]) for s in seqs))
@@ -296,7 +304,8 @@ def cpu_oracle_rate(wl, seconds, threads, fused=True, rope=False):
         done_tok += toks
         t_total += dt
         sample.append(f"{len(seqs)}/{B} {b.kind} sequences")
-    return done_bytes / t_total / 1e9, done_tok / t_total, ", ".join(sample), t_total
+        used.append(len(seqs))
+    return done_bytes / t_total / 1e9, done_tok / t_total, ", ".join(sample), t_total, used
 
 
 # ----------------------------------------------------------------------------- GPU run
@@ -556,9 +565,10 @@ def main():
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = len(os.sched_getaffinity(0))
-        gbs, tps, sample, secs = cpu_oracle_rate(wl, args.cpu_sample_seconds, threads, fused,
+        gbs, tps, sample, secs, used = cpu_oracle_rate(wl, args.cpu_sample_seconds, threads, fused,
                                                  args.rope)
-        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s",
+                                "cores": min(threads, max(used)),
                                 "kind": "oracle", "sample": sample + f" ({secs:.1f} s wall)",
                                 "seq_tokens_per_s": round(tps, 1)}
     if rank == 0:
@@ -570,15 +580,25 @@ def main():
 
 def main_reference(args):
     """The oracle as it stands, on the host cores, one bounded sample per step."""
+    import oracle
     from paged_kv_attention_09_gb300 import workloads as W
     wl = W.workload(args.workload)
     threads = len(os.sched_getaffinity(0))
-    per_step = max(0.5, args.cpu_sample_seconds / max(1, args.steps + args.warmup) * 4)
-    for _ in range(args.warmup):
-        cpu_oracle_rate(wl, per_step / 4, threads, args.fused, args.rope)
+    oc = oracle.cache_from_workload(wl)  # once, outside every step
+    # the first warm-up step finds the sample size (sequences per batch) that takes about
+    # the per-step share of the budget; every later step runs exactly that sample once
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)
+    counts = None
+    for _ in range(max(1, args.warmup)):
+        *_, took, used = cpu_oracle_rate(wl, per_step, threads, args.fused, args.rope, oc, counts)
+        if counts is None:
+            # a sample of one sequence per core that overruns its share of the budget
+            # falls back to one sequence (on one core) per batch
+            counts = [1] * len(used) if took > 2 * per_step else used
     vals, secs = [], 0.0
     for _ in range(args.steps):
-        gbs, tps, sample, s = cpu_oracle_rate(wl, per_step, threads, args.fused, args.rope)
+        gbs, tps, sample, s, _ = cpu_oracle_rate(wl, per_step, threads, args.fused, args.rope,
+                                                 oc, counts)
         vals.append(gbs)
         secs += s
     v = statistics.fmean(vals)
@@ -590,7 +610,8 @@ def main_reference(args):
             "data": "synthetic (seeded N(0,1) values, shapes of the named model family)",
             "config": {**workload_config(wl, max(1, args.layers)),
                        "timing": "host wall clock around the oracle's bounded sample"},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads,
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s",
+                             "cores": min(threads, max(counts)),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
