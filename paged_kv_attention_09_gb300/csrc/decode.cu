@@ -137,7 +137,7 @@ struct Smem {
   static constexpr int combine = (3 * kW * kMaxHeads + kW * kMaxHeads * (D + 2)) * 4;
   static constexpr int big = stages > combine ? stages : combine;
   static constexpr int probs = KVT == kF32 ? kW * kMaxHeads * kPage * 4 : 0;
-  // INT8: the query fragments (one uint4 per k-step and lane) and per-row constants,
+  // coded formats: the query fragments (one uint4 per k-step and lane) and per-row constants,
   // built once by warp 0 and read by every warp
   static constexpr int aux = quantised(KVT) ? (D / 16) * 32 * 16 + 2 * kMaxHeads * 4 : 0;
   static constexpr int bars = kW * Lo::S * 8;
