@@ -94,3 +94,25 @@ def test_our_arm_line_assembly(capsys, monkeypatch):
     assert r["algorithmic_bytes_per_launch"] == acc["decode"]
     assert d["config"]["workload"] == "tinyllama-int8" and d["config"]["layers"] == 1
     assert d["dtype"] == "int8-kv/f32-acc"
+
+
+def test_profile_traffic_follows_the_kernel_code(tmp_path, monkeypatch):
+    """A committed ncu summary's traffic is used only while its code digest matches: a
+    comment-only edit keeps it, a code edit drops it."""
+    import shutil
+    csrc = os.path.join(ROOT, "paged_kv_attention_09_gb300", "csrc")
+    root = tmp_path / "r"
+    shutil.copytree(csrc, root / "paged_kv_attention_09_gb300" / "csrc")
+    (root / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    digest = bench.code_digest("decode")
+    (root / "profiles" / "decode_w.md").write_text(
+        f"code_sha256: {digest}\ntraffic_bytes_per_launch: 1234\n")
+    assert bench.traffic_from_profiles("decode", "w") == 1234.0
+    src = root / "paged_kv_attention_09_gb300" / "csrc" / "decode.cu"
+    src.write_text(src.read_text() + "\n// a comment\n/* and another */\n")
+    assert bench.code_digest("decode") == digest
+    assert bench.traffic_from_profiles("decode", "w") == 1234.0
+    src.write_text(src.read_text() + "\nstatic int pkv_extra_symbol = 1;\n")
+    assert bench.code_digest("decode") != digest
+    assert bench.traffic_from_profiles("decode", "w") is None
