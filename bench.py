@@ -36,6 +36,7 @@ METRIC = "decode attn achieved HBM GB/s & seq-tokens/s vs 8 TB/s roofline, 1 GB3
 ROPE_THETA = 10000.0
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED = 1900.0, 1700.0
 
 
 def parse():
@@ -169,6 +170,18 @@ def measured_hbm():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16():
+    """Measured dense BF16 TFLOP/s (burst, sustained) of the GB300s, or the
+    fallback figures."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
 class ClockSampler:
@@ -558,19 +571,31 @@ def main():
                             "traffic": traffic_from_profiles("decode", wl.name),
                             "algorithmic_bytes_per_launch": acc["decode"]}
     if "prefill" in avg:
-        line["prefill"] = {"ms": round(avg["prefill"], 5),
-                           "tflops": round(acc["prefill_flops"] / (avg["prefill"] * 1e-3) / 1e12, 1)}
+        tf = acc["prefill_flops"] / (avg["prefill"] * 1e-3) / 1e12
+        burst, sustained, src = measured_bf16()
+        line["prefill"] = {"ms": round(avg["prefill"], 5), "tflops": round(tf, 1),
+                           "frac_of_bf16_burst": round(tf / burst, 4),
+                           "frac_of_bf16_sustained": round(tf / sustained, 4),
+                           "peak_source": src}
     if e2e:
         line["e2e"] = e2e
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = len(os.sched_getaffinity(0))
+        import oracle
+        oc = oracle.cache_from_workload(wl)  # built once for both samples
         gbs, tps, sample, secs, used = cpu_oracle_rate(wl, args.cpu_sample_seconds, threads, fused,
-                                                 args.rope)
+                                                       args.rope, oc)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s",
                                 "cores": min(threads, max(used)),
                                 "kind": "oracle", "sample": sample + f" ({secs:.1f} s wall)",
                                 "seq_tokens_per_s": round(tps, 1)}
+        # the same oracle on one core, on a shorter sample
+        gbs1, tps1, sample1, secs1, _ = cpu_oracle_rate(wl, args.cpu_sample_seconds / 4, 1,
+                                                        fused, args.rope, oc)
+        line["cpu_baseline"]["single_core"] = {
+            "value": round(gbs1, 4), "unit": "GB/s", "seq_tokens_per_s": round(tps1, 1),
+            "sample": sample1 + f" ({secs1:.1f} s wall)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -116,3 +116,34 @@ def test_profile_traffic_follows_the_kernel_code(tmp_path, monkeypatch):
     src.write_text(src.read_text() + "\nstatic int pkv_extra_symbol = 1;\n")
     assert bench.code_digest("decode") != digest
     assert bench.traffic_from_profiles("decode", "w") is None
+
+
+def test_line_with_prefill_and_cpu_baselines(capsys, monkeypatch):
+    """The mixed workload's line: prefill TFLOP/s against the measured BF16 peaks, and the
+    oracle's all-core and single-core rates (the oracle itself replaced here)."""
+    wl = W.workload("mixed")
+    acc = bench.step_accounting(wl)
+    kern = [[0.006], [0.0287], [0.0377]]  # append, decode, prefill
+    monkeypatch.setattr(bench, "run_ours", lambda args, rank, world: (
+        wl, acc, 4, 0.08, kern, None, None, False, 1028))
+    monkeypatch.setattr(bench, "measured_hbm", lambda: (6794.5, "measured"))
+    monkeypatch.setattr(bench, "measured_bf16", lambda: (1903.5, 1700.2, "measured"))
+    calls = []
+
+    def fake_rate(wl_, seconds, threads, fused=True, rope=False, oc=None, counts=None):
+        calls.append(threads)
+        return (0.5 if threads > 1 else 0.1), 1e6, "2/4 decode sequences", 1.0, [2, 1]
+    monkeypatch.setattr(bench, "cpu_oracle_rate", fake_rate)
+    import oracle
+    monkeypatch.setattr(oracle, "cache_from_workload", lambda wl_: None)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "mixed", "--steps", "5",
+                                      "--warmup", "3", "--no-e2e"])
+    bench.main()
+    d = json.loads([l for l in capsys.readouterr().out.splitlines() if l.startswith("{")][-1])
+    tf = acc["prefill_flops"] / 0.0377e-3 / 1e12
+    assert abs(d["prefill"]["tflops"] - tf) < 0.1
+    assert abs(d["prefill"]["frac_of_bf16_burst"] - tf / 1903.5) < 1e-3
+    assert abs(d["prefill"]["frac_of_bf16_sustained"] - tf / 1700.2) < 1e-3
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == 0.5 and cb["single_core"]["value"] == 0.1
+    assert cb["cores"] == min(len(os.sched_getaffinity(0)), 2) and calls[-1] == 1
