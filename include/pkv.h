@@ -6,8 +6,15 @@
  *   pkv_append              write new tokens' K/V rows into cache pages via a slot map
  *   pkv_decode_attn         one query token per sequence against its paged context
  *   pkv_prefill_chunk_attn  a causal chunk of query tokens against its paged context
+ *
+ * and around them:
+ *
  *   pkv_decode_step         one launch for a whole decode step: rotary embedding of the
  *                           new query and key, append of the new K/V row, attention
+ *   pkv_decode_graph_*      a decode step (all layers) captured once per batch-size
+ *                           bucket and replayed with one CUDA graph launch
+ *   pkv_decode_attn_noalloc decode attention with its split scratch inside the library
+ *   *_workspace_size, pkv_set_decode_chunk_pages, pkv_status_string   host helpers
  *
  * Sources (page title, section):
  *   "Tiny-LLM-Inference Project_Status", feature list and dtype contract: paged KV
@@ -60,11 +67,14 @@
  *   Token t of a sequence lives in page block_tables[b][t / page_size] at offset
  *   t % page_size; its slot number is page * page_size + offset.
  *   Element types: PKV_F32 float32, PKV_BF16 bfloat16, and three coded formats whose
- *   value is code * scale with one scale per (token, kv head): PKV_INT8 codes in
- *   [-127, 127] stored in offset binary (the byte holds code + 128), scale = max|x| / 127; PKV_FP8 E4M3 codes (OCP "fn": bias 7, no infinity, largest
- *   finite 448), scale = max|x| / 448; PKV_INT4 4-bit two's-complement codes in
- *   [-7, 7], scale = max|x| / 7 ("tinyloop Current Status", KV cache modes table: INT8
- *   and INT4 KV caches; the TinyInfer review, item 2: INT8 or FP8 KV cache).
+ *   value is code * scale with one scale per (token, kv head):
+ *     PKV_INT8  codes in [-127, 127] stored in offset binary (the byte holds code + 128),
+ *               scale = max|x| / 127;
+ *     PKV_FP8   E4M3 codes (OCP "fn": bias 7, no infinity, largest finite 448),
+ *               scale = max|x| / 448;
+ *     PKV_INT4  4-bit two's-complement codes in [-7, 7], scale = max|x| / 7
+ *   ("tinyloop Current Status", KV cache modes table: INT8 and INT4 KV caches; the
+ *   TinyInfer review, item 2: INT8 or FP8 KV cache).
  *   All cache pointers must be 16-byte aligned.
  *
  * Sliding window (pkv_cache.window; "tinyloop Current Status", KV cache modes table: a
