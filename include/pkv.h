@@ -14,7 +14,8 @@
  *   pkv_decode_graph_*      a decode step (all layers) captured once per batch-size
  *                           bucket and replayed with one CUDA graph launch
  *   pkv_decode_attn_noalloc decode attention with its split scratch inside the library
- *   *_workspace_size, pkv_set_decode_chunk_pages, pkv_status_string   host helpers
+ *   *_ex                    the decode calls with per-call options (pkv_decode_opts)
+ *   *_workspace_size, pkv_status_string                               host helpers
  *
  * Sources (page title, section):
  *   "Tiny-LLM-Inference Project_Status", feature list and dtype contract: paged KV
@@ -150,14 +151,32 @@ pkv_status pkv_append(const pkv_cache* cache, const void* k_new, const void* v_n
                       int32_t* dev_status, void* stream);
 
 /*
+ * Options of one decode call (pkv_decode_attn_ex, pkv_decode_step_ex,
+ * pkv_decode_attn_noalloc_ex, pkv_decode_workspace_size_ex); a NULL pointer means every
+ * option at its default.
+ *   split_pages  pages of a sequence's context handled by one thread block (split-K);
+ *                0 (default) chooses it from the shape and the device's SM count.  The
+ *                split only reorders floating-point sums: a fixed value gives
+ *                bit-identical results on every device, and bounds the workspace.
+ *                Must be >= 0.
+ */
+typedef struct pkv_decode_opts {
+  int32_t split_pages;
+} pkv_decode_opts;
+
+/*
  * Scratch bytes pkv_decode_attn (and pkv_decode_step) needs for this shape on the
- * current device (host call, no launch).  The split of long contexts across thread blocks is a fixed
- * function of (shape, device SM count, pkv_set_decode_chunk_pages), so equal
- * arguments give bit-identical results.  Writes the size to *bytes (0 is possible).
+ * current device (host call, no launch).  The split of long contexts across thread
+ * blocks is a fixed function of the shape, the device's SM count and the options, so
+ * equal arguments give bit-identical results.  Writes the size to *bytes (0 is possible).
+ * The size covers both calls; the _ex form answers for the given options.
  */
 pkv_status pkv_decode_workspace_size(const pkv_cache* cache, int32_t num_seqs,
                                      int32_t num_q_heads, int32_t max_blocks_per_seq,
                                      size_t* bytes);
+pkv_status pkv_decode_workspace_size_ex(const pkv_cache* cache, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                        const pkv_decode_opts* opts, size_t* bytes);
 
 /*
  * Batched decode attention ("mini-llm-inference-engine" README: true batched decode;
@@ -179,6 +198,14 @@ pkv_status pkv_decode_attn(const pkv_cache* cache, const void* q, int32_t q_dtyp
                            int32_t max_blocks_per_seq, const int32_t* context_lens,
                            float scale, float* out, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, void* stream);
+/* pkv_decode_attn with options (see pkv_decode_opts; size the workspace with
+ * pkv_decode_workspace_size_ex and the same options). */
+pkv_status pkv_decode_attn_ex(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                              int32_t num_seqs, int32_t num_q_heads,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, float scale, float* out,
+                              void* workspace, size_t workspace_bytes,
+                              const pkv_decode_opts* opts, int32_t* dev_status, void* stream);
 
 /*
  * One decode step in one launch ("tinyloop Current Status", model architecture support
@@ -214,6 +241,15 @@ pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtyp
                            const int32_t* context_lens, float scale, float* out,
                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
                            void* stream);
+/* pkv_decode_step with options (see pkv_decode_opts). */
+pkv_status pkv_decode_step_ex(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                              const void* k_new, const void* v_new, int32_t new_dtype,
+                              const int32_t* slot_mapping, const int32_t* positions,
+                              double rope_theta, int32_t num_seqs, int32_t num_q_heads,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, float scale, float* out,
+                              void* workspace, size_t workspace_bytes,
+                              const pkv_decode_opts* opts, int32_t* dev_status, void* stream);
 
 /*
  * Scratch bytes pkv_prefill_chunk_attn needs (host call, no launch); see above.
@@ -255,15 +291,22 @@ pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t
  * split-K scratch taken from a fixed array of PKV_NOALLOC_SCRATCH_BYTES in the
  * library's own device memory (reserved on every GPU that loads the library, until the
  * process exits).  It allocates nothing and calls no allocating routine.
- *   - Shapes whose split scratch (what pkv_decode_workspace_size reports) exceeds
- *     PKV_NOALLOC_SCRATCH_BYTES return PKV_ERR_WORKSPACE and launch nothing.
+ *   - Shapes whose split scratch (what pkv_decode_workspace_size_ex reports for the
+ *     same options) exceeds PKV_NOALLOC_SCRATCH_BYTES return PKV_ERR_WORKSPACE and
+ *     launch nothing.
  *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any stream
- *     capture.
- *   - Every call shares the one array: calls whose work overlaps on the GPU (other
- *     streams, other threads) race and must be serialised by the caller.  Each call
- *     clears the merge counters it needs on `stream` before its kernel.
- * Other arguments, errors and results are those of pkv_decode_attn.
+ *     device, with that device current) and keeps it for the life of the process; make
+ *     that first call before any stream capture.  A cudaDeviceReset of that device
+ *     makes the kept address stale: do not call this entry point on it afterwards.
+ *   - Every call shares the one array, which keeps the last call's contents: calls
+ *     whose work overlaps on the GPU (other streams, other threads) race and must be
+ *     serialised by the caller.  Each call first clears, on `stream`, the merge counters
+ *     it uses (one small memset): a caller's workspace is the caller's to keep zeroed,
+ *     but this array is shared by calls of every shape, and a call that stopped before
+ *     its merge (a failed launch, a wait that gave up) must not leak counts into the
+ *     next one.
+ * Other arguments, errors and results are those of pkv_decode_attn (the _ex form: of
+ * pkv_decode_attn_ex), bit for bit.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (4u << 20)
 pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void* q, int32_t q_dtype,
@@ -271,6 +314,12 @@ pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void* q, int32_
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
                                    const int32_t* context_lens, float scale, float* out,
                                    int32_t* dev_status, void* stream);
+pkv_status pkv_decode_attn_noalloc_ex(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                                      int32_t num_seqs, int32_t num_q_heads,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, float scale, float* out,
+                                      const pkv_decode_opts* opts, int32_t* dev_status,
+                                      void* stream);
 
 /*
  * Bucketed CUDA-graph executor for small-batch decode steps ("mini-llm-inference-engine"
@@ -352,13 +401,6 @@ int32_t pkv_decode_graph_bucket(const pkv_decode_graph* graph, int32_t num_seqs)
 
 /* Releases the executor's graphs (after its launches have completed); NULL is a no-op. */
 void pkv_decode_graph_destroy(pkv_decode_graph* graph);
-
-/*
- * Tuning override: pages per thread block for the decode split (0 = automatic, the
- * default).  Process-wide; affects pkv_decode_workspace_size.  Meant for tests and
- * sweeps, not for changing results (splits only reorder floating-point sums).
- */
-void pkv_set_decode_chunk_pages(int32_t pages);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* pkv_status_string(pkv_status status);

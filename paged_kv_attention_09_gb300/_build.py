@@ -1,5 +1,8 @@
 """Build libpkv.so (sm_103a) from csrc/ with nvcc: one object per translation unit,
-compiled in parallel, then linked against the shared CUDA runtime."""
+compiled in parallel, then linked against the shared CUDA runtime.
+
+With the environment variable PKV_NVTX=1 at build time, every C entry point is wrapped
+in an NVTX range named after it (for profiler timelines)."""
 from __future__ import annotations
 
 import os
@@ -19,6 +22,10 @@ SOURCES = ("api.cu", "append.cu", "decode.cu", "prefill.cu", "prefill_tc.cu", "n
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", INCLUDE, "-I", CSRC]
+
+
+def _defines() -> list:
+    return ["-DPKV_NVTX"] if os.environ.get("PKV_NVTX") == "1" else []
 
 
 def cuda_home() -> str:
@@ -44,12 +51,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OBJ, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "pkv.h"))
+    # objects built with other defines are stale
+    stamp = os.path.join(OBJ, "defines.txt")
+    want = " ".join(_defines())
+    if not os.path.exists(stamp) or open(stamp).read() != want:
+        force = True
+        with open(stamp, "w") as f:
+            f.write(want)
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
         o = os.path.join(OBJ, src.replace(".cu", ".o"))
         if force or _stale(o, [s, *headers]):
-            cmd = [nvcc, *ARCH, *FLAGS, "-c", s, "-o", o + ".tmp"]
+            cmd = [nvcc, *ARCH, *FLAGS, *_defines(), "-c", s, "-o", o + ".tmp"]
             r = subprocess.run(cmd, capture_output=True, text=True)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -64,7 +78,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         libdir = os.path.join(home, "lib64")
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-               "-Xlinker", f"-rpath,{libdir}"]
+               "-Xlinker", f"-rpath,{libdir}", *(["-ldl"] if _defines() else [])]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -2,19 +2,15 @@
 // planning and launches.  Allocates nothing; every buffer belongs to the caller
 // ("Tiny-LLM-Inference Project_Status", runtime notes: buffers are preallocated from the
 // resolved capacity and an oversized request fails fast instead of reallocating).
-#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "abi.h"
 #include "internal.h"
+#include "nvtx.h"
 #include "pkv.h"
 
-namespace {
-
-std::atomic<int> g_chunk_override{0};
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+namespace pkv {
 
 pkv_status check_cache(const pkv_cache* c) {
   if (!c || !c->k_cache || !c->v_cache) return PKV_ERR_NULL;
@@ -23,43 +19,91 @@ pkv_status check_cache(const pkv_cache* c) {
   if (c->num_pages < 1 || c->num_kv_heads < 1 || c->head_dim < 1) return PKV_ERR_SHAPE;
   if (c->window < 0) return PKV_ERR_SHAPE;
   if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (pkv::quantised(c->kv_dtype) && (!c->k_scale || !c->v_scale)) return PKV_ERR_NULL;
+  if (quantised(c->kv_dtype) && (!c->k_scale || !c->v_scale)) return PKV_ERR_NULL;
   if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PKV_ERR_ALIGN;
-  if (pkv::quantised(c->kv_dtype) && (!aligned16(c->k_scale) || !aligned16(c->v_scale)))
+  if (quantised(c->kv_dtype) && (!aligned16(c->k_scale) || !aligned16(c->v_scale)))
     return PKV_ERR_ALIGN;
   // every page block must stay addressable with 32-bit slot numbers
   if (static_cast<long long>(c->num_pages) * c->page_size > 0x7fffffffLL) return PKV_ERR_SHAPE;
   return PKV_OK;
 }
 
-pkv::CacheView view(const pkv_cache* c) {
-  return pkv::CacheView{c->k_cache, c->v_cache, c->k_scale, c->v_scale,
-                        c->num_pages, c->num_kv_heads, c->head_dim, c->kv_dtype, c->window};
+pkv_status check_decode_shape(const pkv_cache* c, int32_t num_seqs, int32_t Hq, int32_t MB) {
+  if (num_seqs < 0 || Hq < 1 || MB < 1) return PKV_ERR_SHAPE;
+  if (Hq % c->num_kv_heads != 0) return PKV_ERR_SHAPE;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;  // grid.y limit
+  // token positions over a whole block-table row stay 32-bit
+  if (static_cast<long long>(MB) * c->page_size > 0x7fffffffLL) return PKV_ERR_SHAPE;
+  return PKV_OK;
 }
+
+pkv_status check_decode_call(const pkv_cache* c, const void* q, int32_t q_dtype,
+                             int32_t num_seqs, int32_t num_q_heads, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             const float* out, const int32_t* dev_status) {
+  pkv_status s = check_cache(c);
+  if (s != PKV_OK) return s;
+  s = check_decode_shape(c, num_seqs, num_q_heads, max_blocks_per_seq);
+  if (s != PKV_OK) return s;
+  if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !block_tables || !context_lens || !out) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(block_tables) || !aligned4(context_lens))
+    return PKV_ERR_ALIGN;
+  if (dev_status && !aligned4(dev_status)) return PKV_ERR_ALIGN;
+  return PKV_OK;
+}
+
+bool split_pages_of(const pkv_decode_opts* opts, int* pages) {
+  *pages = opts ? opts->split_pages : 0;
+  return *pages >= 0;
+}
+
+CacheView view(const pkv_cache* c) {
+  return CacheView{c->k_cache, c->v_cache, c->k_scale, c->v_scale,
+                   c->num_pages, c->num_kv_heads, c->head_dim, c->kv_dtype, c->window};
+}
+
+}  // namespace pkv
+
+namespace {
+
+using pkv::aligned16;
+using pkv::aligned4;
+using pkv::check_cache;
+using pkv::check_decode_shape;
+using pkv::view;
 
 pkv_status current_device(int* dev) {
   return cudaGetDevice(dev) == cudaSuccess ? PKV_OK : PKV_ERR_DEVICE;
 }
 
-pkv_status check_decode_shape(const pkv_cache* c, int32_t num_seqs, int32_t Hq, int32_t MB) {
-  if (num_seqs < 0 || Hq < 1 || MB < 1) return PKV_ERR_SHAPE;
-  if (Hq % c->num_kv_heads != 0) return PKV_ERR_SHAPE;
-  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;  // grid.y limit
-  if (static_cast<long long>(MB) * c->page_size > 0x7fffffffLL) return PKV_ERR_SHAPE;
-  return PKV_OK;
+// Plans and launches one decode call (a.step: the fused decode step) after the checks.
+pkv_status decode_launch(const pkv_cache* cache, pkv::DecodeArgs& a, int split_pages,
+                         size_t workspace_bytes, cudaStream_t st) {
+  int dev = 0;
+  pkv_status s = current_device(&dev);
+  if (s != PKV_OK) return s;
+  pkv::DecodePlan plan{};
+  if (!pkv::plan_decode(a.c, a.B, a.Hq, a.MB, a.q_dtype, dev, split_pages, &plan, a.step))
+    return PKV_ERR_DEVICE;
+  if (static_cast<long long>(cache->num_kv_heads) * plan.head_groups > 65535)
+    return PKV_ERR_UNSUPPORTED;
+  if (plan.ws_bytes > 0) {
+    if (!a.ws || workspace_bytes < plan.ws_bytes) return PKV_ERR_WORKSPACE;
+    if (!aligned16(a.ws)) return PKV_ERR_ALIGN;
+  }
+  return pkv::launch_decode(a, plan, st) == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
 }  // namespace
-
-namespace pkv {
-int decode_chunk_override() { return g_chunk_override.load(); }
-}  // namespace pkv
 
 extern "C" {
 
 pkv_status pkv_append(const pkv_cache* cache, const void* k_new, const void* v_new,
                       int32_t new_dtype, const int32_t* slot_mapping, int32_t num_tokens,
                       int32_t* dev_status, void* stream) {
+  PKV_RANGE("pkv_append");
   pkv_status s = check_cache(cache);
   if (s != PKV_OK) return s;
   if (num_tokens < 0) return PKV_ERR_SHAPE;
@@ -74,55 +118,50 @@ pkv_status pkv_append(const pkv_cache* cache, const void* k_new, const void* v_n
   return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
-pkv_status pkv_decode_workspace_size(const pkv_cache* cache, int32_t num_seqs,
-                                     int32_t num_q_heads, int32_t max_blocks_per_seq,
-                                     size_t* bytes) {
+pkv_status pkv_decode_workspace_size_ex(const pkv_cache* cache, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                        const pkv_decode_opts* opts, size_t* bytes) {
   if (!bytes) return PKV_ERR_NULL;
   *bytes = 0;
   pkv_status s = check_cache(cache);
   if (s != PKV_OK) return s;
   s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
   if (s != PKV_OK) return s;
+  int split = 0;
+  if (!pkv::split_pages_of(opts, &split)) return PKV_ERR_SHAPE;
   int dev = 0;
   if ((s = current_device(&dev)) != PKV_OK) return s;
   // one size for both pkv_decode_attn and pkv_decode_step (their plans may differ)
   pkv::DecodePlan plan{}, plan_step{};
   if (!pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, PKV_F32, dev,
-                        g_chunk_override.load(), &plan) ||
+                        split, &plan) ||
       !pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, PKV_F32, dev,
-                        g_chunk_override.load(), &plan_step, true))
+                        split, &plan_step, true))
     return PKV_ERR_DEVICE;
   *bytes = plan.ws_bytes > plan_step.ws_bytes ? plan.ws_bytes : plan_step.ws_bytes;
   return PKV_OK;
 }
 
-pkv_status pkv_decode_attn(const pkv_cache* cache, const void* q, int32_t q_dtype,
-                           int32_t num_seqs, int32_t num_q_heads, const int32_t* block_tables,
-                           int32_t max_blocks_per_seq, const int32_t* context_lens,
-                           float scale, float* out, void* workspace, size_t workspace_bytes,
-                           int32_t* dev_status, void* stream) {
-  pkv_status s = check_cache(cache);
+pkv_status pkv_decode_workspace_size(const pkv_cache* cache, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                     size_t* bytes) {
+  return pkv_decode_workspace_size_ex(cache, num_seqs, num_q_heads, max_blocks_per_seq, nullptr,
+                                      bytes);
+}
+
+pkv_status pkv_decode_attn_ex(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                              int32_t num_seqs, int32_t num_q_heads,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, float scale, float* out,
+                              void* workspace, size_t workspace_bytes,
+                              const pkv_decode_opts* opts, int32_t* dev_status, void* stream) {
+  PKV_RANGE("pkv_decode_attn");
+  pkv_status s = pkv::check_decode_call(cache, q, q_dtype, num_seqs, num_q_heads, block_tables,
+                                        max_blocks_per_seq, context_lens, out, dev_status);
   if (s != PKV_OK) return s;
-  s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
-  if (s != PKV_OK) return s;
-  if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  int split = 0;
+  if (!pkv::split_pages_of(opts, &split)) return PKV_ERR_SHAPE;
   if (num_seqs == 0) return PKV_OK;
-  if (!q || !block_tables || !context_lens || !out) return PKV_ERR_NULL;
-  if (!aligned16(q) || !aligned16(out) || !aligned4(block_tables) || !aligned4(context_lens))
-    return PKV_ERR_ALIGN;
-  if (dev_status && !aligned4(dev_status)) return PKV_ERR_ALIGN;
-  int dev = 0;
-  if ((s = current_device(&dev)) != PKV_OK) return s;
-  pkv::DecodePlan plan{};
-  if (!pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, q_dtype, dev,
-                        g_chunk_override.load(), &plan))
-    return PKV_ERR_DEVICE;
-  if (static_cast<long long>(cache->num_kv_heads) * plan.head_groups > 65535)
-    return PKV_ERR_UNSUPPORTED;
-  if (plan.ws_bytes > 0) {
-    if (!workspace || workspace_bytes < plan.ws_bytes) return PKV_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return PKV_ERR_ALIGN;
-  }
   pkv::DecodeArgs a{};
   a.c = view(cache);
   a.q = q;
@@ -136,18 +175,28 @@ pkv_status pkv_decode_attn(const pkv_cache* cache, const void* q, int32_t q_dtyp
   a.out = out;
   a.ws = workspace;
   a.dev_status = dev_status;
-  const cudaError_t e = pkv::launch_decode(a, plan, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+  return decode_launch(cache, a, split, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
-pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtype,
-                           const void* k_new, const void* v_new, int32_t new_dtype,
-                           const int32_t* slot_mapping, const int32_t* positions,
-                           double rope_theta, int32_t num_seqs, int32_t num_q_heads,
-                           const int32_t* block_tables, int32_t max_blocks_per_seq,
-                           const int32_t* context_lens, float scale, float* out,
-                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                           void* stream) {
+pkv_status pkv_decode_attn(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                           int32_t num_seqs, int32_t num_q_heads, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           float scale, float* out, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream) {
+  return pkv_decode_attn_ex(cache, q, q_dtype, num_seqs, num_q_heads, block_tables,
+                            max_blocks_per_seq, context_lens, scale, out, workspace,
+                            workspace_bytes, nullptr, dev_status, stream);
+}
+
+pkv_status pkv_decode_step_ex(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                              const void* k_new, const void* v_new, int32_t new_dtype,
+                              const int32_t* slot_mapping, const int32_t* positions,
+                              double rope_theta, int32_t num_seqs, int32_t num_q_heads,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, float scale, float* out,
+                              void* workspace, size_t workspace_bytes,
+                              const pkv_decode_opts* opts, int32_t* dev_status, void* stream) {
+  PKV_RANGE("pkv_decode_step");
   pkv_status s = check_cache(cache);
   if (s != PKV_OK) return s;
   s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
@@ -155,6 +204,8 @@ pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtyp
   if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_DTYPE;
   if (new_dtype != PKV_F32 && new_dtype != PKV_BF16) return PKV_ERR_DTYPE;
   if (positions && !(rope_theta > 1.0)) return PKV_ERR_SHAPE;
+  int split = 0;
+  if (!pkv::split_pages_of(opts, &split)) return PKV_ERR_SHAPE;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_new || !v_new || !slot_mapping || !block_tables || !context_lens || !out)
     return PKV_ERR_NULL;
@@ -163,18 +214,6 @@ pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtyp
       (positions && !aligned4(positions)))
     return PKV_ERR_ALIGN;
   if (dev_status && !aligned4(dev_status)) return PKV_ERR_ALIGN;
-  int dev = 0;
-  if ((s = current_device(&dev)) != PKV_OK) return s;
-  pkv::DecodePlan plan{};
-  if (!pkv::plan_decode(view(cache), num_seqs, num_q_heads, max_blocks_per_seq, q_dtype, dev,
-                        g_chunk_override.load(), &plan, true))
-    return PKV_ERR_DEVICE;
-  if (static_cast<long long>(cache->num_kv_heads) * plan.head_groups > 65535)
-    return PKV_ERR_UNSUPPORTED;
-  if (plan.ws_bytes > 0) {
-    if (!workspace || workspace_bytes < plan.ws_bytes) return PKV_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return PKV_ERR_ALIGN;
-  }
   pkv::DecodeArgs a{};
   a.c = view(cache);
   a.q = q;
@@ -199,8 +238,21 @@ pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtyp
   a.slots = slot_mapping;
   a.positions = positions;
   a.rope_theta = rope_theta;
-  const cudaError_t e = pkv::launch_decode(a, plan, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+  return decode_launch(cache, a, split, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                           const void* k_new, const void* v_new, int32_t new_dtype,
+                           const int32_t* slot_mapping, const int32_t* positions,
+                           double rope_theta, int32_t num_seqs, int32_t num_q_heads,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, float scale, float* out,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream) {
+  return pkv_decode_step_ex(cache, q, q_dtype, k_new, v_new, new_dtype, slot_mapping, positions,
+                            rope_theta, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                            context_lens, scale, out, workspace, workspace_bytes, nullptr,
+                            dev_status, stream);
 }
 
 pkv_status pkv_prefill_workspace_size(const pkv_cache* cache, int32_t num_seqs,
@@ -230,6 +282,7 @@ pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t
                                   const int32_t* context_lens, float scale, float* out,
                                   void* workspace, size_t workspace_bytes,
                                   int32_t* dev_status, void* stream) {
+  PKV_RANGE("pkv_prefill_chunk_attn");
   pkv_status s = check_cache(cache);
   if (s != PKV_OK) return s;
   s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
@@ -271,8 +324,6 @@ pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t
   const cudaError_t e = pkv::launch_prefill(a, plan, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
-
-void pkv_set_decode_chunk_pages(int32_t pages) { g_chunk_override.store(pages > 0 ? pages : 0); }
 
 const char* pkv_status_string(pkv_status status) {
   switch (status) {

@@ -9,7 +9,7 @@
 //
 // Thread-block layout: grid (split, sequence, kv-head x head-group).  A block owns up to
 // 8 query heads that share one kv head, and a contiguous range of the sequence's
-// logical pages.  Each of its 4 warps streams every 4th group of PPI pages of that range
+// logical pages.  Each of its 4 warps streams every 4th page of that range
 // through its own ring of shared-memory stages filled by 1-D bulk copies (TMA engine,
 // one copy per K block, V block and scale vector of a (page, kv-head)).  The producer
 // lane validates every page id just before issuing its copies, so the first copies are
@@ -92,13 +92,8 @@ struct RowBytes {
   static constexpr int value = KVT == kF32 ? 4 * D : KVT == kBF16 ? 2 * D : KVT == kINT4 ? D / 2 : D;
 };
 
-// Pages per iteration of a warp, stages (iterations in flight) per warp, and the
-// resident blocks per SM the kernel is compiled for.  The copies always land well
-// before a warp needs them, so the stage depth is kept small in favour of more
-// resident warps (the per-page math is what bounds these kernels).
-#ifndef PKV_INT8_PPI
-#define PKV_INT8_PPI 1
-#endif
+// Stages (pages in flight) per warp, and the resident blocks per SM the kernel is
+// compiled for.
 #ifndef PKV_INT8_STAGES
 #define PKV_INT8_STAGES 3
 #endif
@@ -107,7 +102,6 @@ struct RowBytes {
 #endif
 template <int KVT, int D>
 struct Tune {
-  static constexpr int PPI = quantised(KVT) ? PKV_INT8_PPI : 1;
   static constexpr int S = quantised(KVT) ? PKV_INT8_STAGES
                          : KVT == kBF16 ? (D == 64 ? 3 : PKV_BF16_STAGES)
                                         : (D == 64 ? 3 : 2);
@@ -123,9 +117,8 @@ struct Layout {
   static constexpr int vBytes = kBytes;                            // V block of one (page, head)
   static constexpr int sBytes = quantised(KVT) ? kPage * 4 : 0;  // one scale vector
   static constexpr int pageBytes = kBytes + vBytes + 2 * sBytes;
-  static constexpr int PPI = Tune<KVT, D>::PPI;
   static constexpr int S = Tune<KVT, D>::S;
-  static constexpr int stageBytes = PPI * pageBytes;
+  static constexpr int stageBytes = pageBytes;
 };
 
 template <int KVT, int D, bool STEP = false>
@@ -222,7 +215,7 @@ struct F32Warp {
   float m[HM], l[HM];
   float o[HM][NC];
 
-  __device__ void finish(const uint8_t*, int) {}
+  __device__ void finish(const uint8_t*, int, uint32_t) {}
   // (loading the queries before the first copy measured slower here: they are only
   // consumed by the first page anyway)
   __device__ void prefetch(const DParams&, int, int, int, int, int) {}
@@ -360,7 +353,7 @@ struct Bf16Warp {
   float o[NT][4];
   float m, l, row_scale;
 
-  __device__ void finish(const uint8_t*, int) {}
+  __device__ void finish(const uint8_t*, int, uint32_t) {}
   // Query elements of k-slots {2c, 2c+1} and {2c+8, 2c+9} of every k-step (the standard
   // fragment order), loaded as raw bits: two BF16 or two FP32 values per slot pair.
   __device__ void prefetch(const DParams& p, int b, int h0, int nh, int lane, int) {
@@ -505,37 +498,52 @@ struct Bf16Warp {
 // One path for the three coded formats: the codes become exact f16 MMA operands.
 //   INT8  1152 + code (two byte permutes per 4 stored codes); bias removed afterwards
 //   INT4  (24 + code) / 16 (one shift and one mask-and-xor per 2 codes); the factor 16
-//         goes into the score scale and the probabilities, the bias is removed afterwards
+//         goes into the score scale and the V scales, the bias is removed afterwards
 //   FP8   the E4M3 value itself (hardware conversion, 2 codes per instruction), no bias
+// The per-page path is written against an explicit instruction budget: every shared
+// address is a per-lane base plus a constant (the ring of stages is unrolled), the V
+// codes arrive with two ldmatrix per 64 head-dim rows, the softmax runs on packed FP32
+// pairs, and masking is confined to the few pages that are only partly attended.
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale margin of the coded formats' softmax
+
+// (a, b) -> f16x2 high part and f16x2 remainder: a = hi + lo to ~22 bits.
+__device__ __forceinline__ void split_h2x(float2 a, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __float22half2_rn(a);
+  const float2 f = __half22float2(h);
+  const __half2 r = __float22half2_rn(__fadd2_rn(a, make_float2(-f.x, -f.y)));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
 
 template <int KVT, int D>
 struct QuantWarp {
   static constexpr int KS = D / 16;  // k-steps of the q.k product
   static constexpr int MT = D / 16;  // m-tiles (16 head-dim rows) of O^T = V^T P^T
-  static constexpr int PPI = Tune<KVT, D>::PPI;  // pages per iteration
+  static constexpr int RB = RowBytes<KVT, D>::value;  // bytes of one stored K row
   // the operands are 2^kMulLog2 (kBias + code)
   static constexpr float kBias = KVT == kINT8 ? 1152.f : KVT == kINT4 ? 24.f : 0.f;
   static constexpr int kMulLog2 = KVT == kINT4 ? -4 : 0;
-  const uint4* qs;                   // [k-step][lane] f16 A fragments of the query rows
-                                     // (hi 0-7, lo 8-15), in shared memory
+  // per-lane shared-window addresses in stage 0 of this warp's ring (a stage adds a
+  // constant): scale vectors, the two K rows, the ldmatrix row of the V block, and the
+  // first query fragment
+  uint32_t a_sc, a_k, a_v, a_q;
   // O^T accumulators: lane (r, c) holds head-dim rows 16 mt + r and 16 mt + r + 8 of
   // heads 2c and 2c + 1 (the C layout of the transposed product)
   float o[MT][4];
-  // per query head r = lane / 4: nm = -(running max in log2 units); scores stay in raw
-  // units and the head's log2 scale row_scale applies inside the exponent
-  float nm, l, sp, row_scale, kbias;
+  // per query head r = lane / 4, both halves equal: -(running max) in log2 units, and
+  // the head's log2 scale (scores stay in raw units; the scale applies in the exponent)
+  float2 nm2, rs2;
+  float2 l2, sp2;  // running sums of P and of P * s_v, two partial sums each
+  float kbias;     // kBias * sum(q) of the head, as the MMA sees q
 
   // k-slot pair {2c, 2c+1} of k-step ks <-> head_dim 64(ks/4) + 16c + 4(ks%4): each lane's
   // K operand is then one contiguous 16-byte shared-memory load per n-tile.
   __device__ static int kslot_d(int ks, int c) { return 64 * (ks >> 2) + 16 * c + 4 * (ks & 3); }
 
-  // (loading the queries ahead of the first copy, into registers or by a bulk copy into
-  // shared memory, measured slower for this register-bound kernel)
   __device__ void prefetch(const DParams&, int, int, int, int, int) {}
 
-  // Warp 0 builds the fragments and the per-row constants; the caller synchronises the
-  // block before any warp reads them (finish()).
+  // Warp 0 builds the query fragments and the per-row constants in shared memory; the
+  // caller synchronises the block before any warp reads them (finish()).
   __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t* aux, int w,
                        const float* sq) {
     uint4* frag = reinterpret_cast<uint4*>(aux);
@@ -582,130 +590,145 @@ struct QuantWarp {
         rowc[kMaxHeads + r] = ldexpf(kBias, kMulLog2) * qsum;  // K entered as 2^m (kBias + code)
       }
     }
-    nm = CUDART_INF_F;
-    l = 0.f;
-    sp = 0.f;
+    nm2 = make_float2(CUDART_INF_F, CUDART_INF_F);
+    l2 = sp2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < MT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   }
-  __device__ void finish(const uint8_t* aux, int lane) {
-    qs = reinterpret_cast<const uint4*>(aux);
-    const float* rowc = reinterpret_cast<const float*>(aux + KS * 32 * 16);
-    row_scale = rowc[lane >> 2];
-    kbias = rowc[kMaxHeads + (lane >> 2)];
-  }
-
-  // PPI consecutive pages at st + pg * pageBytes; valid[pg] tokens each (a page with
-  // valid 0 was not loaded and its stage memory is stale); the first lo tokens of page 0
-  // are before a sliding window and are not attended.
-  __device__ void pages(const uint8_t* st, const int (&valid)[PPI], int lo, int lane) {
+  // stage0: shared-window address of stage 0 of this warp's ring
+  __device__ void finish(const uint8_t* aux, int lane, uint32_t stage0) {
     using Lo = Layout<KVT, D>;
     const int r = lane >> 2, c = lane & 3;
-    float x[PPI][4];
-    float ksc[PPI][4], vsc[PPI][4];
+    const float* rowc = reinterpret_cast<const float*>(aux + KS * 32 * 16);
+    const float rs = rowc[r];
+    rs2 = make_float2(rs, rs);
+    kbias = rowc[kMaxHeads + r];
+    a_q = smem_u32(aux) + lane * 16;
+    a_sc = stage0 + 2 * Lo::kBytes + c * 16;
+    // K rows of n-tile 0: token 4(r/2) + r%2 (n-tile 1: two tokens further)
+    a_k = stage0 + (4 * (r >> 1) + (r & 1)) * RB + c * (KVT == kINT4 ? 8 : 16);
+    a_v = stage0 + Lo::kBytes + lane * 16;
+  }
+
+  // Tokens of a partly attended page (so: its stage offset) that are not attended get
+  // score -inf and V scale 0; FP8 V codes of those tokens are also set to zero in shared
+  // memory, because a stale E4M3 NaN code would survive a zero probability in the MMA.
+  __device__ void mask_v_codes(uint32_t so, int valid, int lo, int lane) {
+    if constexpr (KVT == kFP8) {
+      using Lo = Layout<KVT, D>;
+      // V block: D rows of 16 token bytes; keep bytes t with lo <= t < valid
+      const uint32_t keep_lo = (valid >= 16 ? 0xffffu : ((1u << valid) - 1u)) & ~((1u << lo) - 1u);
+      uint32_t m[4];
 #pragma unroll
-    for (int pg = 0; pg < PPI; ++pg) {
-      const uint8_t* Ks = st + pg * Lo::pageBytes;
-      const float4 k4 = *reinterpret_cast<const float4*>(Ks + 2 * Lo::kBytes + c * 16);
-      const float4 v4 = *reinterpret_cast<const float4*>(Ks + 2 * Lo::kBytes + Lo::sBytes + c * 16);
-      ksc[pg][0] = k4.x; ksc[pg][1] = k4.y; ksc[pg][2] = k4.z; ksc[pg][3] = k4.w;
-      vsc[pg][0] = v4.x; vsc[pg][1] = v4.y; vsc[pg][2] = v4.z; vsc[pg][3] = v4.w;
-      // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
-      // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3 of head r.
-      // The accumulators of the hi rows start at -kBias sum(q): the code bias cancels
-      // inside the FP32 accumulation.
-      // Each query fragment is read once per page and serves both n-tiles.
-      float sacc[2][4];
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t bits = (keep_lo >> (4 * q)) & 0xfu;
+        m[q] = ((bits & 1u) ? 0xffu : 0u) | ((bits & 2u) ? 0xff00u : 0u) |
+               ((bits & 4u) ? 0xff0000u : 0u) | ((bits & 8u) ? 0xff000000u : 0u);
+      }
+      const uint32_t base = a_v - lane * 16 + so;  // the stage's V block
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        sacc[j][0] = sacc[j][1] = -kbias;
-        sacc[j][2] = sacc[j][3] = 0.f;
+      for (int d = lane; d < D; d += 32) {
+        const uint32_t ad = base + d * 16;
+        uint4 v = lds_u4(ad);
+        v.x &= m[0]; v.y &= m[1]; v.z &= m[2]; v.w &= m[3];
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(ad), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w) : "memory");
+      }
+      __syncwarp();
+      (void)Lo::kBytes;
+    }
+  }
+
+  // Two B operands (k-slot pairs of one k-step) of a 32-bit word of stored K codes.
+  __device__ static void kcvt(uint32_t w, int half, uint32_t& b0, uint32_t& b1) {
+    if constexpr (KVT == kFP8) {
+      e4m3x4_to_f16x4(w, b0, b1);
+    } else if constexpr (KVT == kINT8) {
+      u8x4_to_f16x4_biased(w, b0, b1);
+    } else {  // INT4: nibbles 2 half and 2 half + 1 of the word
+      if (half) {
+        b0 = s4x2_to_f16x2_biased<2>(w);
+        b1 = s4x2_to_f16x2_biased<3>(w);
+      } else {
+        b0 = s4x2_to_f16x2_biased<0>(w);
+        b1 = s4x2_to_f16x2_biased<1>(w);
+      }
+    }
+  }
+
+  // One page at stage offset `so`.  partial: tokens outside [lo, valid) of this page are
+  // not attended (the ragged last page, or the page holding a window's first key).
+  __device__ __forceinline__ void page(uint32_t so, bool partial, int valid, int lo, int lane) {
+    const int c = lane & 3;
+    const float4 k4 = lds_f4(a_sc + so);
+    float4 v4 = lds_f4(a_sc + so + kPage * 4);
+    if constexpr (kMulLog2 != 0) {  // INT4: V operands enter as (kBias + code) / 16
+      v4.x *= 16.f; v4.y *= 16.f; v4.z *= 16.f; v4.w *= 16.f;
+    }
+    // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
+    // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3 of head r.  The
+    // accumulators of the hi rows start at -kbias: the code bias cancels in FP32.
+    float s0[4], s1[4];
+#pragma unroll
+    for (int blk = 0; blk < D / 64; ++blk) {
+      uint32_t kw0[4], kw1[4];
+      if constexpr (KVT == kINT4) {
+        const uint2 u = lds_u2(a_k + so + blk * 32);
+        const uint2 v = lds_u2(a_k + so + 2 * RB + blk * 32);
+        kw0[0] = u.x; kw0[1] = u.y; kw1[0] = v.x; kw1[1] = v.y;
+        kw0[2] = kw0[3] = kw1[2] = kw1[3] = 0u;
+      } else {
+        const uint4 u = lds_u4(a_k + so + blk * 64);
+        const uint4 v = lds_u4(a_k + so + 2 * RB + blk * 64);
+        kw0[0] = u.x; kw0[1] = u.y; kw0[2] = u.z; kw0[3] = u.w;
+        kw1[0] = v.x; kw1[1] = v.y; kw1[2] = v.z; kw1[3] = v.w;
       }
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk) {
-        // this lane's 16 codes of head-dim columns 64 blk + 16 c .. + 15 for the tokens of
-        // n-tiles 0 and 1: 16 bytes (INT8, FP8) or 8 bytes (INT4) each
-        uint32_t kw[2][4];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int tok = 4 * (r >> 1) + (r & 1) + 2 * j;
-          if constexpr (KVT == kINT4) {
-            const uint2 v2 = *reinterpret_cast<const uint2*>(Ks + tok * (D / 2) + blk * 32 + c * 8);
-            kw[j][0] = v2.x; kw[j][1] = v2.y; kw[j][2] = kw[j][3] = 0u;
-          } else {
-            const uint4 v4 = *reinterpret_cast<const uint4*>(Ks + tok * D + blk * 64 + c * 16);
-            kw[j][0] = v4.x; kw[j][1] = v4.y; kw[j][2] = v4.z; kw[j][3] = v4.w;
-          }
-        }
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint4 f = qs[(4 * blk + s) * 32 + lane];
-          const uint32_t a[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            uint32_t b0, b1;
-            if constexpr (KVT == kINT4) {
-              // columns 4s .. 4s+3: nibbles 2 (s % 2) and 2 (s % 2) + 1 of word s / 2
-              const uint32_t w = kw[j][s >> 1];
-              if (s & 1) {
-                b0 = s4x2_to_f16x2_biased<2>(w);
-                b1 = s4x2_to_f16x2_biased<3>(w);
-              } else {
-                b0 = s4x2_to_f16x2_biased<0>(w);
-                b1 = s4x2_to_f16x2_biased<1>(w);
-              }
-            } else if constexpr (KVT == kFP8) {
-              e4m3x4_to_f16x4(kw[j][s], b0, b1);
-            } else {
-              u8x4_to_f16x4_biased(kw[j][s], b0, b1);
-            }
-            mma_f16(sacc[j], a, b0, b1);
-          }
+      for (int s = 0; s < 4; ++s) {
+        const uint4 f = lds_u4(a_q + (4 * blk + s) * 512);
+        const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+        const int wi = KVT == kINT4 ? (s >> 1) : s;
+        uint32_t b0, b1, b2, b3;
+        kcvt(kw0[wi], s & 1, b0, b1);
+        kcvt(kw1[wi], s & 1, b2, b3);
+        if (blk == 0 && s == 0) {
+          mma_f16_c(s0, a, b0, b1, -kbias, -kbias, 0.f, 0.f);
+          mma_f16_c(s1, a, b2, b3, -kbias, -kbias, 0.f, 0.f);
+        } else {
+          mma_f16(s0, a, b0, b1);
+          mma_f16(s1, a, b2, b3);
         }
       }
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          x[pg][2 * j + e] = (sacc[j][e] + sacc[j][2 + e]) * ksc[pg][2 * j + e];
     }
-    bool partial = lo > 0;
-#pragma unroll
-    for (int pg = 0; pg < PPI; ++pg) partial |= valid[pg] < kPage;
-    // (FP8 only: tokens not attended may hold NaN codes, which the zeroed probability
-    // would not cancel in the MMA; their V operands are masked to zero below)
-    uint32_t vmask[PPI][2];
-#pragma unroll
-    for (int pg = 0; pg < PPI; ++pg) vmask[pg][0] = vmask[pg][1] = 0xffffffffu;
-    if (partial) {  // padding may hold NaN scales: mask by select
-#pragma unroll
-      for (int pg = 0; pg < PPI; ++pg)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const bool ok = (4 * c + i) < valid[pg] && (pg > 0 || (4 * c + i) >= lo);
-          x[pg][i] = ok ? x[pg][i] : -CUDART_INF_F;
-          vsc[pg][i] = ok ? vsc[pg][i] : 0.f;
-          if constexpr (KVT == kFP8) {
-            if (!ok) vmask[pg][i >> 1] &= (i & 1) ? 0x0000ffffu : 0xffff0000u;
-          }
-        }
+    // hi + lo rows, times the tokens' K scales: tokens 4c, 4c+1 and 4c+2, 4c+3
+    float2 x01 = __fmul2_rn(__fadd2_rn(make_float2(s0[0], s0[1]), make_float2(s0[2], s0[3])),
+                            make_float2(k4.x, k4.y));
+    float2 x23 = __fmul2_rn(__fadd2_rn(make_float2(s1[0], s1[1]), make_float2(s1[2], s1[3])),
+                            make_float2(k4.z, k4.w));
+    if (partial) {  // (padding may hold NaN scales: mask by select)
+      const int t = 4 * c;
+      const bool o0 = t < valid && t >= lo, o1 = t + 1 < valid && t + 1 >= lo;
+      const bool o2 = t + 2 < valid && t + 2 >= lo, o3 = t + 3 < valid && t + 3 >= lo;
+      x01.x = o0 ? x01.x : -CUDART_INF_F; x01.y = o1 ? x01.y : -CUDART_INF_F;
+      x23.x = o2 ? x23.x : -CUDART_INF_F; x23.y = o3 ? x23.y : -CUDART_INF_F;
+      v4.x = o0 ? v4.x : 0.f; v4.y = o1 ? v4.y : 0.f;
+      v4.z = o2 ? v4.z : 0.f; v4.w = o3 ? v4.w : 0.f;
+      mask_v_codes(so, valid, lo, lane);
     }
-    float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
-#pragma unroll
-    for (int pg = 1; pg < PPI; ++pg)
-      mx = fmaxf(mx, fmaxf(fmaxf(x[pg][0], x[pg][1]), fmaxf(x[pg][2], x[pg][3])));
+    float mx = fmaxf(fmaxf(x01.x, x01.y), fmaxf(x23.x, x23.y));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     // The running max is raised only when a score exceeds it by more than 2^8 in the
     // exponent (probabilities then stay below 256, well inside f16 and FP32), so most
     // pages skip the rescale entirely.
-    const bool need = fmaf(row_scale, mx, nm) > kRescaleLog2;
+    const bool need = fmaf(rs2.x, mx, nm2.x) > kRescaleLog2;
     if (__any_sync(0xffffffffu, need)) {
-      const float nn = need ? -row_scale * mx : nm;
-      const float corr = fast_exp2(nn - nm);  // 0 on the first page (nm = +inf)
-      nm = nn;
-      l *= corr;
-      sp *= corr;
+      const float nn = need ? -rs2.x * mx : nm2.x;
+      const float corr = fast_exp2(nn - nm2.x);  // 0 on the first page (nm = +inf)
+      nm2 = make_float2(nn, nn);
+      const float2 c2 = make_float2(corr, corr);
+      l2 = __fmul2_rn(l2, c2);
+      sp2 = __fmul2_rn(sp2, c2);
       // this lane's accumulators belong to heads 2c and 2c + 1
       const float ca = __shfl_sync(0xffffffffu, corr, 8 * c);
       const float cb = __shfl_sync(0xffffffffu, corr, 8 * c + 4);
@@ -714,76 +737,67 @@ struct QuantWarp {
         o[j][0] *= ca; o[j][1] *= cb; o[j][2] *= ca; o[j][3] *= cb;
       }
     }
-    float pv[PPI][4];
-    float ls = 0.f, ps = 0.f;
+    const float2 e01 = __ffma2_rn(x01, rs2, nm2), e23 = __ffma2_rn(x23, rs2, nm2);
+    const float2 p01 = make_float2(fast_exp2(e01.x), fast_exp2(e01.y));
+    const float2 p23 = make_float2(fast_exp2(e23.x), fast_exp2(e23.y));
+    l2 = __fadd2_rn(l2, __fadd2_rn(p01, p23));
+    const float2 pv01 = __fmul2_rn(p01, make_float2(v4.x, v4.y));
+    const float2 pv23 = __fmul2_rn(p23, make_float2(v4.z, v4.w));
+    sp2 = __fadd2_rn(sp2, __fadd2_rn(pv01, pv23));
+    // B = P^T (tokens x heads): lane (r, c) holds head r, tokens 4c .. 4c+3, which the
+    // k-slot order {2c, 2c+1 | 2c+8, 2c+9} -> tokens {4c, 4c+1 | 4c+2, 4c+3} makes a
+    // ready-made fragment; the hi and lo parts accumulate into the same C.
+    uint32_t bh0, bl0, bh1, bl1;
+    split_h2x(pv01, bh0, bl0);
+    split_h2x(pv23, bh1, bl1);
+    // A = V^T rows 16 j + r and 16 j + r + 8, tokens 4c .. 4c+3 (same k-slot order).
+    // ldmatrix hands lane (r, c) bytes 4c .. 4c+3 of block rows r + 8 i.
+    constexpr int NW = KVT == kINT4 ? MT : 2 * MT;  // words: V rows (pair rows for INT4)
+    uint32_t w[NW];
 #pragma unroll
-    for (int pg = 0; pg < PPI; ++pg)
+    for (int q = 0; q < NW / 4; ++q) {
+      uint32_t f[4];
+      ldsm_x4(f, a_v + so + q * 512);
+      w[4 * q] = f[0]; w[4 * q + 1] = f[1]; w[4 * q + 2] = f[2]; w[4 * q + 3] = f[3];
+    }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float pr = fast_exp2(fmaf(row_scale, x[pg][i], nm));
-        pv[pg][i] = pr * vsc[pg][i];
-        ls += pr;
-        ps += pv[pg][i];
+    for (int j = 0; j < MT; ++j) {
+      uint32_t a[4];
+      if constexpr (KVT == kINT4) {
+        // one word: row pair 8 j + r, tokens 4c .. 4c+3 stored in the order 0, 2, 1, 3;
+        // low nibbles row 16 j + r, high nibbles row 16 j + r + 8
+        a[0] = s4x2_to_f16x2_biased<0>(w[j]);
+        a[1] = s4x2_to_f16x2_biased<1>(w[j]);
+        a[2] = s4x2_to_f16x2_biased<2>(w[j]);
+        a[3] = s4x2_to_f16x2_biased<3>(w[j]);
+      } else if constexpr (KVT == kFP8) {
+        e4m3x4_to_f16x4(w[2 * j], a[0], a[2]);
+        e4m3x4_to_f16x4(w[2 * j + 1], a[1], a[3]);
+      } else {
+        u8x4_to_f16x4_biased(w[2 * j], a[0], a[2]);
+        u8x4_to_f16x4_biased(w[2 * j + 1], a[1], a[3]);
       }
-    l += ls;
-    sp += ps;
-#pragma unroll
-    for (int pg = 0; pg < PPI; ++pg) {
-      // B = P^T (tokens x heads): lane (r, c) holds head r, tokens 4c .. 4c+3, which the
-      // k-slot order {2c, 2c+1 | 2c+8, 2c+9} -> tokens {4c, 4c+1 | 4c+2, 4c+3} makes a
-      // ready-made fragment; the hi and lo parts accumulate into the same C.
-      uint32_t bh[2], bl[2];
-      // (scaled by 2^-kMulLog2, exactly, so that the products carry kBias + code)
-      constexpr float vm = kMulLog2 == 0 ? 1.f : 16.f;
-      static_assert(kMulLog2 == 0 || kMulLog2 == -4, "probability factor");
-      split_h2(pv[pg][0] * vm, pv[pg][1] * vm, bh[0], bl[0]);
-      split_h2(pv[pg][2] * vm, pv[pg][3] * vm, bh[1], bl[1]);
-      // A = V^T rows 16 j + r and 16 j + r + 8, tokens 4c .. 4c+3 (same k-slot order)
-      const uint8_t* Vs = st + pg * Lo::pageBytes + Lo::kBytes;
-#pragma unroll
-      for (int j = 0; j < MT; ++j) {
-        uint32_t a[4];
-        if constexpr (KVT == kINT4) {
-          // one word: row pair 8 j + r, tokens 4c .. 4c+3 stored in the order 0, 2, 1, 3;
-          // low nibbles row 16 j + r, high nibbles row 16 j + r + 8
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + (8 * j + r) * kPage + 4 * c);
-          a[0] = s4x2_to_f16x2_biased<0>(w);
-          a[1] = s4x2_to_f16x2_biased<1>(w);
-          a[2] = s4x2_to_f16x2_biased<2>(w);
-          a[3] = s4x2_to_f16x2_biased<3>(w);
-        } else {
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r) * kPage + 4 * c);
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(Vs + (16 * j + r + 8) * kPage + 4 * c);
-          if constexpr (KVT == kFP8) {
-            e4m3x4_to_f16x4(w0, a[0], a[2]);
-            e4m3x4_to_f16x4(w1, a[1], a[3]);
-            a[0] &= vmask[pg][0]; a[1] &= vmask[pg][0];
-            a[2] &= vmask[pg][1]; a[3] &= vmask[pg][1];
-          } else {
-            u8x4_to_f16x4_biased(w0, a[0], a[2]);
-            u8x4_to_f16x4_biased(w1, a[1], a[3]);
-          }
-        }
-        mma_f16(o[j], a, bh[0], bh[1]);
-        mma_f16(o[j], a, bl[0], bl[1]);
-      }
+      mma_f16(o[j], a, bh0, bh1);
+      mma_f16(o[j], a, bl0, bl1);
     }
   }
 
   __device__ void store(float* cm, float* cl, float* cO, int lane) {
     const int r = lane >> 2, c = lane & 3;
-    float lt = l, st = sp;
+    float lt = l2.x + l2.y, st = sp2.x + sp2.y;
     lt += __shfl_xor_sync(0xffffffffu, lt, 1);
     lt += __shfl_xor_sync(0xffffffffu, lt, 2);
     st += __shfl_xor_sync(0xffffffffu, st, 1);
     st += __shfl_xor_sync(0xffffffffu, st, 2);
     if (c == 0) {
-      cm[r] = -nm;  // the running max in log2 units, as the merge expects
+      cm[r] = -nm2.x;  // the running max in log2 units, as the merge expects
       cl[r] = lt;
     }
-    // V entered the MMA as kBias + code: remove kBias * sum(P) of heads 2c and 2c + 1
-    const float ba = kBias * __shfl_sync(0xffffffffu, st, 8 * c);
-    const float bb = kBias * __shfl_sync(0xffffffffu, st, 8 * c + 4);
+    // V entered the MMA as 2^m (kBias + code) against P s_v 2^-m: remove kBias 2^m
+    // sum(P s_v 2^-m) of heads 2c and 2c + 1
+    constexpr float vb = kBias * (kMulLog2 == 0 ? 1.f : 0.0625f);
+    const float ba = vb * __shfl_sync(0xffffffffu, st, 8 * c);
+    const float bb = vb * __shfl_sync(0xffffffffu, st, 8 * c + 4);
     float* oa = cO + (2 * c) * (D + 2);
     float* ob = oa + (D + 2);
 #pragma unroll
@@ -828,7 +842,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     decode_kernel(const __grid_constant__ DParams p) {
   using Lo = Layout<KVT, D>;
   using Sm = Smem<KVT, D, STEP>;
-  constexpr int S = Lo::S, PPI = Lo::PPI;
+  constexpr int S = Lo::S;
   constexpr int kW = Tune<KVT, D>::W, kThreads = kW * 32;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
@@ -846,12 +860,12 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   // The block-table entries of this warp's first 32 pages do not depend on the context
   // length: read them together with it (validated below), so that the first copies wait
   // for one global round trip instead of two.  The warp's page m is the block's logical
-  // page pb + (w + (m / PPI) kW) PPI + m % PPI.  (With a sliding window the block's
+  // page pb + w + m kW.  (With a sliding window the block's
   // range starts at the window's first page, known once the length is: a second trip.)
   const int win = WIN ? p.window : 0;
   int pb = split * p.chunk;
   const int32_t* bt = p.bt + static_cast<size_t>(b) * p.MB;
-  const int j_off = (w + (lane / PPI) * kW) * PPI + lane % PPI;
+  const int j_off = w + lane * kW;
   int raw_first = win == 0 && pb + j_off < min(p.MB, pb + p.chunk) ? bt[pb + j_off] : -1;
   typename WarpOf<KVT, D>::type st;
   // query loads, in flight with the length and table reads (a fused step with rotation
@@ -914,19 +928,16 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   uint8_t* my_stages = stages + static_cast<size_t>(w) * S * Lo::stageBytes;
   uint64_t* my_bars = bars + w * S;
   float* probs = probs_all + w * kMaxHeads * kPage;
-  // this warp's iterations: page groups w, w + kW, ... of PPI pages each
-  const int ngroups = (pe - pb + PPI - 1) / PPI;
-  const int n_my = ngroups > w ? (ngroups - w + kW - 1) / kW : 0;
+  // this warp's iterations: the block's pages w, w + kW, ...
+  const int n_my = pe - pb > w ? (pe - pb - w + kW - 1) / kW : 0;
 
   // ---- page ids: lane l holds the id of this warp's page m = 32 k + l (batch k) for the
-  // current and the next batch.  -2 marks a page past the block's range.  An id outside
-  // the pool is replaced by page 0 (so every copy stays inside the cache) and flagged:
-  // the block's outputs then become NaN.
+  // current and the next batch; the warp's page m is the block's page pb + w + m kW.  An
+  // id outside the pool is replaced by page 0 (so every copy stays inside the cache) and
+  // flagged: the block's outputs then become NaN.
   int werr = 0;
   auto check_id = [&](int m, int raw) -> int {
-    const int it = m / PPI;
-    const int j = pb + (w + it * kW) * PPI + m % PPI;
-    if (it >= n_my || j >= pe) return -2;
+    if (m >= n_my) return 0;
     if (raw < 0 || raw >= p.num_pages) {
       werr |= 0x1;  // PKV_DEV_BAD_PAGE
       return 0;
@@ -935,32 +946,31 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   };
   auto load_ids = [&](int batch) -> int {
     const int m = 32 * batch + lane;
-    const int it = m / PPI;
-    const int j = pb + (w + it * kW) * PPI + m % PPI;
-    return check_id(m, it < n_my && j < pe ? bt[j] : -1);
+    return check_id(m, m < n_my ? bt[pb + w + m * kW] : -1);
   };
   int ids_cur = check_id(lane, raw_first), ids_nxt = load_ids(1);
 
-  // ---- copy issue: lane l < NK PPI issues one copy (kind l % NK of page l / NK of the
-  // iteration), so a whole stage costs one warp instruction; lane 0 posts the byte count.
-  constexpr int NK = quantised(KVT) ? 4 : 2;  // K, V (and the two scale vectors)
-  const int cq = lane / NK, ck = lane % NK;
-  // this lane's copy: size, and destination inside stage 0 (the source is selected per
-  // issue from the kernel parameters, which costs no registers across the loop)
+  // ---- copy issue: lane l < NK issues one copy of the iteration's page (K block, V
+  // block, and for the coded formats the two scale vectors), so a whole stage costs one
+  // warp instruction; lane 0 posts the byte count.  The lane's source base, page stride
+  // and destination are computed once.
+  constexpr int NK = quantised(KVT) ? 4 : 2;
+  const int ck = lane < NK ? lane : 0;
   const uint32_t c_bytes = ck < 2 ? static_cast<uint32_t>(Lo::kBytes) : static_cast<uint32_t>(Lo::sBytes);
-  const uint32_t c_dst = smem_u32(my_stages) + cq * Lo::pageBytes +
-                         (ck == 0 ? 0 : ck == 1 ? Lo::kBytes : 2 * Lo::kBytes + (ck - 2) * Lo::sBytes);
+  const uint32_t c_dst = smem_u32(my_stages) +
+                         (ck == 0 ? 0u : ck == 1 ? static_cast<uint32_t>(Lo::kBytes)
+                                                 : static_cast<uint32_t>(2 * Lo::kBytes + (ck - 2) * Lo::sBytes));
+  const uint8_t* c_src = (ck == 0 ? p.k : ck == 1 ? p.v
+                          : reinterpret_cast<const uint8_t*>(ck == 2 ? p.ks : p.vs)) +
+                         static_cast<size_t>(g) * c_bytes;
+  const uint32_t c_stride = static_cast<uint32_t>(p.Hkv) * c_bytes;  // from one page to the next
+  const uint32_t bar0 = smem_u32(my_bars);
+  const uint64_t pol = l2_evict_first_policy();  // streamed once: keep L2 for others
   auto issue = [&](int i, int stage) {
-    const uint64_t pol = l2_evict_first_policy();  // streamed once: keep L2 for others
-    const int j0 = pb + (w + i * kW) * PPI;
-    const int cnt = min(PPI, pe - j0);  // pages of this iteration (>= 1)
-    const int pid = __shfl_sync(0xffffffffu, ids_cur, (i * PPI + cq) & 31);
-    const uint32_t bar = smem_u32(&my_bars[stage]);
-    mbar_arrive_expect_tx_if(lane == 0, bar, static_cast<uint32_t>(cnt * Lo::pageBytes));
-    const uint8_t* base = ck == 0 ? p.k : ck == 1 ? p.v
-                        : reinterpret_cast<const uint8_t*>(NK == 4 && ck == 2 ? p.ks : p.vs);
-    const size_t blk = static_cast<size_t>(max(pid, 0) * p.Hkv + g);
-    bulk_g2s_if(lane < NK * PPI && cq < cnt, c_dst + stage * Lo::stageBytes, base + blk * c_bytes,
+    const uint32_t pid = static_cast<uint32_t>(__shfl_sync(0xffffffffu, ids_cur, i & 31));
+    const uint32_t bar = bar0 + 8 * stage;
+    mbar_arrive_expect_tx_if(lane == 0, bar, static_cast<uint32_t>(Lo::pageBytes));
+    bulk_g2s_if(lane < NK, c_dst + stage * Lo::stageBytes, c_src + static_cast<size_t>(pid) * c_stride,
                 c_bytes, bar, pol);
   };
   if (n_my > 0) {
@@ -1135,25 +1145,34 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
 
   st.init(p, b, h0, nh, lane, aux, w, sq);
   if constexpr (quantised(KVT)) __syncthreads();  // warp 0 built the shared query fragments
-  st.finish(aux, lane);
+  st.finish(aux, lane, smem_u32(my_stages));
   __syncwarp();
 
-  // One ring step: wait for stage `stage`, consume its pages, refill it with iteration
+  // Partly attended pages: the ragged last page of the sequence (iteration i_tail of the
+  // warp that holds it) and, under a window, the page of the window's first key (block
+  // 0, warp 0, iteration 0).  Every other page is consumed without masks.
+  const int jl = np - 1 - pb - w;
+  const int i_tail = (L & (kPage - 1)) != 0 && np == pe && jl >= 0 && jl % kW == 0 ? jl / kW : -1;
+  const int i_head = WIN && (lo & (kPage - 1)) != 0 && split == 0 && w == 0 ? 0 : -1;
+
+  // One ring step: wait for stage `stage`, consume its page, refill it with iteration
   // i + S.  For the tensor-core paths the loop below unrolls the ring, so every stage
   // address is a constant.
   auto step = [&](int i, int stage, uint32_t phase) -> bool {
-    const bool ok = mbar_wait(&my_bars[stage], phase);
-    if (!__all_sync(0xffffffffu, ok)) return false;
+#ifdef PKV_TEST_HOOKS
+    if (i == 0 && g_test_fail_first_wait) return false;  // a wait that gives up at once
+#endif
+    if (!mbar_wait_warp(bar0 + 8 * stage, phase)) return false;
     if (i == 0) {
       for (int k = 1; k < min(S, n_my); ++k) issue(k, k);
     }
-    const uint8_t* sp = my_stages + stage * Lo::stageBytes;
-    const int j0 = pb + (w + i * kW) * PPI;
+    uint8_t* sp = my_stages + stage * Lo::stageBytes;
+    const int j0 = pb + w + i * kW;  // the block's page
     if constexpr (STEP) {
       // the fused step: the new token replaces whatever the cache held at its slot
-      if (patch && j0 <= np - 1 && np - 1 < j0 + PPI) {
+      if (patch && j0 == np - 1) {
         constexpr int RB = RowBytes<KVT, D>::value;
-        uint8_t* pg = my_stages + stage * Lo::stageBytes + (np - 1 - j0) * Lo::pageBytes;
+        uint8_t* pg = my_stages + stage * Lo::stageBytes;
         const uint8_t* nk = nrow;
         const uint8_t* nv = nrow + RB + 16;
         if constexpr (KVT == kINT4) {
@@ -1188,45 +1207,51 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
         __syncwarp();
       }
     }
-    // the window's first page (block 0, warp 0, iteration 0) skips the keys before it
-    const int lo_t = WIN && j0 * kPage < lo ? lo - j0 * kPage : 0;
-    if constexpr (KVT == kF32) {
-      const int valid = min(kPage, L - j0 * kPage);
-      constexpr int HM = f32_head_cap<D>();
-      switch (nh) {  // the FP32 path unrolls over the block's head count
-        case 1: st.template page<1>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
-        case 2: st.template page<2>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
-        case 3: st.template page<3>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
-        case 4: st.template page<4>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
-        default: st.template page<HM>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+    const bool partial = i == i_tail || (WIN && i == i_head);
+    if constexpr (quantised(KVT)) {
+      int valid = kPage, lo_t = 0;
+      if (partial) {
+        valid = min(kPage, L - j0 * kPage);
+        lo_t = WIN && j0 * kPage < lo ? lo - j0 * kPage : 0;
       }
-    } else if constexpr (KVT == kBF16) {
-      st.page(sp, min(kPage, L - j0 * kPage), lo_t, lane);
+      st.page(static_cast<uint32_t>(stage * Lo::stageBytes), partial, valid, lo_t, lane);
     } else {
-      int valid[PPI];
-#pragma unroll
-      for (int q = 0; q < PPI; ++q) valid[q] = j0 + q < pe ? min(kPage, L - (j0 + q) * kPage) : 0;
-      st.pages(sp, valid, lo_t, lane);
+      const int valid = min(kPage, L - j0 * kPage);
+      // the window's first page (block 0, warp 0, iteration 0) skips the keys before it
+      const int lo_t = WIN && j0 * kPage < lo ? lo - j0 * kPage : 0;
+      if constexpr (KVT == kF32) {
+        constexpr int HM = f32_head_cap<D>();
+        switch (nh) {  // the FP32 path unrolls over the block's head count
+          case 1: st.template page<1>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+          case 2: st.template page<2>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+          case 3: st.template page<3>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+          case 4: st.template page<4>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+          default: st.template page<HM>(sp, probs, valid, lo_t, p.scale_log2, lane); break;
+        }
+      } else {
+        st.page(sp, valid, lo_t, lane);
+      }
     }
     const int nxt = i + S;
     if (nxt < n_my) {
-      if (((nxt * PPI) & 31) == 0) {
+      if ((nxt & 31) == 0) {
         // the issue index enters a new batch of ids: it becomes the current one
         ids_cur = ids_nxt;
-        ids_nxt = load_ids(((nxt * PPI) >> 5) + 1);
+        ids_nxt = load_ids((nxt >> 5) + 1);
       }
       __syncwarp();
       issue(nxt, stage);
     }
     return true;
   };
-  int i = 0, stage = 0;  // where a timed-out wait stopped
-  uint32_t phase = 0;
+  int i_fail = -1;  // the iteration whose wait gave up
   if constexpr (KVT == kF32) {
     // (the FP32 page code is large: a rolled ring keeps it in the instruction cache)
-    for (; i < n_my; ++i) {
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < n_my; ++i) {
       if (!step(i, stage, phase)) {
-        werr |= 0x10;  // PKV_DEV_TIMEOUT
+        i_fail = i;
         break;
       }
       if (++stage == S) {
@@ -1236,31 +1261,27 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     }
   } else {
     uint32_t ph = 0;
-    bool going = true;
-    for (int base = 0; going && base < n_my; base += S, ph ^= 1u) {
+    for (int base = 0; base < n_my; base += S, ph ^= 1u) {
 #pragma unroll
       for (int k = 0; k < S; ++k) {
         if (base + k >= n_my) break;
         if (!step(base + k, k, ph)) {
-          werr |= 0x10;  // PKV_DEV_TIMEOUT
-          i = base + k;
-          stage = k;
-          phase = ph;
-          going = false;
+          i_fail = base + k;
           break;
         }
       }
+      if (i_fail >= 0) break;
     }
   }
-  if (werr & 0x10) {
-    // Drain (bounded) whatever this warp still has in flight before leaving: iterations
-    // i .. i + S - 1 (only iteration 0 when the very first wait gave up).
-    int s2 = stage;
-    uint32_t ph2 = phase;
-    for (int k = i; k < (i == 0 ? 1 : min(n_my, i + S)); ++k) {
-      if (k > i) (void)mbar_wait(&my_bars[s2], ph2);
-      if (++s2 == S) { s2 = 0; ph2 ^= 1u; }
-    }
+  if (i_fail >= 0) {
+    werr |= 0x10;  // PKV_DEV_TIMEOUT
+    // Drain (bounded) every copy this warp still has in flight before its stage memory is
+    // reused or the block exits: the iteration whose wait gave up and the ones issued
+    // after it (iterations i_fail .. i_fail + S - 1; only iteration 0 when the very first
+    // wait gave up, as the other stages are requested after it).
+    const int last = i_fail == 0 ? 1 : min(n_my, i_fail + S);
+    for (int k = i_fail; k < last; ++k)
+      (void)mbar_wait_warp(bar0 + 8 * (k % S), static_cast<uint32_t>((k / S) & 1));
   }
   werr = __reduce_or_sync(0xffffffffu, werr);
   if (werr && lane == 0) atomicOr(&s_flag, werr);
@@ -1434,7 +1455,6 @@ struct Variant {
   const void* fn;
   int smem;
   int index;
-  int ppi;
   int max_splits;  // the last block's merge keeps (2 splits + 1) x 8 floats in shared memory
   int warps;       // warps per block
 };
@@ -1445,7 +1465,7 @@ constexpr int max_splits_of() {
 }
 
 #define PKV_VARIANT(T, D, ST, WN, I)                                                        \
-  {kernel_ptr<T, D, ST, WN>(), Smem<T, D, ST>::total, I, Tune<T, D>::PPI, max_splits_of<T, D>(), \
+  {kernel_ptr<T, D, ST, WN>(), Smem<T, D, ST>::total, I, max_splits_of<T, D>(), \
    Tune<T, D>::W}
 // index: dtype-and-head-dim slot (0 .. 9), + 10 for the fused decode step, + 20 for the
 // sliding window
@@ -1468,7 +1488,7 @@ Variant variant(int dtype, int D, bool step, bool win) {
     PKV_VARIANTS_OF(false, true, 20, 1000000)
     PKV_VARIANTS_OF(true, true, 30, 1100000)
 #undef PKV_VARIANTS_OF
-    default: return {nullptr, 0, -1, 1, 1, 4};
+    default: return {nullptr, 0, -1, 1, 4};
   }
 }
 #undef PKV_VARIANT
@@ -1537,7 +1557,7 @@ bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int dev
     long long splits = 1;
     if (units > 0 && 4 * units < 3 * slots) {
       splits = (2 * slots + units - 1) / units;
-      const long long by_len = mb / (8 * v.warps * v.ppi);
+      const long long by_len = mb / (8 * v.warps);
       if (splits > by_len) splits = by_len;
       if (splits > 32) splits = 32;
       if (splits < 1) splits = 1;

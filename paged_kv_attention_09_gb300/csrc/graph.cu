@@ -13,6 +13,7 @@
 #include <new>
 
 #include "internal.h"
+#include "nvtx.h"
 #include "pkv.h"
 
 struct pkv_decode_graph {
@@ -141,6 +142,7 @@ int32_t pkv_decode_graph_bucket(const pkv_decode_graph* g, int32_t num_seqs) {
 }
 
 pkv_status pkv_decode_graph_launch(pkv_decode_graph* g, int32_t num_seqs, void* stream) {
+  PKV_RANGE("pkv_decode_graph_launch");
   if (!g) return PKV_ERR_NULL;
   if (num_seqs < 0) return PKV_ERR_SHAPE;
   if (num_seqs == 0) return PKV_OK;

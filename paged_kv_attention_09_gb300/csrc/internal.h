@@ -78,8 +78,6 @@ struct DecodeArgs {
 // step: plan for the fused decode-step kernels (their shared memory is a little larger).
 bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int device,
                  int chunk_override, DecodePlan* plan, bool step = false);
-// The process-wide split override set by pkv_set_decode_chunk_pages (0 = automatic).
-int decode_chunk_override();
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st);
 
 // ---------------------------------------------------------------- prefill

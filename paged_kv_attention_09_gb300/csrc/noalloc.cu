@@ -11,7 +11,9 @@
 
 #include <cuda_runtime.h>
 
+#include "abi.h"
 #include "internal.h"
+#include "nvtx.h"
 #include "pkv.h"
 
 // The scratch every call shares.  Every GPU that loads the library holds these bytes
@@ -40,55 +42,45 @@ pkv_status scratch_address(int device, void** out) {
   return PKV_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-
 }  // namespace
 
-extern "C" pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void* q,
-                                              int32_t q_dtype, int32_t num_seqs,
-                                              int32_t num_q_heads, const int32_t* block_tables,
-                                              int32_t max_blocks_per_seq,
-                                              const int32_t* context_lens, float scale,
-                                              float* out, int32_t* dev_status, void* stream) {
-  if (!cache || !cache->k_cache || !cache->v_cache) return PKV_ERR_NULL;
-  if (cache->kv_dtype < PKV_F32 || cache->kv_dtype > PKV_INT4) return PKV_ERR_DTYPE;
-  if (cache->page_size != 16) return PKV_ERR_PAGE_SIZE;
-  if (cache->num_pages < 1 || cache->num_kv_heads < 1 || cache->window < 0) return PKV_ERR_SHAPE;
-  if (cache->head_dim != 64 && cache->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  const bool coded = pkv::quantised(cache->kv_dtype);
-  if (coded && (!cache->k_scale || !cache->v_scale)) return PKV_ERR_NULL;
-  if (!aligned16(cache->k_cache) || !aligned16(cache->v_cache)) return PKV_ERR_ALIGN;
-  if (coded && (!aligned16(cache->k_scale) || !aligned16(cache->v_scale))) return PKV_ERR_ALIGN;
-  if (num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1) return PKV_ERR_SHAPE;
-  if (num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_SHAPE;
-  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
-  if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_DTYPE;
+extern "C" pkv_status pkv_decode_attn_noalloc_ex(const pkv_cache* cache, const void* q,
+                                                 int32_t q_dtype, int32_t num_seqs,
+                                                 int32_t num_q_heads,
+                                                 const int32_t* block_tables,
+                                                 int32_t max_blocks_per_seq,
+                                                 const int32_t* context_lens, float scale,
+                                                 float* out, const pkv_decode_opts* opts,
+                                                 int32_t* dev_status, void* stream) {
+  PKV_RANGE("pkv_decode_attn_noalloc");
+  // the same checks, in the same order, as pkv_decode_attn
+  pkv_status s = pkv::check_decode_call(cache, q, q_dtype, num_seqs, num_q_heads, block_tables,
+                                        max_blocks_per_seq, context_lens, out, dev_status);
+  if (s != PKV_OK) return s;
+  int split = 0;
+  if (!pkv::split_pages_of(opts, &split)) return PKV_ERR_SHAPE;
   if (num_seqs == 0) return PKV_OK;
-  if (!q || !block_tables || !context_lens || !out) return PKV_ERR_NULL;
-  if (!aligned16(q) || !aligned16(out) || !aligned4(block_tables) || !aligned4(context_lens))
-    return PKV_ERR_ALIGN;
-  if (dev_status && !aligned4(dev_status)) return PKV_ERR_ALIGN;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_DEVICE;
-  const pkv::CacheView view{cache->k_cache,  cache->v_cache,     cache->k_scale,
-                            cache->v_scale,  cache->num_pages,   cache->num_kv_heads,
-                            cache->head_dim, cache->kv_dtype,   cache->window};
+  const pkv::CacheView view = pkv::view(cache);
   pkv::DecodePlan plan{};
-  if (!pkv::plan_decode(view, num_seqs, num_q_heads, max_blocks_per_seq, q_dtype, dev,
-                        pkv::decode_chunk_override(), &plan))
+  if (!pkv::plan_decode(view, num_seqs, num_q_heads, max_blocks_per_seq, q_dtype, dev, split,
+                        &plan))
     return PKV_ERR_DEVICE;
   if (static_cast<long long>(cache->num_kv_heads) * plan.head_groups > 65535)
     return PKV_ERR_UNSUPPORTED;
   if (plan.ws_bytes > sizeof(g_decode_scratch)) return PKV_ERR_WORKSPACE;  // beyond the fixed maximum
 
   void* scratch = nullptr;
-  pkv_status s = scratch_address(dev, &scratch);
+  s = scratch_address(dev, &scratch);
   if (s != PKV_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (plan.n_splits > 1) {
-    // the merge counters lead the scratch and must start at zero
+    // The merge counters lead the scratch and must start at zero.  A caller's workspace
+    // is the caller's to keep zeroed (the kernel leaves its counters at zero), but this
+    // array is shared by calls of every shape, and a call that stopped before its merge
+    // (a failed launch, a wait that gave up) must not leak counts into the next call.
     const size_t counters = static_cast<size_t>(num_seqs) * cache->num_kv_heads * plan.head_groups * 4;
     if (cudaMemsetAsync(scratch, 0, counters, st) != cudaSuccess) return PKV_ERR_LAUNCH;
   }
@@ -106,4 +98,15 @@ extern "C" pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void
   a.ws = scratch;
   a.dev_status = dev_status;
   return pkv::launch_decode(a, plan, st) == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+extern "C" pkv_status pkv_decode_attn_noalloc(const pkv_cache* cache, const void* q,
+                                              int32_t q_dtype, int32_t num_seqs,
+                                              int32_t num_q_heads, const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq,
+                                              const int32_t* context_lens, float scale,
+                                              float* out, int32_t* dev_status, void* stream) {
+  return pkv_decode_attn_noalloc_ex(cache, q, q_dtype, num_seqs, num_q_heads, block_tables,
+                                    max_blocks_per_seq, context_lens, scale, out, nullptr,
+                                    dev_status, stream);
 }

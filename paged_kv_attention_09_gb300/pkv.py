@@ -27,8 +27,9 @@ STATUS = {0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_DTYPE"
           4: "PKV_ERR_PAGE_SIZE", 5: "PKV_ERR_ALIGN", 6: "PKV_ERR_WORKSPACE",
           7: "PKV_ERR_UNSUPPORTED", 8: "PKV_ERR_LAUNCH", 9: "PKV_ERR_DEVICE"}
 EXPORTS = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn", "pkv_decode_step",
+           "pkv_decode_workspace_size_ex", "pkv_decode_attn_ex", "pkv_decode_step_ex",
            "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn",
-           "pkv_decode_attn_noalloc", "pkv_set_decode_chunk_pages", "pkv_status_string",
+           "pkv_decode_attn_noalloc", "pkv_decode_attn_noalloc_ex", "pkv_status_string",
            "pkv_decode_graph_workspace_size", "pkv_decode_graph_create",
            "pkv_decode_graph_launch", "pkv_decode_graph_bucket", "pkv_decode_graph_destroy")
 GRAPH_MAX_BUCKETS = 16
@@ -47,6 +48,10 @@ class pkv_cache(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("window", ctypes.c_int32)]
+
+
+class pkv_decode_opts(ctypes.Structure):
+    _fields_ = [("split_pages", ctypes.c_int32)]
 
 
 class pkv_graph_layer(ctypes.Structure):
@@ -80,20 +85,26 @@ def load(path: str = LIB_PATH):
     P, I32, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     C = ctypes.POINTER(pkv_cache)
     lib.pkv_append.argtypes = [C, P, P, I32, P, I32, P, P]
+    O = ctypes.POINTER(pkv_decode_opts)
     lib.pkv_decode_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
+    lib.pkv_decode_workspace_size_ex.argtypes = [C, I32, I32, I32, O, ctypes.POINTER(SZ)]
     lib.pkv_decode_attn.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, P, SZ, P, P]
+    lib.pkv_decode_attn_ex.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, P, SZ, O, P, P]
     lib.pkv_decode_step.argtypes = [C, P, I32, P, P, I32, P, P, ctypes.c_double, I32, I32, P,
                                     I32, P, F, P, P, SZ, P, P]
+    lib.pkv_decode_step_ex.argtypes = [C, P, I32, P, P, I32, P, P, ctypes.c_double, I32, I32,
+                                       P, I32, P, F, P, P, SZ, O, P, P]
     lib.pkv_prefill_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.pkv_prefill_chunk_attn.argtypes = [C, P, I32, I32, I32, P, I32, P, I32, P, F, P, P, SZ,
                                            P, P]
     for fn in ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn", "pkv_decode_step",
+               "pkv_decode_workspace_size_ex", "pkv_decode_attn_ex", "pkv_decode_step_ex",
                "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn"):
         getattr(lib, fn).restype = ctypes.c_int
     lib.pkv_decode_attn_noalloc.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, P, P]
     lib.pkv_decode_attn_noalloc.restype = ctypes.c_int
-    lib.pkv_set_decode_chunk_pages.argtypes = [I32]
-    lib.pkv_set_decode_chunk_pages.restype = None
+    lib.pkv_decode_attn_noalloc_ex.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, O, P, P]
+    lib.pkv_decode_attn_noalloc_ex.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
     GD = ctypes.POINTER(pkv_decode_graph_desc)
@@ -181,8 +192,9 @@ def pkv_status_string(code: int) -> str:
     return load().pkv_status_string(code).decode()
 
 
-def pkv_set_decode_chunk_pages(pages: int) -> None:
-    load().pkv_set_decode_chunk_pages(int(pages))
+def _opts(split_pages: int):
+    """The options argument of the _ex calls (None: every option at its default)."""
+    return None if not split_pages else ctypes.byref(pkv_decode_opts(int(split_pages)))
 
 
 def pkv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
@@ -195,11 +207,14 @@ def pkv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
 
 
 def pkv_decode_workspace_size(cache: KVCache, num_seqs: int, num_q_heads: int,
-                              max_blocks_per_seq: int) -> int:
+                              max_blocks_per_seq: int, split_pages: int = 0) -> int:
+    """Scratch bytes of the decode calls for this shape; ``split_pages`` as in
+    pkv_decode_opts (0: automatic)."""
     c = cache.struct()
     n = ctypes.c_size_t(0)
-    _check(load().pkv_decode_workspace_size(ctypes.byref(c), num_seqs, num_q_heads,
-                                            max_blocks_per_seq, ctypes.byref(n)),
+    _check(load().pkv_decode_workspace_size_ex(ctypes.byref(c), num_seqs, num_q_heads,
+                                               max_blocks_per_seq, _opts(split_pages),
+                                               ctypes.byref(n)),
            "pkv_decode_workspace_size")
     return int(n.value)
 
@@ -207,31 +222,35 @@ def pkv_decode_workspace_size(cache: KVCache, num_seqs: int, num_q_heads: int,
 def pkv_decode_attn(cache: KVCache, q: torch.Tensor, block_tables: torch.Tensor,
                     context_lens: torch.Tensor, scale: float, out: torch.Tensor,
                     workspace: Optional[torch.Tensor] = None,
-                    dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+                    dev_status: Optional[torch.Tensor] = None, stream=None,
+                    split_pages: int = 0) -> None:
     c = cache.struct()
     B, Hq, _ = q.shape
     wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pkv_decode_attn(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
-                                  _ptr(block_tables), int(block_tables.shape[1]),
-                                  _ptr(context_lens), float(scale), _ptr(out), _ptr(workspace),
-                                  wb, _ptr(dev_status), _stream(stream)), "pkv_decode_attn")
+    _check(load().pkv_decode_attn_ex(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
+                                     _ptr(block_tables), int(block_tables.shape[1]),
+                                     _ptr(context_lens), float(scale), _ptr(out),
+                                     _ptr(workspace), wb, _opts(split_pages), _ptr(dev_status),
+                                     _stream(stream)), "pkv_decode_attn")
 
 
 def pkv_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                     slot_mapping: torch.Tensor, positions: Optional[torch.Tensor],
                     rope_theta: float, block_tables: torch.Tensor, context_lens: torch.Tensor,
                     scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
-                    dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+                    dev_status: Optional[torch.Tensor] = None, stream=None,
+                    split_pages: int = 0) -> None:
     """One fused decode step (rotate, append the new row, attend); see include/pkv.h."""
     c = cache.struct()
     B, Hq, _ = q.shape
     wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pkv_decode_step(ctypes.byref(c), _ptr(q), _CODE[q.dtype], _ptr(k_new),
-                                  _ptr(v_new), _CODE[k_new.dtype], _ptr(slot_mapping),
-                                  _ptr(positions), float(rope_theta), B, Hq, _ptr(block_tables),
-                                  int(block_tables.shape[1]), _ptr(context_lens), float(scale),
-                                  _ptr(out), _ptr(workspace), wb, _ptr(dev_status),
-                                  _stream(stream)), "pkv_decode_step")
+    _check(load().pkv_decode_step_ex(ctypes.byref(c), _ptr(q), _CODE[q.dtype], _ptr(k_new),
+                                     _ptr(v_new), _CODE[k_new.dtype], _ptr(slot_mapping),
+                                     _ptr(positions), float(rope_theta), B, Hq,
+                                     _ptr(block_tables), int(block_tables.shape[1]),
+                                     _ptr(context_lens), float(scale), _ptr(out),
+                                     _ptr(workspace), wb, _opts(split_pages), _ptr(dev_status),
+                                     _stream(stream)), "pkv_decode_step")
 
 
 class GraphLayer:
@@ -315,15 +334,17 @@ class DecodeGraph:
 
 def pkv_decode_attn_noalloc(cache: KVCache, q: torch.Tensor, block_tables: torch.Tensor,
                             context_lens: torch.Tensor, scale: float, out: torch.Tensor,
-                            dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+                            dev_status: Optional[torch.Tensor] = None, stream=None,
+                            split_pages: int = 0) -> None:
     """pkv_decode_attn with its split scratch in the library's fixed device array (for
     callers that cannot allocate); see include/pkv.h for the size limit and sharing."""
     c = cache.struct()
     B, Hq, _ = q.shape
-    _check(load().pkv_decode_attn_noalloc(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
-                                          _ptr(block_tables), int(block_tables.shape[1]),
-                                          _ptr(context_lens), float(scale), _ptr(out),
-                                          _ptr(dev_status), _stream(stream)),
+    _check(load().pkv_decode_attn_noalloc_ex(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
+                                             _ptr(block_tables), int(block_tables.shape[1]),
+                                             _ptr(context_lens), float(scale), _ptr(out),
+                                             _opts(split_pages), _ptr(dev_status),
+                                             _stream(stream)),
            "pkv_decode_attn_noalloc")
 
 

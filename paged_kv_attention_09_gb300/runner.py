@@ -44,11 +44,13 @@ class DeviceWorkload:
     step_rows: torch.Tensor
     batches: list
     dev_status: torch.Tensor
+    split_pages: int = 0  # decode split-K pages per block (0: automatic)
 
 
 def upload(wl: Workload, device="cuda", cache_fill: Optional[float] = None,
-           fill_history: bool = True) -> DeviceWorkload:
-    """Allocate the cache and batch tensors; optionally append the history rows."""
+           fill_history: bool = True, split_pages: int = 0) -> DeviceWorkload:
+    """Allocate the cache and batch tensors; optionally append the history rows.
+    ``split_pages``: the decode calls' split-K pages per block (0: automatic)."""
     cache = pkv.KVCache.allocate(wl.num_pages, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, device)
     if cache_fill is not None:  # sentinel for never-written slots (NaN poisons padding)
         if wl.kv_dtype in pkv.CODED:
@@ -72,14 +74,14 @@ def upload(wl: Workload, device="cuda", cache_fill: Optional[float] = None,
         max_q = int(b.chunk_lens.max()) if b.chunk_lens is not None and len(b.chunk_lens) else 1
         out = torch.empty(q.shape[0], Hq, D, dtype=torch.float32, device=device)
         if b.kind == "decode":
-            nbytes = pkv.pkv_decode_workspace_size(cache, B, Hq, b.max_blocks)
+            nbytes = pkv.pkv_decode_workspace_size(cache, B, Hq, b.max_blocks, split_pages)
         else:
             nbytes = pkv.pkv_prefill_workspace_size(cache, B, Hq, max_q, b.max_blocks)
         batches.append(DeviceBatch(b.kind, q, torch.from_numpy(b.block_tables).to(device),
                                    torch.from_numpy(b.context_lens).to(device), qsl, max_q, out,
                                    pkv.workspace_for(nbytes, device)))
     dw = DeviceWorkload(wl, cache, k_src, v_src, slots, step_rows, batches,
-                        torch.zeros(1, dtype=torch.int32, device=device))
+                        torch.zeros(1, dtype=torch.int32, device=device), split_pages)
     if fill_history:
         hist = torch.from_numpy(wl.history_rows).to(device)
         append_rows(dw, hist)
@@ -97,7 +99,7 @@ def run_batch(dw: DeviceWorkload, i: int, stream=None) -> torch.Tensor:
     b = dw.batches[i]
     if b.kind == "decode":
         pkv.pkv_decode_attn(dw.cache, b.q, b.block_tables, b.context_lens, dw.wl.scale, b.out,
-                            b.workspace, dw.dev_status, stream)
+                            b.workspace, dw.dev_status, stream, split_pages=dw.split_pages)
     else:
         pkv.pkv_prefill_chunk_attn(dw.cache, b.q, b.q_start_loc, b.max_q_len, b.block_tables,
                                    b.context_lens, dw.wl.scale, b.out, b.workspace,
@@ -132,5 +134,6 @@ def run_decode_step(dw: DeviceWorkload, inputs, i: int = 0, rope_theta: float = 
     b = dw.batches[i]
     k, v, slots, pos = inputs
     pkv.pkv_decode_step(dw.cache, b.q, k, v, slots, pos, rope_theta, b.block_tables,
-                        b.context_lens, dw.wl.scale, b.out, b.workspace, dw.dev_status, stream)
+                        b.context_lens, dw.wl.scale, b.out, b.workspace, dw.dev_status, stream,
+                        split_pages=dw.split_pages)
     return b.out

@@ -23,15 +23,13 @@ def oracle_outputs(wl, oc=None, seqs=None):
 
 
 def gpu_outputs(wl, cache_fill=None, chunk_pages=0):
-    pkv.pkv_set_decode_chunk_pages(chunk_pages)
-    try:
-        dw = runner.upload(wl, "cuda", cache_fill=cache_fill)
-        outs = runner.run_step(dw)
-        torch.cuda.synchronize()
-        status = int(dw.dev_status.item())
-        return [o.cpu().numpy().astype(np.float64) for o in outs], status, dw
-    finally:
-        pkv.pkv_set_decode_chunk_pages(0)
+    """One step of the workload through the library (chunk_pages: the decode calls'
+    split-K pages per block, 0 = automatic); outputs, device status, device workload."""
+    dw = runner.upload(wl, "cuda", cache_fill=cache_fill, split_pages=chunk_pages)
+    outs = runner.run_step(dw)
+    torch.cuda.synchronize()
+    status = int(dw.dev_status.item())
+    return [o.cpu().numpy().astype(np.float64) for o in outs], status, dw
 
 
 def max_err(a, b, rows=None):

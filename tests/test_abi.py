@@ -139,3 +139,40 @@ def test_graph_descriptor_validation(lib):
     assert lib.pkv_decode_graph_launch(None, 1, None) == 1
     assert lib.pkv_decode_graph_bucket(None, 3) == 0
     lib.pkv_decode_graph_destroy(None)  # a no-op
+
+
+def test_decode_entry_points_validate_alike(lib):
+    """pkv_decode_attn, its _ex form and the no-allocation entry point reject the same
+    arguments with the same codes before touching CUDA: among them a block table or a
+    page pool too large for 32-bit token positions."""
+    P = None
+    ok = dict(num_pages=8)
+
+    def calls(c, mb=4, hq=4, q=0x80000, qd=pkv.F32, out=0xB0000, opts=None):
+        o = ctypes.byref(opts) if opts is not None else None
+        return [
+            lib.pkv_decode_attn(ctypes.byref(c), q, qd, 2, hq, 0x90000, mb, 0xA0000, 0.1, out,
+                                P, 0, P, P),
+            lib.pkv_decode_attn_ex(ctypes.byref(c), q, qd, 2, hq, 0x90000, mb, 0xA0000, 0.1, out,
+                                   P, 0, o, P, P),
+            lib.pkv_decode_attn_noalloc(ctypes.byref(c), q, qd, 2, hq, 0x90000, mb, 0xA0000, 0.1,
+                                        out, P, P),
+            lib.pkv_decode_attn_noalloc_ex(ctypes.byref(c), q, qd, 2, hq, 0x90000, mb, 0xA0000,
+                                           0.1, out, o, P, P),
+        ]
+    huge_mb = 0x7fffffff // 16 + 1                            # mb * 16 overflows int32
+    assert calls(_cache(**ok), mb=huge_mb) == [2, 2, 2, 2]
+    assert calls(_cache(num_pages=0x7fffffff // 16 + 1)) == [2, 2, 2, 2]
+    assert calls(_cache(**ok), hq=3) == [2, 2, 2, 2]             # Hq % Hkv
+    assert calls(_cache(**ok), qd=pkv.INT8) == [3, 3, 3, 3]      # q dtype
+    assert calls(_cache(**ok), out=0xB0004) == [5, 5, 5, 5]      # alignment
+    assert calls(_cache(**ok), q=None) == [1, 1, 1, 1]
+    assert calls(_cache(kv_dtype=pkv.INT8, k_scale=None)) == [1, 1, 1, 1]
+    # a negative split is invalid; the forms without options cannot pass one
+    assert calls(_cache(**ok), opts=pkv.pkv_decode_opts(-1))[1::2] == [2, 2]
+    n = ctypes.c_size_t(0)
+    assert lib.pkv_decode_workspace_size(ctypes.byref(_cache()), 2, 4, huge_mb,
+                                         ctypes.byref(n)) == 2
+    assert lib.pkv_decode_workspace_size_ex(ctypes.byref(_cache()), 2, 4, 4,
+                                            ctypes.byref(pkv.pkv_decode_opts(-3)),
+                                            ctypes.byref(n)) == 2

@@ -118,22 +118,18 @@ def test_bad_page_and_bad_length_give_nan_rows_and_status():
 def test_workspace_is_left_zero_for_the_next_call():
     wl = W.small_workload(98, num_q_heads=8, num_kv_heads=2, head_dim=64, kv_dtype=W.INT8,
                           q_dtype=W.F32, decode_lens=[200, 200])
-    pkv.pkv_set_decode_chunk_pages(2)
-    try:
-        dw = runner.upload(wl)
-        ws = dw.batches[0].workspace
-        assert ws is not None
-        first = None
-        for _ in range(3):
-            runner.run_batch(dw, 0)
-            torch.cuda.synchronize()
-            o = dw.batches[0].out.cpu().numpy()
-            first = o if first is None else first
-            assert np.array_equal(o, first)
-        tickets = ws[: 2 * 2].cpu().numpy()  # B * Hkv tickets lead the workspace
-        assert not tickets.any()
-    finally:
-        pkv.pkv_set_decode_chunk_pages(0)
+    dw = runner.upload(wl, split_pages=2)
+    ws = dw.batches[0].workspace
+    assert ws is not None
+    first = None
+    for _ in range(3):
+        runner.run_batch(dw, 0)
+        torch.cuda.synchronize()
+        o = dw.batches[0].out.cpu().numpy()
+        first = o if first is None else first
+        assert np.array_equal(o, first)
+    tickets = ws[: 2 * 2].cpu().numpy()  # B * Hkv tickets lead the workspace
+    assert not tickets.any()
 
 
 # Full-size workloads in the benchmark's launch configuration (automatic split); the

@@ -39,14 +39,11 @@ def test_decode_with_shared_prefix_pages(kv):
     db = dw.batches[0]
     db.block_tables.copy_(torch.from_numpy(bt))
     for chunk in (0, 2):  # automatic split, and a forced split so shared pages cross blocks
-        pkv.pkv_set_decode_chunk_pages(chunk)
-        try:
-            db.workspace = pkv.workspace_for(pkv.pkv_decode_workspace_size(
-                dw.cache, b.num_seqs, wl.num_q_heads, b.max_blocks), "cuda")
-            runner.run_batch(dw, 0)
-            torch.cuda.synchronize()
-        finally:
-            pkv.pkv_set_decode_chunk_pages(0)
+        dw.split_pages = chunk
+        db.workspace = pkv.workspace_for(pkv.pkv_decode_workspace_size(
+            dw.cache, b.num_seqs, wl.num_q_heads, b.max_blocks, chunk), "cuda")
+        runner.run_batch(dw, 0)
+        torch.cuda.synchronize()
         assert int(dw.dev_status.item()) == 0
         got = db.out.cpu().numpy().astype(np.float64)
         assert max_err(got, ref) <= TOL[kv]

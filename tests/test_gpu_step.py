@@ -30,14 +30,10 @@ def step_case(seed, kv, qd, nd, Hq, Hkv, D, lens, rope=True, chunk=0, slot_edit=
     oc = oracle.cache_from_workload(wl, rows=wl.history_rows)
     ref = oracle.decode_step(oc, b.q, qd, k_new, v_new, nd, slots, pos, THETA, b.block_tables,
                              b.context_lens, wl.scale)
-    pkv.pkv_set_decode_chunk_pages(chunk)
-    try:
-        dw = runner.upload(wl, "cuda")
-        k, v, _, p = runner.decode_step_inputs(dw, 0, rope)
-        runner.run_decode_step(dw, (k, v, torch.from_numpy(slots).cuda(), p), 0, THETA)
-        torch.cuda.synchronize()
-    finally:
-        pkv.pkv_set_decode_chunk_pages(0)
+    dw = runner.upload(wl, "cuda", split_pages=chunk)
+    k, v, _, p = runner.decode_step_inputs(dw, 0, rope)
+    runner.run_decode_step(dw, (k, v, torch.from_numpy(slots).cuda(), p), 0, THETA)
+    torch.cuda.synchronize()
     got = dw.batches[0].out.cpu().numpy().astype(np.float64)
     return wl, ref, got, int(dw.dev_status.item()), dw, oc
 

@@ -27,21 +27,17 @@ def decode_gpu(wl, window, bt=None, chunk=0, poison_rows=None):
         nan = np.uint16(0x7FC0) if wl.new_dtype == W.BF16 else np.float32("nan")
         wl.k_src[poison_rows] = nan
         wl.v_src[poison_rows] = nan
-    pkv.pkv_set_decode_chunk_pages(chunk)
-    try:
-        dw = runner.upload(wl, "cuda", fill_history=False)
-        dw.cache.window = window
-        runner.append_rows(dw, torch.arange(wl.slots.shape[0], device="cuda"))
-        b = dw.batches[0]
-        if bt is not None:
-            b.block_tables.copy_(torch.from_numpy(bt))
-        ws = pkv.pkv_decode_workspace_size(dw.cache, b.q.shape[0], wl.num_q_heads,
-                                           wl.batches[0].max_blocks)
-        b.workspace = pkv.workspace_for(ws, "cuda")
-        runner.run_batch(dw, 0)
-        torch.cuda.synchronize()
-    finally:
-        pkv.pkv_set_decode_chunk_pages(0)
+    dw = runner.upload(wl, "cuda", fill_history=False, split_pages=chunk)
+    dw.cache.window = window
+    runner.append_rows(dw, torch.arange(wl.slots.shape[0], device="cuda"))
+    b = dw.batches[0]
+    if bt is not None:
+        b.block_tables.copy_(torch.from_numpy(bt))
+    ws = pkv.pkv_decode_workspace_size(dw.cache, b.q.shape[0], wl.num_q_heads,
+                                       wl.batches[0].max_blocks, chunk)
+    b.workspace = pkv.workspace_for(ws, "cuda")
+    runner.run_batch(dw, 0)
+    torch.cuda.synchronize()
     return b.out.cpu().numpy().astype(np.float64), int(dw.dev_status.item()), dw
 
 
@@ -155,15 +151,11 @@ def test_window_fused_step(kv, nd, window):
     ref = oracle.decode_step(oc, b.q, W.F32, wl.k_src[rows], wl.v_src[rows], nd, slots, pos,
                              1.0e4, b.block_tables, b.context_lens, wl.scale, window=window)
     for chunk in (0, 3):
-        pkv.pkv_set_decode_chunk_pages(chunk)
-        try:
-            dw = runner.upload(wl, "cuda")
-            dw.cache.window = window
-            inp = runner.decode_step_inputs(dw, 0, True)
-            runner.run_decode_step(dw, inp, 0, 1.0e4)
-            torch.cuda.synchronize()
-        finally:
-            pkv.pkv_set_decode_chunk_pages(0)
+        dw = runner.upload(wl, "cuda", split_pages=chunk)
+        dw.cache.window = window
+        inp = runner.decode_step_inputs(dw, 0, True)
+        runner.run_decode_step(dw, inp, 0, 1.0e4)
+        torch.cuda.synchronize()
         assert int(dw.dev_status.item()) == 0
         got = dw.batches[0].out.cpu().numpy().astype(np.float64)
         assert max_err(got, ref) <= TOL[kv]
