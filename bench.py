@@ -63,6 +63,13 @@ def parse():
     ap.add_argument("--graphs", action="store_true",
                     help="end-to-end leg: the step's launches through the bucketed "
                          "CUDA-graph executor (decode-only workloads)")
+    ap.add_argument("--workloads", default="all",
+                    help="comma-separated workloads whose kernels the line reports one by "
+                         "one ('all': the five configurations and the FP8 / INT4 caches; "
+                         "'none')")
+    ap.add_argument("--compare", default=None,
+                    help="an earlier line of this benchmark (or a file holding one): report "
+                         "every kernel's change and the ones more than 10%% slower")
     return ap.parse_args()
 
 
@@ -323,197 +330,352 @@ def cpu_oracle_rate(wl, seconds, threads, fused=True, rope=False, oc=None, count
 
 # ----------------------------------------------------------------------------- GPU run
 
+# Workloads whose kernels the line reports one by one: the five configurations of the
+# benchmark (tiny, SmolLM2, Qwen2.5, TinyLlama INT8, mixed) and the FP8 / INT4 caches at
+# the TinyLlama shapes.
+ALL_WORKLOADS = ("tiny", "smollm2-f32", "qwen-bf16", "tinyllama-int8", "mixed",
+                 "tinyllama-fp8", "tinyllama-int4")
+KERNEL_LAUNCHES = 50      # launches per captured graph of one kernel
+KERNEL_REPLAYS = 5        # at least this many timed replays of that graph ...
+KERNEL_MIN_MS = 200.0     # ... and at least this much timed GPU time, for the clock record
+
+
+def kernel_graph_ms(capture_fn, replay_fn, n_launch):
+    """Time one kernel: a CUDA graph of ``n_launch`` launches (over rotating replicas),
+    replayed at least KERNEL_REPLAYS times and until KERNEL_MIN_MS of timed region have
+    passed; the median replay over ``n_launch`` is the time per launch.  Returns (ms per
+    launch, replays)."""
+    g = capture_fn(n_launch)
+    replay_fn(g)  # warm
+    times = []
+    while len(times) < KERNEL_REPLAYS or (sum(times) < KERNEL_MIN_MS and len(times) < 20000):
+        times.append(replay_fn(g))
+    return statistics.median(times) / n_launch, len(times)
+
+
+class Prepared:
+    """A workload on the device: R replicas of every input (R x the step's bytes > 4x L2),
+    each with `layers` caches, and the step's new rows."""
+
+    def __init__(self, wl, dev, layers=1, replicas=0, fused=False, rope=False):
+        import torch
+
+        from paged_kv_attention_09_gb300 import runner
+        self.wl, self.dev, self.NL = wl, dev, max(1, layers)
+        self.acc = step_accounting(wl)  # per layer
+        ws_bytes = self.acc["total"] * self.NL
+        self.R = replicas or max(2, math.ceil(4 * L2_BYTES / max(ws_bytes, 1)))
+        base = runner.upload(wl, f"cuda:{dev}")
+        self.base = base
+        self.fused = fused and wl.batches[0].kind == "decode"
+        rows = base.step_rows
+        self.dec_in = None
+        if self.fused:  # the decode batch's new rows go through pkv_decode_step
+            self.dec_in = runner.decode_step_inputs(base, 0, rope=rope)
+            rows = rows[wl.batches[0].num_seqs:]
+        self.step_k, self.step_v, self.step_s = (base.k_src[rows].contiguous(),
+                                                 base.v_src[rows].contiguous(),
+                                                 base.slots[rows].contiguous())
+        self.n_append = int(self.step_s.numel())
+        reps = [base]
+        for _ in range(self.R - 1):
+            batches = [runner.DeviceBatch(b.kind, b.q.clone(), b.block_tables.clone(),
+                                          b.context_lens.clone(),
+                                          None if b.q_start_loc is None else b.q_start_loc.clone(),
+                                          b.max_q_len, torch.empty_like(b.out),
+                                          None if b.workspace is None else torch.zeros_like(b.workspace))
+                       for b in base.batches]
+            reps.append(runner.DeviceWorkload(wl, base.cache.clone(), base.k_src, base.v_src,
+                                              base.slots, base.step_rows, batches,
+                                              base.dev_status))
+        self.reps = reps
+        # every replica's layers: the replica itself, then copies of its cache that share
+        # its tables, lengths, queries and outputs
+        self.layered = [[dw] + [runner.DeviceWorkload(wl, dw.cache.clone(), dw.k_src, dw.v_src,
+                                                      dw.slots, dw.step_rows, dw.batches,
+                                                      dw.dev_status)
+                                for _ in range(self.NL - 1)] for dw in reps]
+        self.stream = torch.cuda.Stream(device=f"cuda:{dev}")
+        self.stream.wait_stream(torch.cuda.current_stream())
+        self.names = (["append"] if self.n_append else []) + [b.kind for b in wl.batches]
+
+    def run_j(self, dw, j, rope_theta=ROPE_THETA):
+        from paged_kv_attention_09_gb300 import runner
+        if self.fused and j == 0:
+            runner.run_decode_step(dw, self.dec_in, 0, rope_theta, self.stream)
+        else:
+            runner.run_batch(dw, j, self.stream)
+
+    def append_only(self, i):
+        from paged_kv_attention_09_gb300 import pkv
+        for dw in self.layered[i % self.R]:
+            pkv.pkv_append(dw.cache, self.step_k, self.step_v, self.step_s, dw.dev_status,
+                           self.stream)
+
+    def batch_only(self, j):
+        def run(i):
+            for dw in self.layered[i % self.R]:
+                self.run_j(dw, j)
+        return run
+
+    def step(self, i):
+        from paged_kv_attention_09_gb300 import pkv
+        for dw in self.layered[i % self.R]:
+            if self.n_append:
+                pkv.pkv_append(dw.cache, self.step_k, self.step_v, self.step_s, dw.dev_status,
+                               self.stream)
+            for j in range(len(self.wl.batches)):
+                self.run_j(dw, j)
+
+    def kernel_fns(self):
+        """(name, launch function) of every kernel of the step, in order."""
+        return ([("append", self.append_only)] if self.n_append else []) + \
+            [(b.kind, self.batch_only(j)) for j, b in enumerate(self.wl.batches)]
+
+    def capture(self, fn, k, first=0):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(k):
+                fn(first + i)
+        return g
+
+    def replay_ms(self, g):
+        # replay() launches on the current stream: make it the stream the events use
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            g.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def kernel_times(self):
+        """Per-kernel time (ms per launch per layer) and replays, by kernel name."""
+        out = {}
+        for name, fn in self.kernel_fns():
+            ms, reps = kernel_graph_ms(lambda n, fn=fn: self.capture(fn, n), self.replay_ms,
+                                       KERNEL_LAUNCHES)
+            out[name] = {"ms": ms / self.NL, "replays": reps, "launches_per_graph": KERNEL_LAUNCHES}
+        return out
+
+    def status(self):
+        return int(self.base.dev_status.item())
+
+
+def workload_entry(wl, acc, kt, peak, bf16):
+    """The line's record of one workload's kernels: time per launch, and for the decode
+    kernel its achieved GB/s against the measured copy peak and 8 TB/s, KV tokens/s and
+    decode steps/s; for the prefill kernel TFLOP/s against the measured BF16 peaks."""
+    burst, sustained, _ = bf16
+    e = {}
+    for name, t in kt.items():
+        us = t["ms"] * 1e3
+        rec = {"us": round(us, 3), "replays": t["replays"],
+               "launches_per_graph": t["launches_per_graph"]}
+        if name == "decode":
+            gbs = acc["decode"] / (us * 1e-6) / 1e9
+            rec.update({"GBs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+                        "frac_of_8tbs": round(gbs / 8000.0, 4),
+                        "kv_tokens_per_s": round(acc["kv_tokens"] / (us * 1e-6), 1),
+                        "decode_steps_per_s": round(acc["seqs"] / (us * 1e-6), 1),
+                        "bytes_per_launch": acc["decode"]})
+        elif name == "prefill":
+            tf = acc["prefill_flops"] / (us * 1e-6) / 1e12
+            rec.update({"TFLOPs": round(tf, 1), "frac_of_bf16_burst": round(tf / burst, 4),
+                        "frac_of_bf16_sustained": round(tf / sustained, 4),
+                        "flops_per_launch": acc["prefill_flops"]})
+        elif name == "append":
+            rec["GBs"] = round(acc["append"] / (us * 1e-6) / 1e9, 1)
+        e[name] = rec
+    return e
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
 
-    from paged_kv_attention_09_gb300 import pkv, runner
+    from paged_kv_attention_09_gb300 import pkv
     from paged_kv_attention_09_gb300 import workloads as W
 
     dev = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(dev)
     pkv.load()
+    peak, _ = measured_hbm()
+    bf16 = measured_bf16()
     wl = W.workload(args.workload)
-    acc = step_accounting(wl)  # per layer
-    NL = max(1, args.layers)
-    ws_bytes = acc["total"] * NL
-    R = args.replicas or max(2, math.ceil(4 * L2_BYTES / max(ws_bytes, 1)))
-    base = runner.upload(wl, f"cuda:{dev}")
-    fused = args.fused and wl.batches[0].kind == "decode"
-    rows = base.step_rows
-    dec_in = None
-    if fused:  # the decode batch's new rows go through pkv_decode_step
-        dec_in = runner.decode_step_inputs(base, 0, rope=args.rope)
-        rows = rows[wl.batches[0].num_seqs:]
-    step_k, step_v, step_s = (base.k_src[rows].contiguous(), base.v_src[rows].contiguous(),
-                              base.slots[rows].contiguous())
-    n_append = int(step_s.numel())
-    reps = [base]
-    for _ in range(R - 1):
-        c = base.cache
-        cache = c.clone()
-        batches = [runner.DeviceBatch(b.kind, b.q.clone(), b.block_tables.clone(),
-                                      b.context_lens.clone(),
-                                      None if b.q_start_loc is None else b.q_start_loc.clone(),
-                                      b.max_q_len, torch.empty_like(b.out),
-                                      None if b.workspace is None else torch.zeros_like(b.workspace))
-                   for b in base.batches]
-        reps.append(runner.DeviceWorkload(wl, cache, base.k_src, base.v_src, base.slots,
-                                          base.step_rows, batches, base.dev_status))
-    # every replica's layers: the replica itself, then copies of its cache that share its
-    # tables, lengths, queries and outputs
-    layered = [[dw] + [runner.DeviceWorkload(wl, dw.cache.clone(), dw.k_src, dw.v_src, dw.slots,
-                                             dw.step_rows, dw.batches, dw.dev_status)
-                       for _ in range(NL - 1)] for dw in reps]
-    stream = torch.cuda.Stream(device=f"cuda:{dev}")
-    stream.wait_stream(torch.cuda.current_stream())
-    n_batches = len(wl.batches)
+    pr = Prepared(wl, dev, layers=args.layers, replicas=args.replicas, fused=args.fused,
+                  rope=args.rope)
+    acc, R, NL, K = pr.acc, pr.R, pr.NL, args.steps
 
-    def append_only(i):
-        if n_append:
-            for dw in layered[i % R]:
-                pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
-
-    def run_j(dw, j):
-        if fused and j == 0:
-            runner.run_decode_step(dw, dec_in, 0, ROPE_THETA, stream)
-        else:
-            runner.run_batch(dw, j, stream)
-
-    def batch_only(j):
-        def run(i):
-            for dw in layered[i % R]:
-                run_j(dw, j)
-        return run
-
-    def step(i):
-        for dw in layered[i % R]:
-            if n_append:
-                pkv.pkv_append(dw.cache, step_k, step_v, step_s, dw.dev_status, stream)
-            for j in range(n_batches):
-                run_j(dw, j)
-
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(pr.stream):
         for i in range(args.warmup):
-            step(i)
+            pr.step(i)
     torch.cuda.synchronize()
-    status = int(base.dev_status.item())
-    if status != 0:
-        raise RuntimeError(f"device status {status} after warm-up")
-
-    K = args.steps
-
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(K):
-                fn(args.warmup + i)
-        return g
-
-    def replay_ms(g):
-        # replay() launches on the current stream: make it the stream the events use
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
+    if pr.status() != 0:
+        raise RuntimeError(f"device status {pr.status()} after warm-up")
 
     # The K timed steps are one CUDA graph (launch overhead out of the timed region);
-    # every kernel in it is ours.  Per-kernel averages come from graphs of that kernel
-    # alone over the same rotating replicas.
-    g_step = capture(step)
-    g_kern = ([capture(append_only)] if n_append else []) + \
-        [capture(batch_only(j)) for j in range(n_batches)]
-    with torch.cuda.stream(stream):
+    # every kernel in it is ours.
+    g_step = pr.capture(pr.step, K, args.warmup)
+    with torch.cuda.stream(pr.stream):
         g_step.replay()
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    wl_list = [] if args.workloads == "none" else \
+        (list(ALL_WORKLOADS) if args.workloads == "all" else args.workloads.split(","))
+    tables = {}
     with ClockSampler(dev) as clk:
-        total_ms = replay_ms(g_step)
-    if world > 1:
-        dist.barrier()
-    kern_ms = [[replay_ms(g) / (K * NL)] for g in g_kern]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        total_ms = pr.replay_ms(g_step)
+        if world > 1:
+            dist.barrier()
+        del g_step
+        # per-kernel times: the benchmarked workload (its layers and step form), then every
+        # other workload of the table, one at a time on the device
+        kern = pr.kernel_times()
+        tables[wl.name] = workload_entry(wl, acc, kern, peak, bf16)
+        for name in wl_list:
+            if name == wl.name:
+                continue
+            other = Prepared(W.workload(name), dev)
+            with torch.cuda.stream(other.stream):
+                for i in range(3):
+                    other.step(i)
+            torch.cuda.synchronize()
+            if other.status() != 0:
+                raise RuntimeError(f"device status {other.status()} on {name}")
+            tables[name] = workload_entry(other.wl, other.acc, other.kernel_times(), peak, bf16)
+            del other
+            torch.cuda.empty_cache()
     if world > 1:
         total_ms = max_over_ranks(total_ms, f"cuda:{dev}")
     ms = total_ms / K
-    del g_step, g_kern
 
     # ---- end to end through the C ABI with host buffers: H2D of the step's inputs
     # (q, new K/V, slots, tables, lengths) from pinned memory, the calls, D2H of outputs
     e2e = None
     if not args.no_e2e:
-        step_dev = [step_k, step_v, step_s] + ([t for t in dec_in if t is not None] if fused else [])
-        host_in = [t.cpu().pin_memory() for t in step_dev]
-        for b in base.batches:
-            host_in += [b.q.cpu().pin_memory(), b.block_tables.cpu().pin_memory(),
-                        b.context_lens.cpu().pin_memory()]
+        e2e = run_e2e(args, pr, world, dev, acc, K)
+    if pr.status() != 0:
+        raise RuntimeError(f"device status {pr.status()} after the timed steps")
+    return {"wl": wl, "acc": acc, "R": R, "ms": ms, "kern": kern, "clocks": clk.summary(),
+            "e2e": e2e, "fused": pr.fused, "n_append": pr.n_append, "workloads": tables}
+
+
+def run_e2e(args, pr, world, dev, acc, K):
+    """The same step through the public API with host buffers: every step copies its
+    inputs from pinned host memory and its outputs back, inside the timed region."""
+    import torch
+
+    from paged_kv_attention_09_gb300 import pkv
+    wl, NL, R, stream = pr.wl, pr.NL, pr.R, pr.stream
+    step_dev = [pr.step_k, pr.step_v, pr.step_s] + \
+        ([t for t in pr.dec_in if t is not None] if pr.fused else [])
+    host_in = [t.cpu().pin_memory() for t in step_dev]
+    for b in pr.base.batches:
+        host_in += [b.q.cpu().pin_memory(), b.block_tables.cpu().pin_memory(),
+                    b.context_lens.cpu().pin_memory()]
+        if b.q_start_loc is not None:
+            host_in.append(b.q_start_loc.cpu().pin_memory())
+    host_out = [b.out.cpu().pin_memory() for b in pr.base.batches]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    graphs = None
+    if args.graphs:
+        if len(wl.batches) != 1 or wl.batches[0].kind != "decode":
+            raise SystemExit("--graphs: decode-only workloads")
+        gk, gv, gs, gp = pr.dec_in if pr.fused else (pr.step_k, pr.step_v, pr.step_s, None)
+        graphs = []
+        for dws in pr.layered:
+            b = dws[0].batches[0]
+            graphs.append(pkv.DecodeGraph(
+                [pkv.GraphLayer(dw.cache, b.q, b.out, gk, gv) for dw in dws], b.block_tables,
+                b.context_lens, wl.scale, [b.q.shape[0]], slot_mapping=gs, fused=pr.fused,
+                positions=gp, rope_theta=ROPE_THETA, dev_status=dws[0].dev_status))
+
+    def e2e_step(i):
+        dw = pr.reps[i % R]
+        dev_in = list(step_dev)
+        for b in dw.batches:
+            dev_in += [b.q, b.block_tables, b.context_lens]
             if b.q_start_loc is not None:
-                host_in.append(b.q_start_loc.cpu().pin_memory())
-        host_out = [b.out.cpu().pin_memory() for b in base.batches]
-        h2d = sum(t.numel() * t.element_size() for t in host_in)
-        d2h = sum(t.numel() * t.element_size() for t in host_out)
-        graphs = None
-        if args.graphs:
-            if n_batches != 1 or wl.batches[0].kind != "decode":
-                raise SystemExit("--graphs: decode-only workloads")
-            gk, gv, gs, gp = dec_in if fused else (step_k, step_v, step_s, None)
-            graphs = []
-            for dws in layered:
-                b = dws[0].batches[0]
-                graphs.append(pkv.DecodeGraph(
-                    [pkv.GraphLayer(dw.cache, b.q, b.out, gk, gv) for dw in dws], b.block_tables,
-                    b.context_lens, wl.scale, [b.q.shape[0]], slot_mapping=gs, fused=fused,
-                    positions=gp, rope_theta=ROPE_THETA, dev_status=dws[0].dev_status))
-
-        def e2e_step(i):
-            dw = reps[i % R]
-            dev_in = list(step_dev)
-            for b in dw.batches:
-                dev_in += [b.q, b.block_tables, b.context_lens]
-                if b.q_start_loc is not None:
-                    dev_in.append(b.q_start_loc)
-            for d, h in zip(dev_in, host_in):
-                d.copy_(h, non_blocking=True)  # on `stream` (the current stream here)
-            if graphs is not None:
-                graphs[i % R].launch(dw.batches[0].q.shape[0], stream)
-            else:
-                for dwl in layered[i % R]:
-                    if n_append:
-                        pkv.pkv_append(dwl.cache, step_k, step_v, step_s, dwl.dev_status, stream)
-                    for j in range(n_batches):
-                        run_j(dwl, j)
-            for b, h in zip(dw.batches, host_out):
-                h.copy_(b.out, non_blocking=True)
-
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup):
-                e2e_step(i)
-            torch.cuda.synchronize()
-            s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s2.record(stream)
-            for i in range(K):
-                e2e_step(i)
-            e2.record(stream)
-            torch.cuda.synchronize()
-        e2e_ms = s2.elapsed_time(e2) / K
-        if world > 1:
-            e2e_ms = max_over_ranks(e2e_ms, f"cuda:{dev}")
-        e2e = {"value": round(job_rate(acc["total"] * NL, world, e2e_ms * 1e-3) / 1e9, 2),
-               "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_ms, 5),
-               "launches": "one CUDA graph per step" if graphs is not None else "direct"}
+                dev_in.append(b.q_start_loc)
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)  # on `stream` (the current stream here)
         if graphs is not None:
-            for g in graphs:
-                g.close()
-    status = int(base.dev_status.item())
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed steps")
-    return wl, acc, R, ms, kern_ms, clk.summary(), e2e, fused, n_append
+            graphs[i % R].launch(dw.batches[0].q.shape[0], stream)
+        else:
+            pr.step(i)
+        for b, h in zip(dw.batches, host_out):
+            h.copy_(b.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for i in range(K):
+            e2e_step(i)
+        e2.record(stream)
+        torch.cuda.synchronize()
+    e2e_ms = s2.elapsed_time(e2) / K
+    if world > 1:
+        e2e_ms = max_over_ranks(e2e_ms, f"cuda:{dev}")
+    if graphs is not None:
+        for g in graphs:
+            g.close()
+    return {"value": round(job_rate(acc["total"] * NL, world, e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms, 5),
+            "launches": "one CUDA graph per step" if graphs is not None else "direct"}
+
+
+def compare_lines(prev, line, threshold=0.10):
+    """Per-kernel regression check against an earlier line of this benchmark: every
+    kernel time of the `workloads` table present in both, its relative change, and the
+    kernels slower by more than `threshold`."""
+    out, slow = {}, []
+    for wname, kernels in line.get("workloads", {}).items():
+        for kname, rec in kernels.items():
+            old = prev.get("workloads", {}).get(wname, {}).get(kname)
+            if not old or not old.get("us") or "us" not in rec:
+                continue
+            ch = rec["us"] / old["us"] - 1.0
+            key = f"{wname}/{kname}"
+            out[key] = {"prev_us": old["us"], "us": rec["us"], "change": round(ch, 4)}
+            if ch > threshold:
+                slow.append(key)
+    return {"threshold": threshold, "kernels": out, "regressions": slow}
+
+
+def read_line(path):
+    """The last JSON object line of a file (a bench line, or a driver record holding one
+    under parsed / in its output)."""
+    text = open(path).read()
+    try:
+        d = json.loads(text)
+        if isinstance(d, dict):
+            if "workloads" in d:
+                return d
+            for k in ("parsed",):
+                if isinstance(d.get(k), dict):
+                    return d[k]
+            text = json.dumps(d)
+    except ValueError:
+        pass
+    found = None
+    for m in re.finditer(r'\{"metric".*?\}(?=\s*(?:\\n|\n|$))', text):
+        try:
+            found = json.loads(m.group(0).encode().decode("unicode_escape"))
+        except ValueError:
+            continue
+    if found is None:
+        raise ValueError(f"no bench line in {path}")
+    return found
 
 
 def main():
@@ -527,10 +689,11 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    wl, acc, R, ms, kern_ms, clocks, e2e, fused, n_append = run_ours(args, rank, world)
+    r = run_ours(args, rank, world)
+    wl, acc, R, ms, kern = r["wl"], r["acc"], r["R"], r["ms"], r["kern"]
+    clocks, e2e, fused, n_append = r["clocks"], r["e2e"], r["fused"], r["n_append"]
     K = args.steps
-    names = (["append"] if n_append else []) + [b.kind for b in wl.batches]
-    avg = {n: statistics.fmean(v) for n, v in zip(names, kern_ms)}
+    avg = {n: v["ms"] for n, v in kern.items()}
     from paged_kv_attention_09_gb300 import workloads as W
     peak, peak_kind = measured_hbm()
     NL = max(1, args.layers)
@@ -549,7 +712,9 @@ def main():
                      ("; prefill chunk rows appended, then prefill attention"
                       if len(wl.batches) > 1 else "") if fused else
                      "append new K/V rows, then attention over every batch"),
-            "timing": "CUDA events around one CUDA-graph replay of the K steps",
+            "timing": ("value: CUDA events around one CUDA-graph replay of the K steps; "
+                       f"kernels: median of >= {KERNEL_REPLAYS} replays of a graph of "
+                       f"{KERNEL_LAUNCHES} launches, replayed for >= {KERNEL_MIN_MS:.0f} ms"),
             "bytes_per_step": acc["total"] * NL, "replicas": R,
             "l2": f"rotating {R} replicas of every input ({R} x {acc['total'] * NL / 1e6:.1f} MB "
                   f"per cycle > {L2_BYTES / 2**20:.0f} MiB L2)",
@@ -577,9 +742,13 @@ def main():
                            "frac_of_bf16_burst": round(tf / burst, 4),
                            "frac_of_bf16_sustained": round(tf / sustained, 4),
                            "peak_source": src}
+    if r.get("workloads"):
+        line["workloads"] = r["workloads"]
     if e2e:
         line["e2e"] = e2e
     line["clocks"] = clocks
+    if args.compare:
+        line["compare"] = compare_lines(read_line(args.compare), line)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = len(os.sched_getaffinity(0))
         import oracle

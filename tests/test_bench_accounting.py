@@ -68,12 +68,15 @@ def test_our_arm_line_assembly(capsys, monkeypatch):
     wl = W.workload("tinyllama-int8")
     acc = bench.step_accounting(wl)
     ms = 0.034  # per step
-    kern = [[0.0026], [0.0308]]  # append, decode (per launch)
+    kern = {"append": {"ms": 0.0026, "replays": 5, "launches_per_graph": 50},
+            "decode": {"ms": 0.0308, "replays": 5, "launches_per_graph": 50}}
     e2e = {"value": 1.0, "unit": "GB/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 1,
            "ms_per_step": 0.08, "launches": "direct"}
     clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 5, "reasons": []}
-    monkeypatch.setattr(bench, "run_ours",
-                        lambda args, rank, world: (wl, acc, 4, ms, kern, clocks, e2e, False, 256))
+    table = {"tinyllama-int8": bench.workload_entry(wl, acc, kern, 6794.5, (1903.5, 1700.2, "m"))}
+    monkeypatch.setattr(bench, "run_ours", lambda args, rank, world: dict(
+        wl=wl, acc=acc, R=4, ms=ms, kern=kern, clocks=clocks, e2e=e2e, fused=False, n_append=256,
+        workloads=table))
     monkeypatch.setattr(bench, "measured_hbm", lambda: (6794.5, "measured"))
     monkeypatch.setattr(sys, "argv", ["bench.py", "--no-cpu-baseline", "--steps", "7",
                                       "--warmup", "3"])
@@ -94,6 +97,9 @@ def test_our_arm_line_assembly(capsys, monkeypatch):
     assert r["algorithmic_bytes_per_launch"] == acc["decode"]
     assert d["config"]["workload"] == "tinyllama-int8" and d["config"]["layers"] == 1
     assert d["dtype"] == "int8-kv/f32-acc"
+    w = d["workloads"]["tinyllama-int8"]["decode"]
+    assert w["us"] == 30.8 and abs(w["GBs"] - r["achieved"]) < 0.2
+    assert abs(w["frac_of_8tbs"] - w["GBs"] / 8000) < 1e-4
 
 
 def test_profile_traffic_follows_the_kernel_code(tmp_path, monkeypatch):
@@ -123,9 +129,11 @@ def test_line_with_prefill_and_cpu_baselines(capsys, monkeypatch):
     oracle's all-core and single-core rates (the oracle itself replaced here)."""
     wl = W.workload("mixed")
     acc = bench.step_accounting(wl)
-    kern = [[0.006], [0.0287], [0.0377]]  # append, decode, prefill
-    monkeypatch.setattr(bench, "run_ours", lambda args, rank, world: (
-        wl, acc, 4, 0.08, kern, None, None, False, 1028))
+    kern = {k: {"ms": v, "replays": 5, "launches_per_graph": 50}
+            for k, v in (("append", 0.006), ("decode", 0.0287), ("prefill", 0.0377))}
+    monkeypatch.setattr(bench, "run_ours", lambda args, rank, world: dict(
+        wl=wl, acc=acc, R=4, ms=0.08, kern=kern, clocks=None, e2e=None, fused=False,
+        n_append=1028, workloads={}))
     monkeypatch.setattr(bench, "measured_hbm", lambda: (6794.5, "measured"))
     monkeypatch.setattr(bench, "measured_bf16", lambda: (1903.5, 1700.2, "measured"))
     calls = []
@@ -147,3 +155,37 @@ def test_line_with_prefill_and_cpu_baselines(capsys, monkeypatch):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == 0.5 and cb["single_core"]["value"] == 0.1
     assert cb["cores"] == min(len(os.sched_getaffinity(0)), 2) and calls[-1] == 1
+
+
+def test_kernel_graph_time_protocol():
+    """A kernel's time is the median replay of a graph of 50 launches, over at least 5
+    replays and at least 200 ms of timed replays."""
+    replays = []
+
+    def replay(g):
+        replays.append(g)
+        return 20.0 if len(replays) % 2 else 30.0  # ms per replay of 50 launches
+    ms, n = bench.kernel_graph_ms(lambda k: ("graph", k), replay, 50)
+    assert replays[0] == ("graph", 50)
+    assert n == len(replays) - 1 >= 5            # one untimed warm replay first
+    assert sum(20.0 if i % 2 else 30.0 for i in range(2, n + 2)) >= 200.0
+    assert ms in (20.0 / 50, 30.0 / 50, 25.0 / 50)
+
+
+def test_workload_entry_and_regression_compare():
+    wl = W.workload("mixed")
+    acc = bench.step_accounting(wl)
+    kt = {"decode": {"ms": 0.028, "replays": 7, "launches_per_graph": 50},
+          "prefill": {"ms": 0.040, "replays": 7, "launches_per_graph": 50}}
+    e = bench.workload_entry(wl, acc, kt, 6652.7, (1935.2, 1754.5, "measured"))
+    gbs = acc["decode"] / 28e-6 / 1e9
+    assert abs(e["decode"]["GBs"] - gbs) < 0.1
+    assert abs(e["decode"]["frac_of_measured"] - gbs / 6652.7) < 1e-4
+    assert abs(e["decode"]["kv_tokens_per_s"] - 4 * 32768 / 28e-6) < 1.0
+    tf = acc["prefill_flops"] / 40e-6 / 1e12
+    assert abs(e["prefill"]["TFLOPs"] - tf) < 0.1
+    assert abs(e["prefill"]["frac_of_bf16_burst"] - tf / 1935.2) < 1e-4
+    prev = {"workloads": {"mixed": {"decode": {"us": 25.0}, "prefill": {"us": 40.0}}}}
+    c = bench.compare_lines(prev, {"workloads": {"mixed": e}})
+    assert c["regressions"] == ["mixed/decode"]          # 28 vs 25 us: 12% slower
+    assert c["kernels"]["mixed/prefill"]["change"] == 0.0
