@@ -45,15 +45,21 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, defines=(), lib: str = LIB,
+          obj: str = OBJ) -> str:
+    """Compile and link the library; returns its path.  ``defines``, ``lib``, ``obj``:
+    extra preprocessor definitions and where a variant build (tests) puts its library and
+    objects."""
     home = cuda_home()
     nvcc = os.path.join(home, "bin", "nvcc")
-    os.makedirs(OBJ, exist_ok=True)
+    OBJ_, LIB_ = obj, lib
+    os.makedirs(OBJ_, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "pkv.h"))
     # objects built with other defines are stale
-    stamp = os.path.join(OBJ, "defines.txt")
-    want = " ".join(_defines())
+    stamp = os.path.join(OBJ_, "defines.txt")
+    defs = _defines() + list(defines)
+    want = " ".join(defs)
     if not os.path.exists(stamp) or open(stamp).read() != want:
         force = True
         with open(stamp, "w") as f:
@@ -61,9 +67,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
-        o = os.path.join(OBJ, src.replace(".cu", ".o"))
+        o = os.path.join(OBJ_, src.replace(".cu", ".o"))
         if force or _stale(o, [s, *headers]):
-            cmd = [nvcc, *ARCH, *FLAGS, *_defines(), "-c", s, "-o", o + ".tmp"]
+            cmd = [nvcc, *ARCH, *FLAGS, *defs, "-c", s, "-o", o + ".tmp"]
             r = subprocess.run(cmd, capture_output=True, text=True)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -74,16 +80,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if force or _stale(LIB, objs):
+    if force or _stale(LIB_, objs):
         libdir = os.path.join(home, "lib64")
-        tmp = LIB + f".tmp{os.getpid()}"
+        tmp = LIB_ + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", f"-rpath,{libdir}", *(["-ldl"] if _defines() else [])]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, LIB_)
+    return LIB_
 
 
 if __name__ == "__main__":

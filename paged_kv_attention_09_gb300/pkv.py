@@ -79,6 +79,13 @@ def load(path: str = LIB_PATH):
     global _lib
     if _lib is not None:
         return _lib
+    _lib = bind(path)
+    return _lib
+
+
+def bind(path: str):
+    """A handle on the library at ``path`` with every entry point's argument types (a
+    variant build, e.g. a test build, is used beside the product library this way)."""
     if not os.path.exists(path):
         raise RuntimeError(f"libpkv.so not built ({path}); run __graft_entry__.build()")
     lib = ctypes.CDLL(path)
@@ -117,7 +124,6 @@ def load(path: str = LIB_PATH):
     for fn in ("pkv_decode_graph_workspace_size", "pkv_decode_graph_create",
                "pkv_decode_graph_launch", "pkv_decode_graph_bucket"):
         getattr(lib, fn).restype = ctypes.c_int
-    _lib = lib
     return lib
 
 

@@ -176,3 +176,8 @@ def test_decode_entry_points_validate_alike(lib):
     assert lib.pkv_decode_workspace_size_ex(ctypes.byref(_cache()), 2, 4, 4,
                                             ctypes.byref(pkv.pkv_decode_opts(-3)),
                                             ctypes.byref(n)) == 2
+
+
+def test_product_library_has_no_test_hooks(lib):
+    """The give-up-at-once wait used by the timeout test exists only in test builds."""
+    assert not hasattr(lib, "pkv_test_fail_first_wait")

@@ -4,6 +4,8 @@ Chunks of assorted lengths (1 token, page-aligned, ragged, longer than a tile) o
 assorted prior contexts (none, partial page, several tiles); FP32 and BF16 queries;
 NaN-poisoned padding; device-side errors; sampled rows of the full-size mixed workload.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -65,19 +67,42 @@ def test_prefill_lq1_matches_decode():
     assert max_err(got_p[0], got_d[0]) <= 2e-3
 
 
-def test_mixed_full_size_prefill_sampled_rows():
+def _oracle_prefill_by_pieces(oc, b, scale, pieces):
+    """The oracle's prefill of batch b, computed as `pieces` row ranges per sequence on a
+    thread pool: rows r0..r1-1 of a chunk of Lq rows over context L are themselves a
+    causal chunk of r1 - r0 rows over context L - (Lq - r1) (each row keeps its position
+    and sees the same keys), so the pieces together are the whole chunk."""
+    from concurrent.futures import ThreadPoolExecutor
+    jobs = []
+    for s in range(b.num_seqs):
+        q0, q1 = int(b.q_start_loc[s]), int(b.q_start_loc[s + 1])
+        Lq, L = q1 - q0, int(b.context_lens[s])
+        cuts = np.linspace(0, Lq, pieces + 1).astype(int)
+        for r0, r1 in zip(cuts[:-1], cuts[1:]):
+            if r1 > r0:
+                jobs.append((s, q0 + r0, q0 + r1, L - (Lq - r1)))
+    out = np.full(b.q.shape, np.nan)
+
+    def run(job):
+        s, a0, a1, ctx = job
+        out[a0:a1] = oracle.prefill(oc, b.q[a0:a1], b.q_dtype,
+                                    np.array([0, a1 - a0], np.int32),
+                                    b.block_tables[s:s + 1], np.array([ctx], np.int32), scale)
+    with ThreadPoolExecutor(max(1, len(os.sched_getaffinity(0)))) as ex:
+        list(ex.map(run, jobs))
+    return out
+
+
+def test_mixed_full_size_prefill_every_row():
+    """The mixed workload's two 512-token chunks over 2048 prior tokens, in the
+    benchmark's launch configuration: every (chunk row, head) against the oracle."""
     wl = W.workload("mixed")
     got, status, _ = gpu_outputs(wl)
     assert status == 0
     i = [k for k, b in enumerate(wl.batches) if b.kind == "prefill"][0]
     b = wl.batches[i]
     oc = oracle.cache_from_workload(wl)
-    # the oracle recomputes chosen rows as one-token chunks at their positions
-    rows = [0, 1, 255, 511, 512, 700, 1023]
-    for r in rows:
-        s = 0 if r < 512 else 1
-        pos = int(b.context_lens[s]) - 512 + (r - 512 * s)
-        ref = oracle.decode(oc, b.q[r:r + 1], b.q_dtype, b.block_tables[s:s + 1],
-                            np.array([pos + 1], np.int32), wl.scale)
-        assert max_err(got[i][r], ref[0]) <= 2e-3, r
+    ref = _oracle_prefill_by_pieces(oc, b, wl.scale, pieces=8)
+    assert got[i].shape == ref.shape == (1024, 12, 128)
+    assert max_err(got[i], ref) <= 2e-3
     assert np.all(np.isfinite(got[i]))
