@@ -247,6 +247,13 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(p1), "r"(bias));
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
