@@ -67,6 +67,10 @@ def parse():
                     help="comma-separated workloads whose kernels the line reports one by "
                          "one ('all': the five configurations and the FP8 / INT4 caches; "
                          "'none')")
+    ap.add_argument("--profile", action="store_true",
+                    help="a short run for a profiler: the warm-up and the K timed steps only "
+                         "(no per-kernel table, no end-to-end leg, no CPU baseline); its "
+                         "numbers are not benchmark values")
     ap.add_argument("--compare", default=None,
                     help="an earlier line of this benchmark (or a file holding one): report "
                          "every kernel's change and the ones more than 10%% slower")
@@ -522,7 +526,7 @@ def run_ours(args, rank, world):
     with torch.cuda.stream(pr.stream):
         g_step.replay()
     torch.cuda.synchronize()
-    wl_list = [] if args.workloads == "none" else \
+    wl_list = [] if args.workloads == "none" or args.profile else \
         (list(ALL_WORKLOADS) if args.workloads == "all" else args.workloads.split(","))
     tables = {}
     with ClockSampler(dev) as clk:
@@ -533,6 +537,10 @@ def run_ours(args, rank, world):
         if world > 1:
             dist.barrier()
         del g_step
+        if args.profile:
+            return {"wl": wl, "acc": acc, "R": R, "ms": total_ms / K, "kern": {},
+                    "clocks": None, "e2e": None, "fused": pr.fused, "n_append": pr.n_append,
+                    "workloads": {}}
         # per-kernel times: the benchmarked workload (its layers and step form), then every
         # other workload of the table, one at a time on the device
         kern = pr.kernel_times()
@@ -749,7 +757,7 @@ def main():
     line["clocks"] = clocks
     if args.compare:
         line["compare"] = compare_lines(read_line(args.compare), line)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         threads = len(os.sched_getaffinity(0))
         import oracle
         oc = oracle.cache_from_workload(wl)  # built once for both samples

@@ -79,6 +79,7 @@ struct DParams {
   int32_t* dev_status;
   int q_dtype, Hkv, Hq, G, hpc, head_groups, MB, B, num_pages, chunk;
   int window;  // sliding window in tokens (0: none)
+  int cluster;  // 1: the split blocks of a sequence form a cluster and merge on chip
   float scale_log2;
   // the fused decode step (STEP kernels only)
   uint8_t* kw;
@@ -135,7 +136,9 @@ struct Smem {
   static constexpr int kW = Tune<KVT, D>::W;
   static constexpr int stages = kW * Lo::S * Lo::stageBytes;
   // merge area: per-warp max[8], sum[8], acc[8][D+2], then weights [warp][8] (floats)
-  static constexpr int combine = (3 * kW * kMaxHeads + kW * kMaxHeads * (D + 2)) * 4;
+  // (+ the block's partial for the on-chip split merge: max[8], sum[8], O[8][D])
+  static constexpr int combine =
+      (3 * kW * kMaxHeads + kW * kMaxHeads * (D + 2) + 2 * kMaxHeads + kMaxHeads * D) * 4;
   static constexpr int big = stages > combine ? stages : combine;
   static constexpr int probs = KVT == kF32 ? kW * kMaxHeads * kPage * 4 : 0;
   // coded formats: the query fragments (one uint4 per k-step and lane) and per-row constants,
@@ -356,13 +359,21 @@ struct F32Warp {
 
 // ------------------------------------------------------------------ BF16 (MMA)
 
+// Lazy rescale margin of the tensor-core paths' softmax: the running max is raised only
+// when a score exceeds it by more than 2^8 (in the exponent's log2 units).
+constexpr float kRescaleLog2 = 8.f;
+
 template <int D>
 struct Bf16Warp {
   static constexpr int KS = D / 16;  // k-steps of the q.k product
-  static constexpr int NT = D / 8;   // n-tiles of the P.V product
+  static constexpr int MT = D / 16;  // m-tiles (16 head-dim rows) of O^T = V^T P^T
   uint32_t qa[KS][4];  // raw query bits from prefetch(), then the A fragments
-  float o[NT][4];
-  float m, l, row_scale;
+  // O^T accumulators: lane (r, c) holds head-dim rows 16 mt + r and 16 mt + r + 8 of
+  // heads 2c and 2c + 1
+  float o[MT][4];
+  // per query head r = lane / 4: -(running max) and the running sum, in log2 units (the
+  // max is raised only beyond a 2^8 margin), and the head's log2 scale
+  float nm, l, row_scale;
 
   __device__ void finish(const uint8_t*, int, uint32_t) {}
   // Query elements of k-slots {2c, 2c+1} and {2c+8, 2c+9} of every k-step (the standard
@@ -414,16 +425,18 @@ struct Bf16Warp {
       }
     }
     row_scale = p.scale_log2;
-    m = -CUDART_INF_F;
+    nm = CUDART_INF_F;
     l = 0.f;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    for (int j = 0; j < MT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   }
 
-  // One page.  K and V arrive as tensor-core tiles, so ldmatrix builds every B fragment
-  // from whole 16-byte core-matrix rows without bank conflicts.  n-tile j holds tokens
-  // 8j .. 8j+7; lane (r, c) ends up with tokens 2c, 2c+1, 8+2c, 9+2c.
-  // tokens lo .. valid - 1 are attended (lo > 0 only for the first page of a window)
+  // One page.  K and V arrive as tensor-core tiles, so ldmatrix builds every fragment
+  // from whole 16-byte core-matrix rows without bank conflicts.  Scores: n-tile j holds
+  // tokens 8j .. 8j+7, lane (r, c) ends up with tokens 2c, 2c+1, 8+2c, 9+2c of head r,
+  // which is exactly its B fragment of P^T for the transposed product (k = tokens,
+  // n = heads).  Tokens lo .. valid - 1 are attended (lo > 0 only for the first page of a
+  // window).
   __device__ void page(const uint8_t* st, int valid, int lo, int lane) {
     using Lo = Layout<kBF16, D>;
     const int c = lane & 3;
@@ -458,32 +471,43 @@ struct Bf16Warp {
       vmask0 = (in(2 * c + 0) ? 0x0000ffffu : 0u) | (in(2 * c + 1) ? 0xffff0000u : 0u);
       vmask1 = (in(2 * c + 8) ? 0x0000ffffu : 0u) | (in(2 * c + 9) ? 0xffff0000u : 0u);
     }
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    float mx = fmaxf(fmax3(x[0], x[1], x[2]), x[3]);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float mn = fmaxf(m, mx);
-    const float corr = fast_exp2(m - mn);
-    m = mn;
-    float pr[4];
+    // the running max is raised only when a score exceeds it by more than 2^8 (the
+    // probabilities then stay below 256, exact enough in BF16 hi + lo and in FP32)
+    const bool need = mx + nm > kRescaleLog2;
+    if (__any_sync(0xffffffffu, need)) {
+      const float nn = need ? -mx : nm;
+      const float corr = fast_exp2(nn - nm);  // 0 on the first page (nm = +inf)
+      nm = nn;
+      l *= corr;
+      // this lane's accumulators belong to heads 2c and 2c + 1
+      const float ca = __shfl_sync(0xffffffffu, corr, 8 * c);
+      const float cb = __shfl_sync(0xffffffffu, corr, 8 * c + 4);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(x[i] - mn);
-    l = l * corr + (pr[0] + pr[1]) + (pr[2] + pr[3]);
-    if (__any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        o[j][0] *= corr; o[j][1] *= corr; o[j][2] *= corr; o[j][3] *= corr;
+      for (int j = 0; j < MT; ++j) {
+        o[j][0] *= ca; o[j][1] *= cb; o[j][2] *= ca; o[j][3] *= cb;
       }
     }
-    uint32_t pa[4];
-    split_b2(pr[0], pr[1], pa[0], pa[1]);
-    split_b2(pr[2], pr[3], pa[2], pa[3]);
+    float pr[4];
 #pragma unroll
-    for (int j = 0; j < NT; j += 2) {
-      // matrices: (d-group j, tokens 0-7), (j, 8-15), (j+1, 0-7), (j+1, 8-15): contiguous
-      uint32_t f[4];
-      ldsm_x4(f, Vs + (j << 8) + (lane << 4));
-      mma_bf16(o[j], pa, f[0] & vmask0, f[1] & vmask1);
-      mma_bf16(o[j + 1], pa, f[2] & vmask0, f[3] & vmask1);
+    for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(x[i] + nm);
+    l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    // B = P^T: tokens {2c, 2c+1} and {8+2c, 9+2c} of head r, high part and remainder
+    uint32_t bh0, bl0, bh1, bl1;
+    split_b2(pr[0], pr[1], bh0, bl0);
+    split_b2(pr[2], pr[3], bh1, bl1);
+    // A = V^T rows 16 j .. 16 j + 15 (core matrices of head-dim groups 2j, 2j+1 and token
+    // groups 0, 1, handed out in the a0..a3 order), one ldmatrix per m-tile
+    const uint32_t vrow = Vs + ((0x3120u >> (4 * (lane >> 3))) & 0xfu) * 128 + ((lane & 7) << 4);
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+      uint32_t a[4];
+      ldsm_x4(a, vrow + j * 512);
+      a[0] &= vmask0; a[1] &= vmask0; a[2] &= vmask1; a[3] &= vmask1;
+      mma_bf16(o[j], a, bh0, bh1);
+      mma_bf16(o[j], a, bl0, bl1);
     }
   }
 
@@ -493,13 +517,17 @@ struct Bf16Warp {
     lt += __shfl_xor_sync(0xffffffffu, lt, 1);
     lt += __shfl_xor_sync(0xffffffffu, lt, 2);
     if (c == 0) {
-      cm[r] = m;
+      cm[r] = -nm;  // the running max in log2 units, as the merge expects
       cl[r] = lt;
     }
+    float* oa = cO + (2 * c) * (D + 2);
+    float* ob = oa + (D + 2);
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      cO[r * (D + 2) + 8 * j + 2 * c + 0] = o[j][0] + o[j][2];
-      cO[r * (D + 2) + 8 * j + 2 * c + 1] = o[j][1] + o[j][3];
+    for (int j = 0; j < MT; ++j) {
+      oa[16 * j + r] = o[j][0];
+      ob[16 * j + r] = o[j][1];
+      oa[16 * j + r + 8] = o[j][2];
+      ob[16 * j + r + 8] = o[j][3];
     }
   }
 };
@@ -515,7 +543,6 @@ struct Bf16Warp {
 // address is a per-lane base plus a constant (the ring of stages is unrolled), the V
 // codes arrive with two ldmatrix per 64 head-dim rows, the softmax runs on packed FP32
 // pairs, and masking is confined to the few pages that are only partly attended.
-constexpr float kRescaleLog2 = 8.f;  // lazy rescale margin of the coded formats' softmax
 
 // (a, b) -> f16x2 high part and f16x2 remainder: a = hi + lo to ~22 bits.
 __device__ __forceinline__ void split_h2x(float2 a, uint32_t& hi, uint32_t& lo) {
@@ -878,6 +905,78 @@ struct WarpOf<kINT4, D> {
 
 // ------------------------------------------------------------------ the kernel
 
+// Split-K merge on chip, for a sequence whose split blocks form one thread-block cluster
+// (rank = split).  Every block has left its partial (max, sum, O of its heads) in its own
+// shared memory (`part`); each counts itself done on block 0's counter, and the block that
+// finishes last reads every partial through distributed shared memory, writes the output,
+// and releases the others, which wait (bounded) so that their shared memory outlives the
+// reads.  No global memory is touched and no block waits for another's work.
+template <int D, int kThreads>
+__device__ __noinline__ void cluster_merge(const DParams& p, const float* part, int nsplit, int b,
+                                           int h0, int nh, int tid, int lane, int w,
+                                           uint32_t* s_done, uint64_t* s_release, int* s_last) {
+  constexpr int kW = kThreads / 32;
+  __syncthreads();        // this block's partial is complete
+  cluster_wait_acquire();  // every block's barrier and counter are initialised
+  if (tid == 0) {
+    fence_acq_rel_cluster();
+    const uint32_t old = dsmem_atomic_add(dsmem_addr(smem_u32(s_done), 0), 1);
+    *s_last = old == static_cast<uint32_t>(nsplit - 1);
+  }
+  __syncthreads();
+  if (!*s_last) {
+    if (tid == 0 && !mbar_wait(s_release, 0) && p.dev_status)
+      atomicOr(p.dev_status, 0x10);  // PKV_DEV_TIMEOUT
+    return;
+  }
+  fence_acq_rel_cluster();  // the other blocks' partials are visible
+  __shared__ float wts[9 * kMaxHeads];  // [split][head] weights, then [head] 1 / total sum
+  const uint32_t part_u32 = smem_u32(part);
+  for (int r = w; r < nh; r += kW) {
+    float ms = -CUDART_INF_F, ls = 0.f;
+    if (lane < nsplit) {
+      ms = dsmem_ld_f32(dsmem_addr(part_u32 + 4 * r, lane));
+      ls = dsmem_ld_f32(dsmem_addr(part_u32 + 4 * (kMaxHeads + r), lane));
+    }
+    const bool poisoned = __any_sync(0xffffffffu, isnan(ms));
+    float M = ms;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float f = ms == -CUDART_INF_F ? 0.f : fast_exp2(ms - M);
+    float Ls = ls * f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+    if (lane < nsplit) wts[lane * kMaxHeads + r] = f;
+    if (lane == 0) wts[8 * kMaxHeads + r] = poisoned ? CUDART_NAN_F : (Ls > 0.f ? 1.f / Ls : 0.f);
+  }
+  __syncthreads();
+  constexpr int D4 = D / 4;
+  const size_t row0 = static_cast<size_t>(b) * p.Hq + h0;
+  for (int c = tid; c < nh * D4; c += kThreads) {
+    const int r = c / D4;
+    const uint32_t src = part_u32 + 4 * (2 * kMaxHeads + r * D) + 16 * (c % D4);
+    float4 v[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < nsplit) v[s] = dsmem_ld_f4(dsmem_addr(src, s));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (s < nsplit) {
+        const float wt = wts[s * kMaxHeads + r];
+        acc.x += v[s].x * wt; acc.y += v[s].y * wt; acc.z += v[s].z * wt; acc.w += v[s].w * wt;
+      }
+    }
+    const float inv = wts[8 * kMaxHeads + r];
+    *reinterpret_cast<float4*>(p.out + (row0 + r) * D + 4 * (c % D4)) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+  __syncthreads();  // every read of another block's shared memory is done
+  const uint32_t me = cluster_rank();
+  if (tid < nsplit && static_cast<uint32_t>(tid) != me)
+    mbar_arrive_remote(dsmem_addr(smem_u32(s_release), tid));
+}
+
 // WIN: compiled with the sliding-window range and mask (the kernels without it carry no
 // trace of it: the INT8 kernel sits at its register budget)
 template <int KVT, int D, bool STEP, bool WIN>
@@ -893,9 +992,23 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   uint8_t* aux = smem + Sm::big + Sm::probs;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::big + Sm::probs + Sm::aux);
   __shared__ int s_flag, s_last;
+  // on-chip split merge: this block's release by the merging block, and (block 0 of the
+  // cluster) the count of blocks that finished
+  __shared__ __align__(8) uint64_t s_release;
+  __shared__ uint32_t s_done;
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int split = blockIdx.x, b = blockIdx.y, z = blockIdx.z;
+  if (p.cluster) {
+    // Every thread of every block of the cluster arrives here first, before any exit: a
+    // block reaches into another's shared memory only after the matching wait.
+    if (tid == 0) {
+      mbar_init(&s_release, 1);
+      s_done = 0;
+      fence_barrier_init();
+    }
+    cluster_arrive_release();
+  }
   const int g = z / p.head_groups, hg = z % p.head_groups;
   const int h0 = g * p.G + hg * p.hpc;
   const int nh = min(p.hpc, p.G - hg * p.hpc);
@@ -1348,6 +1461,8 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   // Merge weights, once per (warp, head): exp2(m_w - M), divided by the total sum when
   // this block holds the whole sequence (NaN when the block met an error).
   float* fw = cO + kW * kMaxHeads * (D + 2);
+  // on-chip split merge: this block's partial, max[8], sum[8], then O[8][D] (16-byte rows)
+  float* part = fw + kW * kMaxHeads;
   const bool single = nsplit == 1;
   if (tid < nh) {
     const int r = tid;
@@ -1369,9 +1484,14 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     } else {
 #pragma unroll
       for (int ww = 0; ww < kW; ++ww) fw[ww * kMaxHeads + r] = f[ww];
-      const size_t prow = static_cast<size_t>(split) * p.B * p.Hq + row;
-      p.ws_m[prow] = err ? CUDART_NAN_F : M;
-      p.ws_l[prow] = Ls;
+      if (p.cluster) {
+        part[r] = err ? CUDART_NAN_F : M;
+        part[kMaxHeads + r] = Ls;
+      } else {
+        const size_t prow = static_cast<size_t>(split) * p.B * p.Hq + row;
+        p.ws_m[prow] = err ? CUDART_NAN_F : M;
+        p.ws_l[prow] = Ls;
+      }
     }
   }
   __syncthreads();
@@ -1383,11 +1503,18 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     const size_t row = static_cast<size_t>(b) * p.Hq + h0 + r;
     if (single) {
       p.out[row * D + d] = O;
+    } else if (p.cluster) {
+      part[2 * kMaxHeads + r * D + d] = O;
     } else {
       p.ws_o[(static_cast<size_t>(split) * p.B * p.Hq + row) * D + d] = O;
     }
   }
   if (single) return;
+  if (p.cluster) {
+    cluster_merge<D, kThreads>(p, part, nsplit, b, h0, nh, tid, lane, w, &s_done, &s_release,
+                               &s_last);
+    return;
+  }
 
   // ---- split-K: the last block of this (sequence, head group) merges all partials
   __threadfence();
@@ -1545,9 +1672,16 @@ Variant variant(int dtype, int D, bool step, bool win) {
 // Per-device facts queried once: SM count, and for each kernel variant its resident
 // blocks per SM (after raising its dynamic shared-memory limit).
 constexpr int kMaxDevices = 64;
+constexpr int kMaxCluster = 8;  // portable cluster size: the largest on-chip split merge
 struct DevInfo {
   int sms = 0;
   int occ[kVariants] = {};
+  // clusters of n blocks of the variant that can be resident at once (-1: not asked yet)
+  int clusters[kVariants][kMaxCluster + 1];
+  DevInfo() {
+    for (auto& v : clusters)
+      for (int& c : v) c = -1;
+  }
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -1571,6 +1705,34 @@ bool device_facts(int device, const Variant& v, int* sms, int* occ) {
   *sms = d.sms;
   *occ = d.occ[v.index];
   return true;
+}
+
+// How many clusters of n blocks of variant v can be resident at once on `device` (asked
+// once; 0 if none can be launched).
+int clusters_resident(int device, const Variant& v, int n) {
+  if (device < 0 || device >= kMaxDevices || v.index < 0 || n < 2 || n > kMaxCluster) return 0;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  int& c = g_dev[device].clusters[v.index][n];
+  if (c < 0) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(n, 1, 1);
+    cfg.blockDim = dim3(v.warps * 32);
+    cfg.dynamicSmemBytes = v.smem;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = n;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int num = 0;
+    if (cudaOccupancyMaxActiveClusters(&num, v.fn, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      num = 0;
+    }
+    c = num;
+  }
+  return c;
 }
 
 }  // namespace
@@ -1617,8 +1779,16 @@ bool plan_decode(const CacheView& c, int B, int Hq, int MB, int q_dtype, int dev
   if ((mb + chunk - 1) / chunk > v.max_splits) chunk = (mb + v.max_splits - 1) / v.max_splits;
   plan->chunk_pages = chunk;
   plan->n_splits = (mb + chunk - 1) / chunk;
+  // Up to kMaxCluster splits merge on chip (a cluster per sequence and head group, no
+  // workspace) when every cluster of the launch is resident at once (a cluster is placed
+  // whole on one GPC, so fewer clusters than slots / n fit, and a second wave of clusters
+  // costs far more than the merge saves); otherwise the splits merge through the
+  // workspace and the last-arriving block.
+  const long long units_all = static_cast<long long>(B) * c.Hkv * plan->head_groups;
+  plan->cluster = plan->n_splits > 1 && plan->n_splits <= kMaxCluster &&
+                  units_all <= clusters_resident(device, v, plan->n_splits);
   size_t ws = 0;
-  if (plan->n_splits > 1) {
+  if (plan->n_splits > 1 && !plan->cluster) {
     const size_t rows = static_cast<size_t>(plan->n_splits) * B * Hq;
     const size_t tickets = static_cast<size_t>(B) * c.Hkv * plan->head_groups;
     ws = ((tickets * 4 + 255) / 256) * 256 + rows * (c.D + 2) * 4;
@@ -1666,7 +1836,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
       for (int i = 0; i < a.c.D / 2; ++i) p.inv_freq[i] = std::pow(a.rope_theta, -2.0 * i / a.c.D);
     }
   }
-  if (plan.n_splits > 1) {
+  p.cluster = plan.cluster;
+  if (plan.n_splits > 1 && !plan.cluster) {
     const size_t tickets = static_cast<size_t>(a.B) * a.c.Hkv * plan.head_groups;
     uint8_t* base = static_cast<uint8_t*>(a.ws);
     p.ws_ticket = reinterpret_cast<int*>(base);
@@ -1679,7 +1850,20 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   // (the shared-memory limit was raised by plan_decode on this device)
   const dim3 grid(plan.n_splits, a.B, a.c.Hkv * plan.head_groups);
   void* args[] = {&p};
-  return cudaLaunchKernel(v.fn, grid, dim3(v.warps * 32), args, v.smem, st);
+  if (!plan.cluster) return cudaLaunchKernel(v.fn, grid, dim3(v.warps * 32), args, v.smem, st);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(v.warps * 32);
+  cfg.dynamicSmemBytes = v.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = plan.n_splits;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, v.fn, args);
 }
 
 }  // namespace pkv

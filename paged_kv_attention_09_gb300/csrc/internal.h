@@ -47,7 +47,8 @@ struct DecodePlan {
   int head_groups;    // ceil(G / heads_per_cta)
   int chunk_pages;    // pages per thread block
   int n_splits;       // grid.x = ceil(max_blocks / chunk_pages)
-  size_t ws_bytes;    // workspace bytes
+  int cluster;        // 1: the n_splits blocks of a sequence form a cluster and merge on chip
+  size_t ws_bytes;    // workspace bytes (0 for on-chip merges)
 };
 
 struct DecodeArgs {

@@ -120,7 +120,7 @@ def test_bad_page_and_bad_length_give_nan_rows_and_status():
 def test_workspace_is_left_zero_for_the_next_call():
     wl = W.small_workload(98, num_q_heads=8, num_kv_heads=2, head_dim=64, kv_dtype=W.INT8,
                           q_dtype=W.F32, decode_lens=[200, 200])
-    dw = runner.upload(wl, split_pages=2)
+    dw = runner.upload(wl, split_pages=1)  # 13 splits: merged through the workspace
     ws = dw.batches[0].workspace
     assert ws is not None
     first = None

@@ -3,11 +3,11 @@
 Programs that embed the library inside an engine whose pool owns all device memory, or
 that forbid allocation after start-up, cannot hand the library a workspace; this entry
 point keeps its split-K scratch in a fixed array inside the library instead.  The tests
-call it through the C ABI on workloads whose plan splits sequences across blocks (so the
-scratch is really used), twice in a row (the array keeps the previous call's contents),
-and require the result of pkv_decode_attn with a caller workspace bit for bit: both run
-the same plan and kernel.  The file name sorts last so that a stop-at-first-failure run
-has run every other test first.
+call it through the C ABI on workloads whose plan splits sequences across more blocks
+than merge on chip (so the scratch is really used), twice in a row (the array keeps the
+previous call's contents), and require the result of pkv_decode_attn with a caller
+workspace bit for bit: both run the same plan and kernel.  The file name sorts last so
+that a stop-at-first-failure run has run every other test first.
 """
 import ctypes
 
@@ -73,10 +73,10 @@ def _both(dw, b, split_pages=0):
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_noalloc_matches_workspace_entry_on_two_calls(case):
     wl = W.small_workload(4000 + case, **CASES[case])
-    dw = runner.upload(wl)
+    dw = runner.upload(wl, split_pages=16)  # >= 13 splits: merged through the scratch
     b = dw.batches[0]
-    assert b.workspace is not None, "the automatic plan must split so that scratch is used"
-    ref, got = _both(dw, b)
+    assert b.workspace is not None, "the plan must use scratch"
+    ref, got = _both(dw, b, split_pages=16)
     for call, g in enumerate(got):
         assert np.all(np.isfinite(g)), f"call {call}"
         assert np.array_equal(g, ref), f"call {call}: not bit-identical to pkv_decode_attn"
@@ -118,3 +118,16 @@ def test_noalloc_rejects_scratch_beyond_its_maximum():
     torch.cuda.synchronize()
     assert not out.any(), "nothing may be launched"
     assert int(status.item()) == 0
+
+
+def test_noalloc_with_an_on_chip_merge_needs_no_scratch():
+    """A sequence split over at most 8 blocks merges on chip: no workspace is needed, and
+    the no-allocation entry point gives pkv_decode_attn's result bit for bit."""
+    wl = W.small_workload(4200, num_q_heads=12, num_kv_heads=2, head_dim=128, kv_dtype=W.BF16,
+                          q_dtype=W.BF16, decode_lens=[16 * 64, 16 * 30 + 3, 5])
+    dw = runner.upload(wl, split_pages=8)  # 8 splits of the 64-page table
+    b = dw.batches[0]
+    assert pkv.pkv_decode_workspace_size(dw.cache, 3, 12, b.block_tables.shape[1], 8) == 0
+    ref, got = _both(dw, b, split_pages=8)
+    for call, g in enumerate(got):
+        assert np.array_equal(g, ref), f"call {call}"
