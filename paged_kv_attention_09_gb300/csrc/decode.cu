@@ -144,8 +144,10 @@ struct Smem {
   // coded formats: the query fragments (one uint4 per k-step and lane) and per-row constants,
   // built once by warp 0 and read by every warp
   // (+ the raw query rows of the block, bulk-copied at block start, and their barrier)
+  // (a fused-step kernel lands the raw rows in its rotated-query area instead: rotation
+  // reads the queries itself, so the two are never used in one call)
   static constexpr int auxFrag = (D / 16) * 32 * 16 + 2 * kMaxHeads * 4;
-  static constexpr int auxQ = kMaxHeads * D * 4;
+  static constexpr int auxQ = STEP ? 0 : kMaxHeads * D * 4;
   static constexpr int aux = quantised(KVT) ? auxFrag + auxQ + 16 : 0;
   static constexpr int bars = kW * Lo::S * 8;
   // fused step: the block's rotated query rows (float), cos and sin of the rotation
@@ -155,6 +157,9 @@ struct Smem {
   static constexpr int stepRow = STEP ? 2 * (RowBytes<KVT, D>::value + 16) : 0;
   static constexpr int step0 = big + probs + aux + bars;
   static constexpr int total = step0 + stepQ + stepRope + stepRow;
+  // the coded formats' raw query rows and their barrier (offsets from the base)
+  static constexpr int qraw = STEP ? step0 : big + probs + auxFrag;
+  static constexpr int qbar = big + probs + auxFrag + auxQ;
 };
 
 __device__ __forceinline__ float4 load_q4(const void* q, int q_dtype, size_t i) {
@@ -232,7 +237,7 @@ struct F32Warp {
   __device__ void finish(const uint8_t*, int, uint32_t) {}
   // (loading the queries before the first copy measured slower here: they are only
   // consumed by the first page anyway)
-  __device__ void prefetch(const DParams&, int, int, int, int, int, uint8_t*) {}
+  __device__ void prefetch(const DParams&, int, int, int, int, int, uint8_t*, uint8_t*) {}
   // sq: the block's query rows as float in shared memory (the fused step), else nullptr
   __device__ void init(const DParams& p, int b, int h0, int nh, int lane, uint8_t*, int,
                        const float* sq) {
@@ -378,7 +383,8 @@ struct Bf16Warp {
   __device__ void finish(const uint8_t*, int, uint32_t) {}
   // Query elements of k-slots {2c, 2c+1} and {2c+8, 2c+9} of every k-step (the standard
   // fragment order), loaded as raw bits: two BF16 or two FP32 values per slot pair.
-  __device__ void prefetch(const DParams& p, int b, int h0, int nh, int lane, int, uint8_t*) {
+  __device__ void prefetch(const DParams& p, int b, int h0, int nh, int lane, int, uint8_t*,
+                           uint8_t*) {
     const int r = lane >> 2, c = lane & 3;
     const bool has = r < nh;
     const size_t row = (static_cast<size_t>(b) * p.Hq + h0 + r) * D;
@@ -581,17 +587,17 @@ struct QuantWarp {
   // The block's query rows (heads h0 .. h0 + nh - 1 of sequence b, contiguous in q) are
   // requested by one bulk copy at block start, ahead of the block-table and length reads,
   // so that they do not queue behind the first wave of page copies.
-  static constexpr int kQOff = Smem<KVT, D>::auxFrag;
-  static constexpr int kQBar = kQOff + Smem<KVT, D>::auxQ;
-  __device__ void prefetch(const DParams& p, int b, int h0, int nh, int lane, int w, uint8_t* aux) {
+  // qraw, qbar: where the rows land (kMaxHeads * D floats at most) and their barrier
+  __device__ void prefetch(const DParams& p, int b, int h0, int nh, int lane, int w,
+                           uint8_t* qraw, uint8_t* qbar) {
     if (w == 0 && lane == 0) {
       const uint32_t elt = p.q_dtype == kBF16 ? 2u : 4u;
       const uint32_t bytes = static_cast<uint32_t>(nh * D) * elt;
-      uint64_t* bar = reinterpret_cast<uint64_t*>(aux + kQBar);
+      uint64_t* bar = reinterpret_cast<uint64_t*>(qbar);
       mbar_init(bar, 1);
       fence_barrier_init();
       mbar_arrive_expect_tx(bar, bytes);
-      bulk_g2s(aux + kQOff,
+      bulk_g2s(qraw,
                static_cast<const uint8_t*>(p.q) + (static_cast<size_t>(b) * p.Hq + h0) * D * elt,
                bytes, bar, l2_evict_first_policy());
     }
@@ -599,15 +605,15 @@ struct QuantWarp {
   }
   // A block that leaves before init() (a split past its sequence's pages) first lets the
   // query copy land, so that no copy writes into the shared memory of an exited block.
-  __device__ void drain_prefetch(uint8_t* aux, int w) {
-    if (w == 0) (void)mbar_wait_warp(smem_u32(aux + kQBar), 0);
+  __device__ void drain_prefetch(uint8_t* qbar, int w) {
+    if (w == 0) (void)mbar_wait_warp(smem_u32(qbar), 0);
   }
 
   // Warp 0 builds the query fragments and the per-row constants in shared memory; the
   // caller synchronises the block before any warp reads them (finish()).  Returns false
   // if the wait for the prefetched rows gave up.
   __device__ bool init(const DParams& p, int b, int h0, int nh, int lane, uint8_t* aux, int w,
-                       const float* sq) {
+                       const float* sq, const uint8_t* qraw, uint8_t* qbar) {
     uint4* frag = reinterpret_cast<uint4*>(aux);
     float* rowc = reinterpret_cast<float*>(aux + KS * 32 * 16);
     bool ok = true;
@@ -615,10 +621,9 @@ struct QuantWarp {
       const int r = lane >> 2, c = lane & 3;
       const bool has = r < nh;
       if (!sq) {
-        ok = mbar_wait_warp(smem_u32(aux + kQBar), 0);
-        if (!ok) (void)mbar_wait_warp(smem_u32(aux + kQBar), 0);  // drain before reuse
+        ok = mbar_wait_warp(smem_u32(qbar), 0);
+        if (!ok) (void)mbar_wait_warp(smem_u32(qbar), 0);  // drain before reuse
       }
-      const uint8_t* qraw = aux + kQOff;
       float4 qv[KS];
       float qmax = 0.f;
 #pragma unroll
@@ -1027,10 +1032,10 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   // query loads, in flight with the length and table reads (a fused step with rotation
   // reads its rotated queries from shared memory instead)
   const bool rope = STEP && p.positions != nullptr;
-  if (!rope) st.prefetch(p, b, h0, nh, lane, w, aux);
+  if (!rope) st.prefetch(p, b, h0, nh, lane, w, smem + Sm::qraw, smem + Sm::qbar);
   // the fused step's loads, raw bits, likewise issued before anything waits: thread t
   // holds query pairs t, t + kThreads, ... (pair (h, i) = elements i and i + D/2 of head
-  // h0 + h); warp 0 holds the new token's K and V rows, E = D/32 elements per lane
+  // h0 + h); the last warp holds the new token's K and V rows, E = D/32 elements per lane
   constexpr int QPT = STEP ? (kMaxHeads * (D / 2) + kThreads - 1) / kThreads : 1;
   constexpr int NE = D / 32;
   uint32_t qr[QPT][2], kr[NE], vr[NE];
@@ -1051,11 +1056,13 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
         }
       }
     }
+    // (the block's last warp takes the new row, so that its quantisation runs beside
+    // warp 0's query fragments rather than after them)
     const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D + lane * NE;
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
       kr[e] = vr[e] = 0u;
-      if (w == 0) {
+      if (w == kW - 1) {
         if (nb) {
           kr[e] = static_cast<const uint16_t*>(p.k_new)[src + e];
           vr[e] = static_cast<const uint16_t*>(p.v_new)[src + e];
@@ -1075,7 +1082,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   const int nsplit = len_ok ? max(1, (np - lo / kPage + p.chunk - 1) / p.chunk) : 1;
   if (split >= nsplit) {
     if constexpr (quantised(KVT)) {
-      if (!rope) st.drain_prefetch(aux, w);
+      if (!rope) st.drain_prefetch(smem + Sm::qbar, w);
     }
     return;
   }
@@ -1195,7 +1202,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     }
     patch = slot >= 0 && slot_ok && np > 0 && pe == np;
     t_new = (L - 1) & (kPage - 1);
-    if (patch && w == 0) {
+    if (patch && w == kW - 1) {
       constexpr int E = NE;  // lane l holds elements E l .. E l + E - 1
       const bool nb = p.new_dtype == kBF16;
       float kx[E], vx[E];
@@ -1301,12 +1308,15 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
         }
       }
     }
-    __syncthreads();  // rotated queries and the new row are ready
+    // rotated queries and the new row are ready (for the coded formats without rotation
+    // the block barrier after the query fragments below covers the new row)
+    if (rope || !quantised(KVT)) __syncthreads();
     if (rope) sq = sqw;  // (without rotation the queries load as in plain decode)
   }
 
   if constexpr (quantised(KVT)) {
-    if (!st.init(p, b, h0, nh, lane, aux, w, sq)) werr |= 0x10;  // PKV_DEV_TIMEOUT
+    if (!st.init(p, b, h0, nh, lane, aux, w, sq, smem + Sm::qraw, smem + Sm::qbar))
+      werr |= 0x10;  // PKV_DEV_TIMEOUT
     __syncthreads();  // warp 0 built the shared query fragments
   } else {
     st.init(p, b, h0, nh, lane, aux, w, sq);

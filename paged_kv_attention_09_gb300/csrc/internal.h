@@ -84,8 +84,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
 // ---------------------------------------------------------------- prefill
 struct PrefillPlan {
   int rows_per_cta;   // (token, head) rows per thread block
-  int n_row_tiles;    // grid.x
-  size_t ws_bytes;
+  int n_row_tiles;    // row tiles per (sequence, kv head)
+  int ksplit;         // blocks sharing a row tile's key range (1: no split)
+  size_t ws_bytes;    // workspace bytes (partials and tickets of a split; 0 otherwise)
 };
 
 struct PrefillArgs {
@@ -104,8 +105,9 @@ struct PrefillArgs {
 bool plan_prefill(const CacheView& c, int B, int Hq, int max_q_len, int MB, int q_dtype,
                   int device, PrefillPlan* plan);
 cudaError_t launch_prefill(const PrefillArgs& a, const PrefillPlan& plan, cudaStream_t st);
-// tcgen05 path (BF16 KV): query rows per block, and the launch over n_row_tiles blocks.
+// tcgen05 path (BF16 KV): query rows per block, and the launch over n_row_tiles x ksplit
+// blocks per (sequence, kv head).
 int prefill_tc_rows();
-cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, cudaStream_t st);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, int ksplit, cudaStream_t st);
 
 }  // namespace pkv

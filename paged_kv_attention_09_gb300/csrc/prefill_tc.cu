@@ -60,6 +60,13 @@ struct TParams {
   const int32_t* lens;
   float* out;
   int32_t* dev_status;
+  // key-range split: each row tile's key tiles are divided among ksplit blocks, which
+  // leave partial (max, sum, O) states in the workspace for the last of them to merge
+  int ksplit;
+  float* ws_o;      // [tile][split][row][D]
+  float* ws_m;      // [tile][split][row]
+  float* ws_l;      // [tile][split][row]
+  int* ws_ticket;   // [tile]
   int q_dtype, Hkv, Hq, G, MB, num_pages;
   int window;  // sliding window in tokens (0: none)
   float scale_log2;
@@ -98,6 +105,87 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col, int kext) {
   return ((((row >> 3) * (kext >> 3)) + (col >> 3)) << 7) + ((row & 7) << 4) + ((col & 7) << 1);
 }
 
+// Index of a row tile of the launch: [sequence][kv head][row tile].
+__device__ __forceinline__ int tile_index(const TParams& p, int tile, int g, int b) {
+  return (b * p.Hkv + g) * (gridDim.x / p.ksplit) + tile;
+}
+
+// Key-range split: the block that takes a row tile's last ticket (an atomic, no waiting)
+// merges the ksplit partial states of its 128 rows, in split order, into the output,
+// and resets the ticket.  `scratch`: ((ksplit + 1) x 128) floats of shared memory.
+template <int D>
+__device__ __noinline__ void split_merge(const TParams& p, int tile, int g, int b, int q0, int nrows,
+                                         int err, int tid, uint8_t* scratch) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  int* ticket = p.ws_ticket + tile_index(p, tile, g, b);
+  if (tid == 0) s_last = atomicAdd(ticket, 1) == p.ksplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int KS = p.ksplit;
+  const size_t base = static_cast<size_t>(tile_index(p, tile, g, b)) * KS * kRowsTC;
+  const int row0 = tile * kRowsTC;
+  float* wts = reinterpret_cast<float*>(scratch);  // [split][row], then [row] 1 / sum
+  if (tid < kRowsTC) {
+    const int r = tid;
+    float m[3], l[3];
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {  // every load in flight at once
+      m[s] = s < KS ? __ldcg(p.ws_m + base + s * kRowsTC + r) : -CUDART_INF_F;
+      l[s] = s < KS ? __ldcg(p.ws_l + base + s * kRowsTC + r) : 0.f;
+    }
+    const bool poisoned = isnan(m[0]) || isnan(m[1]) || isnan(m[2]);
+    const float M = fmaxf(fmaxf(m[0], m[1]), m[2]);
+    float L = 0.f;
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+      const float f = m[s] == -CUDART_INF_F ? 0.f : fast_exp2(m[s] - M);
+      if (s < KS) wts[s * kRowsTC + r] = f;
+      L += l[s] * f;
+    }
+    wts[KS * kRowsTC + r] = poisoned ? CUDART_NAN_F : 1.f / L;
+  }
+  __syncthreads();
+  if (!err) {
+    constexpr int D4 = D / 4;
+    constexpr int CH = 4;  // output chunks per thread and round: their loads go out together
+    for (int c0 = tid; c0 < kRowsTC * D4; c0 += CH * kThreadsTC) {
+      float4 v[CH][3];
+#pragma unroll
+      for (int u = 0; u < CH; ++u) {
+        const int c = c0 + u * kThreadsTC;
+        const int r = c / D4, d4 = c % D4;
+#pragma unroll
+        for (int s = 0; s < 3; ++s)
+          v[u][s] = c < kRowsTC * D4 && s < KS
+                        ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + (base + s * kRowsTC + r) * D) + d4)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < CH; ++u) {
+        const int c = c0 + u * kThreadsTC;
+        const int r = c / D4, d4 = c % D4;
+        const int rho = row0 + r;
+        if (c >= kRowsTC * D4 || rho >= nrows) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 3; ++s) {
+          if (s < KS) {
+            const float f = wts[s * kRowsTC + r];
+            acc.x += v[u][s].x * f; acc.y += v[u][s].y * f; acc.z += v[u][s].z * f; acc.w += v[u][s].w * f;
+          }
+        }
+        const float inv = wts[KS * kRowsTC + r];
+        float* dst = p.out + (static_cast<size_t>(q0 + rho / p.G) * p.Hq + g * p.G + rho % p.G) * D;
+        reinterpret_cast<float4*>(dst)[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      }
+    }
+  }
+  if (tid == 0) *ticket = 0;  // leave the counter ready for the next call
+}
+
 template <int D, bool QSPLIT>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     prefill_tc_kernel(const __grid_constant__ TParams p) {
@@ -120,7 +208,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y, b = blockIdx.z;
-  const int row0 = blockIdx.x * kRowsTC;
+  const int tile = blockIdx.x / p.ksplit, ks = blockIdx.x % p.ksplit;
+  const int row0 = tile * kRowsTC;
   const int q0 = p.qsl[b];
   const int Lq = p.qsl[b + 1] - q0;
   const int L = p.lens[b];
@@ -151,10 +240,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   }
   __syncthreads();
   err = s_err;
-  const int n_keys = err ? 0 : n_keys0;
-  const int kbase = err ? 0 : kb0;
-  const int n_pages = (n_keys - kbase + kPage - 1) / kPage;  // pages from kbase on
-  const int n_tiles = (n_keys - kbase + kKeysTC - 1) / kKeysTC;
+  // this block's share of the key tiles: [t0, t1) of the row tile's range from kb0
+  const int nt_all = err ? 0 : (n_keys0 - kb0 + kKeysTC - 1) / kKeysTC;
+  const int t0 = ks * nt_all / p.ksplit, t1 = (ks + 1) * nt_all / p.ksplit;
+  const int n_keys = err ? 0 : min(n_keys0, kb0 + t1 * kKeysTC);
+  const int kbase = err ? 0 : kb0 + t0 * kKeysTC;
+  const int n_pages = max(0, (n_keys - kbase + kPage - 1) / kPage);  // pages from kbase on
+  const int n_tiles = t1 - t0;
 
   // ---- set-up: TMEM, barriers, the query tile(s)
   if (warp == kSoftWarps) {
@@ -412,7 +504,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       tc::st_wait();
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       const int kz = min(kKeysTC, n_keys - key0);      // tile keys kz .. 63: past the end
-      const int hz = j == 0 ? lo_blk - kbase : 0;       // tile keys 0 .. hz - 1: before the window
+      const int hz = j == 0 && ks == 0 ? lo_blk - kbase : 0;  // tile keys 0 .. hz - 1: before the window
       if (kz < kKeysTC || hz > 0) {
         // keys no row may see: pages not loaded, page padding, or keys of the first page
         // before every row's window; they may hold anything (even NaN), so zero them in V
@@ -449,11 +541,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const float M = fmaxf(m_used, m_o);
       const float a_me = m_used == -CUDART_INF_F ? 0.f : fast_exp2(m_used - M);
       const float a_ot = m_o == -CUDART_INF_F ? 0.f : fast_exp2(m_o - M);
-      const float inv = 1.f / (l * a_me + l_o * a_ot);
+      const float lsum = l * a_me + l_o * a_ot;
+      // a split block leaves its unnormalised partial for the merge
+      const bool partial = p.ksplit > 1;
+      const float inv = partial ? 1.f : 1.f / lsum;
       const float wA = (grp == 0 ? a_me : a_ot) * inv, wB = (grp == 0 ? a_ot : a_me) * inv;
       const bool hasB = n_tiles > 1;  // group 1's accumulator holds data
-      float* dst = valid_row ? p.out + (static_cast<size_t>(q0 + rho / p.G) * p.Hq + g * p.G + rho % p.G) * D
-                             : nullptr;
+      const size_t pidx = (static_cast<size_t>(tile_index(p, tile, g, b)) * p.ksplit + ks) * kRowsTC + r;
+      float* dst = !valid_row ? nullptr
+                   : partial ? p.ws_o + pidx * D
+                             : p.out + (static_cast<size_t>(q0 + rho / p.G) * p.Hq + g * p.G + rho % p.G) * D;
+      if (partial && valid_row && grp == 0) {
+        p.ws_m[pidx] = M;
+        p.ws_l[pidx] = lsum;
+      }
       // group grp writes head_dim columns [grp D/2, (grp + 1) D/2) of its row
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -488,8 +589,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (err && valid_row) {
     float* dst = p.out + (static_cast<size_t>(q0 + rho / p.G) * p.Hq + g * p.G + rho % p.G) * D;
     for (int d = (D / 2) * hf; d < (D / 2) * (hf + 1); ++d) dst[d] = CUDART_NAN_F;
+    if (p.ksplit > 1 && hf == 0)  // a poisoned partial turns the merged row into NaN
+      p.ws_m[(static_cast<size_t>(tile_index(p, tile, g, b)) * p.ksplit + ks) * kRowsTC + r] = CUDART_NAN_F;
   }
   if (warp == kSoftWarps) tc::tmem_dealloc(tmem, Sm::tmemCols);
+  if (p.ksplit > 1) {
+    // a block with no key tiles (a short row range split more ways than it has tiles)
+    // leaves an empty partial
+    if (n_tiles == 0 && !err && valid_row && hf == 0) {
+      const size_t pidx = (static_cast<size_t>(tile_index(p, tile, g, b)) * p.ksplit + ks) * kRowsTC + r;
+      p.ws_m[pidx] = -CUDART_INF_F;
+      p.ws_l[pidx] = 0.f;
+      for (int d = 0; d < D; d += 4)
+        *reinterpret_cast<float4*>(p.ws_o + pidx * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    split_merge<D>(p, tile, g, b, q0, nrows, err, tid, smem + Sm::xch0);
+  }
 }
 
 template <int D, bool QSPLIT>
@@ -505,7 +620,7 @@ std::mutex g_tc_mu;
 
 int prefill_tc_rows() { return kRowsTC; }
 
-cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, cudaStream_t st) {
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, int ksplit, cudaStream_t st) {
   TParams p{};
   p.k = static_cast<const uint8_t*>(a.c.k);
   p.v = static_cast<const uint8_t*>(a.c.v);
@@ -548,7 +663,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, cudaStream_
       g_tc_attr[dev][slot] = true;
     }
   }
-  const dim3 grid(n_row_tiles, a.c.Hkv, a.B);
+  p.ksplit = ksplit;
+  if (ksplit > 1) {
+    const size_t tiles = static_cast<size_t>(n_row_tiles) * a.c.Hkv * a.B;
+    uint8_t* base = static_cast<uint8_t*>(a.ws);
+    p.ws_ticket = reinterpret_cast<int*>(base);
+    float* f = reinterpret_cast<float*>(base + ((tiles * 4 + 255) / 256) * 256);
+    const size_t rows = tiles * ksplit * kRowsTC;
+    p.ws_o = f;
+    p.ws_m = f + rows * a.c.D;
+    p.ws_l = p.ws_m + rows;
+  }
+  const dim3 grid(n_row_tiles * ksplit, a.c.Hkv, a.B);
   void* args[] = {&p};
   return cudaLaunchKernel(fn, grid, dim3(kThreadsTC), args, smem, st);
 }
