@@ -252,11 +252,31 @@ pkv_status pkv_decode_step_ex(const pkv_cache* cache, const void* q, int32_t q_d
                               const pkv_decode_opts* opts, int32_t* dev_status, void* stream);
 
 /*
- * Scratch bytes pkv_prefill_chunk_attn needs (host call, no launch); see above.
+ * Options of one prefill call (pkv_prefill_chunk_attn_ex, pkv_prefill_workspace_size_ex);
+ * a NULL pointer means every option at its default.
+ *   key_split  thread blocks that share the key range of one tile of 128 query rows
+ *              (each takes a contiguous share of its key tiles; the last of them to
+ *              finish merges their partial softmax states, through the workspace): 0
+ *              (default) chooses 1..3 from the shape and the device's SM count; otherwise
+ *              1, 2 or 3 (other values return PKV_ERR_SHAPE).  The split only reorders
+ *              floating-point sums.
+ */
+typedef struct pkv_prefill_opts {
+  int32_t key_split;
+} pkv_prefill_opts;
+
+/*
+ * Scratch bytes pkv_prefill_chunk_attn needs on the current device (host call, no
+ * launch), for either query type; see its workspace argument below.  The _ex form
+ * answers for the given options.
  */
 pkv_status pkv_prefill_workspace_size(const pkv_cache* cache, int32_t num_seqs,
                                       int32_t num_q_heads, int32_t max_q_len,
                                       int32_t max_blocks_per_seq, size_t* bytes);
+pkv_status pkv_prefill_workspace_size_ex(const pkv_cache* cache, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t max_q_len,
+                                         int32_t max_blocks_per_seq,
+                                         const pkv_prefill_opts* opts, size_t* bytes);
 
 /*
  * Chunked-prefill attention ("Tiny-LLM-Inference Project_Status": chunked prefill,
@@ -270,7 +290,8 @@ pkv_status pkv_prefill_workspace_size(const pkv_cache* cache, int32_t num_seqs,
  *                  context_lens[b] - Lq + i and attends to positions 0..that position
  *                  (with a cache window W: position - W + 1 .. position).
  *   out            float32 [total_q][num_q_heads][head_dim].
- *   workspace      as for decode (pkv_prefill_workspace_size bytes; may be 0).
+ *   workspace      as for decode (pkv_prefill_workspace_size bytes, which covers both
+ *                  query types; 0 when no row tile's keys are split).
  * The cache must be PKV_BF16 (other formats return PKV_ERR_UNSUPPORTED); the query tile
  * products run on the tcgen05 tensor cores.
  */
@@ -281,6 +302,16 @@ pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t
                                   const int32_t* context_lens, float scale, float* out,
                                   void* workspace, size_t workspace_bytes,
                                   int32_t* dev_status, void* stream);
+/* pkv_prefill_chunk_attn with options (see pkv_prefill_opts; size the workspace with
+ * pkv_prefill_workspace_size_ex and the same options). */
+pkv_status pkv_prefill_chunk_attn_ex(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                                     int32_t num_seqs, int32_t num_q_heads,
+                                     const int32_t* q_start_loc, int32_t max_q_len,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, float scale, float* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     const pkv_prefill_opts* opts, int32_t* dev_status,
+                                     void* stream);
 
 /*
  * Decode attention without caller-provided scratch.  (The pages describe no such

@@ -29,6 +29,8 @@ pkv_status check_decode_call(const pkv_cache* c, const void* q, int32_t q_dtype,
 
 // Split-K pages per block requested by the options (0: automatic); false if invalid.
 bool split_pages_of(const pkv_decode_opts* opts, int* pages);
+// The prefill options with defaults for NULL; false if a value is out of range.
+bool prefill_opts_of(const pkv_prefill_opts* opts, PrefillOpts* out);
 
 CacheView view(const pkv_cache* c);
 

@@ -59,6 +59,11 @@ bool split_pages_of(const pkv_decode_opts* opts, int* pages) {
   return *pages >= 0;
 }
 
+bool prefill_opts_of(const pkv_prefill_opts* opts, PrefillOpts* out) {
+  out->key_split = opts ? opts->key_split : 0;
+  return out->key_split >= 0 && out->key_split <= 3;
+}
+
 CacheView view(const pkv_cache* c) {
   return CacheView{c->k_cache, c->v_cache, c->k_scale, c->v_scale,
                    c->num_pages, c->num_kv_heads, c->head_dim, c->kv_dtype, c->window};
@@ -258,6 +263,14 @@ pkv_status pkv_decode_step(const pkv_cache* cache, const void* q, int32_t q_dtyp
 pkv_status pkv_prefill_workspace_size(const pkv_cache* cache, int32_t num_seqs,
                                       int32_t num_q_heads, int32_t max_q_len,
                                       int32_t max_blocks_per_seq, size_t* bytes) {
+  return pkv_prefill_workspace_size_ex(cache, num_seqs, num_q_heads, max_q_len,
+                                       max_blocks_per_seq, nullptr, bytes);
+}
+
+pkv_status pkv_prefill_workspace_size_ex(const pkv_cache* cache, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t max_q_len,
+                                         int32_t max_blocks_per_seq,
+                                         const pkv_prefill_opts* opts, size_t* bytes) {
   if (!bytes) return PKV_ERR_NULL;
   *bytes = 0;
   pkv_status s = check_cache(cache);
@@ -265,13 +278,20 @@ pkv_status pkv_prefill_workspace_size(const pkv_cache* cache, int32_t num_seqs,
   s = check_decode_shape(cache, num_seqs, num_q_heads, max_blocks_per_seq);
   if (s != PKV_OK) return s;
   if (max_q_len < 0) return PKV_ERR_SHAPE;
+  pkv::PrefillOpts o{};
+  if (!pkv::prefill_opts_of(opts, &o)) return PKV_ERR_SHAPE;
   int dev = 0;
   if ((s = current_device(&dev)) != PKV_OK) return s;
-  pkv::PrefillPlan plan{};
-  if (!pkv::plan_prefill(view(cache), num_seqs, num_q_heads, max_q_len, max_blocks_per_seq,
-                         PKV_BF16, dev, &plan))
-    return PKV_ERR_UNSUPPORTED;
-  *bytes = plan.ws_bytes;
+  // the split (hence the scratch) depends on the query type: cover both
+  size_t need = 0;
+  for (const int32_t qt : {PKV_BF16, PKV_F32}) {
+    pkv::PrefillPlan plan{};
+    if (!pkv::plan_prefill(view(cache), num_seqs, num_q_heads, max_q_len, max_blocks_per_seq, qt,
+                           dev, o, &plan))
+      return PKV_ERR_UNSUPPORTED;
+    if (plan.ws_bytes > need) need = plan.ws_bytes;
+  }
+  *bytes = need;
   return PKV_OK;
 }
 
@@ -282,6 +302,20 @@ pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t
                                   const int32_t* context_lens, float scale, float* out,
                                   void* workspace, size_t workspace_bytes,
                                   int32_t* dev_status, void* stream) {
+  return pkv_prefill_chunk_attn_ex(cache, q, q_dtype, num_seqs, num_q_heads, q_start_loc,
+                                   max_q_len, block_tables, max_blocks_per_seq, context_lens,
+                                   scale, out, workspace, workspace_bytes, nullptr, dev_status,
+                                   stream);
+}
+
+pkv_status pkv_prefill_chunk_attn_ex(const pkv_cache* cache, const void* q, int32_t q_dtype,
+                                     int32_t num_seqs, int32_t num_q_heads,
+                                     const int32_t* q_start_loc, int32_t max_q_len,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, float scale, float* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     const pkv_prefill_opts* opts, int32_t* dev_status,
+                                     void* stream) {
   PKV_RANGE("pkv_prefill_chunk_attn");
   pkv_status s = check_cache(cache);
   if (s != PKV_OK) return s;
@@ -289,6 +323,8 @@ pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t
   if (s != PKV_OK) return s;
   if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_DTYPE;
   if (max_q_len < 0) return PKV_ERR_SHAPE;
+  pkv::PrefillOpts o{};
+  if (!pkv::prefill_opts_of(opts, &o)) return PKV_ERR_SHAPE;
   if (num_seqs == 0 || max_q_len == 0) return PKV_OK;
   if (!q || !q_start_loc || !block_tables || !context_lens || !out) return PKV_ERR_NULL;
   if (!aligned16(q) || !aligned16(out) || !aligned4(q_start_loc) || !aligned4(block_tables) ||
@@ -299,7 +335,7 @@ pkv_status pkv_prefill_chunk_attn(const pkv_cache* cache, const void* q, int32_t
   if ((s = current_device(&dev)) != PKV_OK) return s;
   pkv::PrefillPlan plan{};
   if (!pkv::plan_prefill(view(cache), num_seqs, num_q_heads, max_q_len, max_blocks_per_seq,
-                         q_dtype, dev, &plan))
+                         q_dtype, dev, o, &plan))
     return PKV_ERR_UNSUPPORTED;
   if (plan.n_row_tiles > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
   if (plan.ws_bytes > 0) {

@@ -921,6 +921,11 @@ __device__ __noinline__ void cluster_merge(const DParams& p, const float* part, 
                                            int h0, int nh, int tid, int lane, int w,
                                            uint32_t* s_done, uint64_t* s_release, int* s_last) {
   constexpr int kW = kThreads / 32;
+  // parameters read once into registers: this function is not inlined, so each use of p
+  // would be a load through a generic pointer, repeated after every store
+  float* const out = p.out;
+  int32_t* const dev_status = p.dev_status;
+  const int Hq = p.Hq;
   __syncthreads();        // this block's partial is complete
   cluster_wait_acquire();  // every block's barrier and counter are initialised
   if (tid == 0) {
@@ -930,8 +935,8 @@ __device__ __noinline__ void cluster_merge(const DParams& p, const float* part, 
   }
   __syncthreads();
   if (!*s_last) {
-    if (tid == 0 && !mbar_wait(s_release, 0) && p.dev_status)
-      atomicOr(p.dev_status, 0x10);  // PKV_DEV_TIMEOUT
+    if (tid == 0 && !mbar_wait(s_release, 0) && dev_status)
+      atomicOr(dev_status, 0x10);  // PKV_DEV_TIMEOUT
     return;
   }
   fence_acq_rel_cluster();  // the other blocks' partials are visible
@@ -956,7 +961,7 @@ __device__ __noinline__ void cluster_merge(const DParams& p, const float* part, 
   }
   __syncthreads();
   constexpr int D4 = D / 4;
-  const size_t row0 = static_cast<size_t>(b) * p.Hq + h0;
+  const size_t row0 = static_cast<size_t>(b) * Hq + h0;
   for (int c = tid; c < nh * D4; c += kThreads) {
     const int r = c / D4;
     const uint32_t src = part_u32 + 4 * (2 * kMaxHeads + r * D) + 16 * (c % D4);
@@ -973,7 +978,7 @@ __device__ __noinline__ void cluster_merge(const DParams& p, const float* part, 
       }
     }
     const float inv = wts[8 * kMaxHeads + r];
-    *reinterpret_cast<float4*>(p.out + (row0 + r) * D + 4 * (c % D4)) =
+    *reinterpret_cast<float4*>(out + (row0 + r) * D + 4 * (c % D4)) =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
   __syncthreads();  // every read of another block's shared memory is done

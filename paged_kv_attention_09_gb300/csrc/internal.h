@@ -102,12 +102,17 @@ struct PrefillArgs {
   int32_t* dev_status;
 };
 
+// key_split: 0 automatic, else 1..3
+struct PrefillOpts {
+  int key_split;
+};
 bool plan_prefill(const CacheView& c, int B, int Hq, int max_q_len, int MB, int q_dtype,
-                  int device, PrefillPlan* plan);
+                  int device, const PrefillOpts& opts, PrefillPlan* plan);
 cudaError_t launch_prefill(const PrefillArgs& a, const PrefillPlan& plan, cudaStream_t st);
-// tcgen05 path (BF16 KV): query rows per block, and the launch over n_row_tiles x ksplit
-// blocks per (sequence, kv head).
+// tcgen05 path (BF16 KV): query rows per block, blocks resident per SM for a query dtype,
+// and the launch over n_row_tiles x ksplit blocks per (sequence, kv head).
 int prefill_tc_rows();
+int prefill_tc_blocks_per_sm(int q_dtype);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, int ksplit, cudaStream_t st);
 
 }  // namespace pkv

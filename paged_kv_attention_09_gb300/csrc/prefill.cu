@@ -32,8 +32,8 @@ int sm_count(int device) {
 }  // namespace
 
 bool plan_prefill(const CacheView& c, int B, int Hq, int max_q_len, int MB, int q_dtype,
-                  int device, PrefillPlan* plan) {
-  (void)MB; (void)q_dtype;
+                  int device, const PrefillOpts& opts, PrefillPlan* plan) {
+  (void)MB;
   if (c.dtype != kBF16) return false;
   if (c.D != 64 && c.D != 128) return false;
   const int G = Hq / c.Hkv;
@@ -43,13 +43,17 @@ bool plan_prefill(const CacheView& c, int B, int Hq, int max_q_len, int MB, int 
   // Key-range split: when the row tiles leave SMs idle (one block per SM: the kernel takes
   // all of an SM's tensor memory), up to 3 blocks share a row tile's keys, as many as keep
   // the launch in one wave; their partial states are merged by the last of them.  (A split
-  // into a second wave measured slower than none: 67 us against 38 us on the mixed
-  // workload's 96 tiles.)
+  // into a second wave measured slower than none.)
   const int sms = sm_count(device);
   if (sms <= 0) return false;
+  const long long slots = static_cast<long long>(sms) * prefill_tc_blocks_per_sm(q_dtype);
   const long long tiles = static_cast<long long>(plan->n_row_tiles) * c.Hkv * B;
   int best = 1;
-  while (best < 3 && tiles > 0 && tiles * (best + 1) <= sms) ++best;
+  if (opts.key_split > 0) {
+    best = opts.key_split;
+  } else {
+    while (best < 3 && tiles > 0 && tiles * (best + 1) <= slots) ++best;
+  }
   if (tiles * best > 0x7fffffffLL / 2) best = 1;
   plan->ksplit = best;
   plan->ws_bytes = 0;

@@ -117,15 +117,22 @@ template <int D>
 __device__ __noinline__ void split_merge(const TParams& p, int tile, int g, int b, int q0, int nrows,
                                          int err, int tid, uint8_t* scratch) {
   __shared__ int s_last;
+  // The parameters are read once into registers: this function is not inlined, so each
+  // use of p would be a load through a generic pointer, repeated after every store.
+  const int KS = p.ksplit, G = p.G, Hq = p.Hq;
+  float* const out = p.out;
+  const float* const ws_o = p.ws_o;
+  const float* const ws_m = p.ws_m;
+  const float* const ws_l = p.ws_l;
+  const int tix = tile_index(p, tile, g, b);
   __threadfence();
   __syncthreads();
-  int* ticket = p.ws_ticket + tile_index(p, tile, g, b);
-  if (tid == 0) s_last = atomicAdd(ticket, 1) == p.ksplit - 1;
+  int* ticket = p.ws_ticket + tix;
+  if (tid == 0) s_last = atomicAdd(ticket, 1) == KS - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int KS = p.ksplit;
-  const size_t base = static_cast<size_t>(tile_index(p, tile, g, b)) * KS * kRowsTC;
+  const size_t base = static_cast<size_t>(tix) * KS * kRowsTC;
   const int row0 = tile * kRowsTC;
   float* wts = reinterpret_cast<float*>(scratch);  // [split][row], then [row] 1 / sum
   if (tid < kRowsTC) {
@@ -133,8 +140,8 @@ __device__ __noinline__ void split_merge(const TParams& p, int tile, int g, int 
     float m[3], l[3];
 #pragma unroll
     for (int s = 0; s < 3; ++s) {  // every load in flight at once
-      m[s] = s < KS ? __ldcg(p.ws_m + base + s * kRowsTC + r) : -CUDART_INF_F;
-      l[s] = s < KS ? __ldcg(p.ws_l + base + s * kRowsTC + r) : 0.f;
+      m[s] = s < KS ? __ldcg(ws_m + base + s * kRowsTC + r) : -CUDART_INF_F;
+      l[s] = s < KS ? __ldcg(ws_l + base + s * kRowsTC + r) : 0.f;
     }
     const bool poisoned = isnan(m[0]) || isnan(m[1]) || isnan(m[2]);
     const float M = fmaxf(fmaxf(m[0], m[1]), m[2]);
@@ -160,7 +167,7 @@ __device__ __noinline__ void split_merge(const TParams& p, int tile, int g, int 
 #pragma unroll
         for (int s = 0; s < 3; ++s)
           v[u][s] = c < kRowsTC * D4 && s < KS
-                        ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + (base + s * kRowsTC + r) * D) + d4)
+                        ? __ldcg(reinterpret_cast<const float4*>(ws_o + (base + s * kRowsTC + r) * D) + d4)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
@@ -178,7 +185,7 @@ __device__ __noinline__ void split_merge(const TParams& p, int tile, int g, int 
           }
         }
         const float inv = wts[KS * kRowsTC + r];
-        float* dst = p.out + (static_cast<size_t>(q0 + rho / p.G) * p.Hq + g * p.G + rho % p.G) * D;
+        float* dst = out + (static_cast<size_t>(q0 + rho / G) * Hq + g * G + rho % G) * D;
         reinterpret_cast<float4*>(dst)[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       }
     }
@@ -619,6 +626,11 @@ std::mutex g_tc_mu;
 }  // namespace
 
 int prefill_tc_rows() { return kRowsTC; }
+
+int prefill_tc_blocks_per_sm(int q_dtype) {
+  (void)q_dtype;
+  return 1;  // the kernel takes all of an SM's tensor memory
+}
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, int ksplit, cudaStream_t st) {
   TParams p{};

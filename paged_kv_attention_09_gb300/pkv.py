@@ -29,6 +29,7 @@ STATUS = {0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_DTYPE"
 EXPORTS = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn", "pkv_decode_step",
            "pkv_decode_workspace_size_ex", "pkv_decode_attn_ex", "pkv_decode_step_ex",
            "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn",
+           "pkv_prefill_workspace_size_ex", "pkv_prefill_chunk_attn_ex",
            "pkv_decode_attn_noalloc", "pkv_decode_attn_noalloc_ex", "pkv_status_string",
            "pkv_decode_graph_workspace_size", "pkv_decode_graph_create",
            "pkv_decode_graph_launch", "pkv_decode_graph_bucket", "pkv_decode_graph_destroy")
@@ -52,6 +53,10 @@ class pkv_cache(ctypes.Structure):
 
 class pkv_decode_opts(ctypes.Structure):
     _fields_ = [("split_pages", ctypes.c_int32)]
+
+
+class pkv_prefill_opts(ctypes.Structure):
+    _fields_ = [("key_split", ctypes.c_int32)]
 
 
 class pkv_graph_layer(ctypes.Structure):
@@ -104,9 +109,14 @@ def bind(path: str):
     lib.pkv_prefill_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.pkv_prefill_chunk_attn.argtypes = [C, P, I32, I32, I32, P, I32, P, I32, P, F, P, P, SZ,
                                            P, P]
+    PO = ctypes.POINTER(pkv_prefill_opts)
+    lib.pkv_prefill_workspace_size_ex.argtypes = [C, I32, I32, I32, I32, PO, ctypes.POINTER(SZ)]
+    lib.pkv_prefill_chunk_attn_ex.argtypes = [C, P, I32, I32, I32, P, I32, P, I32, P, F, P, P,
+                                              SZ, PO, P, P]
     for fn in ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attn", "pkv_decode_step",
                "pkv_decode_workspace_size_ex", "pkv_decode_attn_ex", "pkv_decode_step_ex",
-               "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn"):
+               "pkv_prefill_workspace_size", "pkv_prefill_chunk_attn",
+               "pkv_prefill_workspace_size_ex", "pkv_prefill_chunk_attn_ex"):
         getattr(lib, fn).restype = ctypes.c_int
     lib.pkv_decode_attn_noalloc.argtypes = [C, P, I32, I32, I32, P, I32, P, F, P, P, P]
     lib.pkv_decode_attn_noalloc.restype = ctypes.c_int
@@ -354,12 +364,21 @@ def pkv_decode_attn_noalloc(cache: KVCache, q: torch.Tensor, block_tables: torch
            "pkv_decode_attn_noalloc")
 
 
+def _prefill_opts(key_split: int):
+    """The options argument of the prefill _ex calls (None: every option at its default)."""
+    return None if not key_split else ctypes.byref(pkv_prefill_opts(int(key_split)))
+
+
 def pkv_prefill_workspace_size(cache: KVCache, num_seqs: int, num_q_heads: int,
-                               max_q_len: int, max_blocks_per_seq: int) -> int:
+                               max_q_len: int, max_blocks_per_seq: int,
+                               key_split: int = 0) -> int:
+    """Scratch bytes of pkv_prefill_chunk_attn; key_split (0: automatic, 1..3) is the
+    pkv_prefill_opts option."""
     c = cache.struct()
     n = ctypes.c_size_t(0)
-    _check(load().pkv_prefill_workspace_size(ctypes.byref(c), num_seqs, num_q_heads, max_q_len,
-                                             max_blocks_per_seq, ctypes.byref(n)),
+    _check(load().pkv_prefill_workspace_size_ex(ctypes.byref(c), num_seqs, num_q_heads,
+                                                max_q_len, max_blocks_per_seq,
+                                                _prefill_opts(key_split), ctypes.byref(n)),
            "pkv_prefill_workspace_size")
     return int(n.value)
 
@@ -368,16 +387,19 @@ def pkv_prefill_chunk_attn(cache: KVCache, q: torch.Tensor, q_start_loc: torch.T
                            max_q_len: int, block_tables: torch.Tensor,
                            context_lens: torch.Tensor, scale: float, out: torch.Tensor,
                            workspace: Optional[torch.Tensor] = None,
-                           dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+                           dev_status: Optional[torch.Tensor] = None, stream=None,
+                           key_split: int = 0) -> None:
     c = cache.struct()
     B = int(context_lens.shape[0])
     Hq = int(q.shape[1])
     wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pkv_prefill_chunk_attn(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
-                                         _ptr(q_start_loc), int(max_q_len), _ptr(block_tables),
-                                         int(block_tables.shape[1]), _ptr(context_lens),
-                                         float(scale), _ptr(out), _ptr(workspace), wb,
-                                         _ptr(dev_status), _stream(stream)),
+    _check(load().pkv_prefill_chunk_attn_ex(ctypes.byref(c), _ptr(q), _CODE[q.dtype], B, Hq,
+                                            _ptr(q_start_loc), int(max_q_len),
+                                            _ptr(block_tables), int(block_tables.shape[1]),
+                                            _ptr(context_lens), float(scale), _ptr(out),
+                                            _ptr(workspace), wb,
+                                            _prefill_opts(key_split), _ptr(dev_status),
+                                            _stream(stream)),
            "pkv_prefill_chunk_attn")
 
 

@@ -45,12 +45,15 @@ class DeviceWorkload:
     batches: list
     dev_status: torch.Tensor
     split_pages: int = 0  # decode split-K pages per block (0: automatic)
+    key_split: int = 0    # prefill blocks per row tile's keys (0: automatic)
 
 
 def upload(wl: Workload, device="cuda", cache_fill: Optional[float] = None,
-           fill_history: bool = True, split_pages: int = 0) -> DeviceWorkload:
+           fill_history: bool = True, split_pages: int = 0,
+           key_split: int = 0) -> DeviceWorkload:
     """Allocate the cache and batch tensors; optionally append the history rows.
-    ``split_pages``: the decode calls' split-K pages per block (0: automatic)."""
+    ``split_pages``: the decode calls' split-K pages per block (0: automatic);
+    ``key_split``: the prefill calls' option (pkv_prefill_opts)."""
     cache = pkv.KVCache.allocate(wl.num_pages, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, device)
     if cache_fill is not None:  # sentinel for never-written slots (NaN poisons padding)
         if wl.kv_dtype in pkv.CODED:
@@ -76,12 +79,14 @@ def upload(wl: Workload, device="cuda", cache_fill: Optional[float] = None,
         if b.kind == "decode":
             nbytes = pkv.pkv_decode_workspace_size(cache, B, Hq, b.max_blocks, split_pages)
         else:
-            nbytes = pkv.pkv_prefill_workspace_size(cache, B, Hq, max_q, b.max_blocks)
+            nbytes = pkv.pkv_prefill_workspace_size(cache, B, Hq, max_q, b.max_blocks,
+                                                    key_split)
         batches.append(DeviceBatch(b.kind, q, torch.from_numpy(b.block_tables).to(device),
                                    torch.from_numpy(b.context_lens).to(device), qsl, max_q, out,
                                    pkv.workspace_for(nbytes, device)))
     dw = DeviceWorkload(wl, cache, k_src, v_src, slots, step_rows, batches,
-                        torch.zeros(1, dtype=torch.int32, device=device), split_pages)
+                        torch.zeros(1, dtype=torch.int32, device=device), split_pages,
+                        key_split)
     if fill_history:
         hist = torch.from_numpy(wl.history_rows).to(device)
         append_rows(dw, hist)
@@ -103,7 +108,7 @@ def run_batch(dw: DeviceWorkload, i: int, stream=None) -> torch.Tensor:
     else:
         pkv.pkv_prefill_chunk_attn(dw.cache, b.q, b.q_start_loc, b.max_q_len, b.block_tables,
                                    b.context_lens, dw.wl.scale, b.out, b.workspace,
-                                   dw.dev_status, stream)
+                                   dw.dev_status, stream, key_split=dw.key_split)
     return b.out
 
 

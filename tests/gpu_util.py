@@ -22,10 +22,12 @@ def oracle_outputs(wl, oc=None, seqs=None):
     return outs
 
 
-def gpu_outputs(wl, cache_fill=None, chunk_pages=0):
+def gpu_outputs(wl, cache_fill=None, chunk_pages=0, key_split=0):
     """One step of the workload through the library (chunk_pages: the decode calls'
-    split-K pages per block, 0 = automatic); outputs, device status, device workload."""
-    dw = runner.upload(wl, "cuda", cache_fill=cache_fill, split_pages=chunk_pages)
+    split-K pages per block, 0 = automatic; key_split: the prefill calls' option);
+    outputs, device status, device workload."""
+    dw = runner.upload(wl, "cuda", cache_fill=cache_fill, split_pages=chunk_pages,
+                       key_split=key_split)
     outs = runner.run_step(dw)
     torch.cuda.synchronize()
     status = int(dw.dev_status.item())

@@ -95,6 +95,19 @@ def test_decode_and_prefill_validation(lib):
     assert lib.pkv_decode_workspace_size(ctypes.byref(c), 2, 4, 4, None) == 1
 
 
+@pytest.mark.parametrize("key_split", [4, -1])
+def test_prefill_options_out_of_range(lib, key_split):
+    """pkv_prefill_opts.key_split outside 0..3: PKV_ERR_SHAPE from both prefill _ex calls,
+    before any device work."""
+    c = _cache()
+    P = None
+    n = ctypes.c_size_t(0)
+    o = ctypes.byref(pkv.pkv_prefill_opts(key_split))
+    assert lib.pkv_prefill_workspace_size_ex(ctypes.byref(c), 2, 4, 8, 4, o, ctypes.byref(n)) == 2
+    assert lib.pkv_prefill_chunk_attn_ex(ctypes.byref(c), 0x80000, pkv.BF16, 2, 4, 0xC0000, 8,
+                                         0x90000, 4, 0xA0000, 0.1, 0xB0000, P, 0, o, P, P) == 2
+
+
 def test_no_device_is_reported_not_crashed(lib):
     import torch
     if torch.cuda.is_available():

@@ -55,6 +55,45 @@ def test_prefill_bad_inputs_give_nan_rows_and_status():
     assert np.all(np.isfinite(got[0][20:30]))
 
 
+# Long chunks over long contexts so that every split has several key tiles, plus a short
+# chunk (one row tile) whose last split gets few or no key tiles.
+SPLIT_CHUNKS = [(700, 300), (1500, 64), (0, 260), (30, 5)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,qd", [(12, 2, 128, W.BF16), (8, 2, 64, W.F32)])
+def test_prefill_every_key_split(Hq, Hkv, D, qd):
+    """Each key split (1, 2, 3 blocks per row tile, merged through the workspace by the
+    last of them) within tolerance of the oracle, and equal to the unsplit result up to
+    float rounding."""
+    wl = W.small_workload(3200 + D, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                          kv_dtype=W.BF16, q_dtype=qd, prefill=SPLIT_CHUNKS)
+    ref = oracle_outputs(wl)[0]
+    got = {}
+    for key_split in (1, 2, 3):
+        out, status, dw = gpu_outputs(wl, key_split=key_split)
+        assert status == 0
+        assert (dw.batches[0].workspace is None) == (key_split == 1)
+        assert np.all(np.isfinite(out[0]))
+        assert max_err(out[0], ref) <= 2e-3, key_split
+        got[key_split] = out[0]
+    assert max_err(got[2], got[1]) <= 1e-5 and max_err(got[3], got[1]) <= 1e-5
+
+
+def test_prefill_split_bad_inputs_give_nan_rows():
+    """A device-side error in a split row tile turns exactly its sequence's rows into NaN,
+    through the merge too."""
+    wl = W.small_workload(3210, num_q_heads=8, num_kv_heads=2, head_dim=64, kv_dtype=W.BF16,
+                          q_dtype=W.BF16, prefill=[(600, 40), (600, 40), (600, 40)])
+    b = wl.batches[0]
+    b.block_tables[0, 30] = -5                 # bad page inside the first sequence's range
+    b.context_lens[1] = 5                      # chunk (40) longer than the context
+    got, status, _ = gpu_outputs(wl, key_split=3)
+    assert status & pkv.DEV_BAD_PAGE and status & pkv.DEV_BAD_CHUNK
+    assert np.all(np.isnan(got[0][0:80]))
+    ref = oracle_outputs(wl, seqs=[2])[0]
+    assert max_err(got[0][80:120], ref[80:120]) <= 2e-3
+
+
 def test_prefill_lq1_matches_decode():
     """A one-token chunk is a decode step: both kernels must agree within tolerance."""
     wl = W.small_workload(3102, num_q_heads=12, num_kv_heads=2, head_dim=128, kv_dtype=W.BF16,
