@@ -489,19 +489,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // every probability is 0, not exp2(-inf + inf))
       const float nm = m_used == -CUDART_INF_F ? 0.f : -m_used;
       const uint32_t tP = tmem + lane_base + Sm::pCol + kKeysTC * grp;
-      float ls[4];
+      float2 ls[2];
+      const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(nm, nm);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {  // keys 32 hh .. 32 hh + 31 -> P columns 16 hh ..
         uint32_t h[16], lo[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const float a = fast_exp2(fmaf(s[32 * hh + 2 * u], sl, nm));
-          const float e = fast_exp2(fmaf(s[32 * hh + 2 * u + 1], sl, nm));
-          if ((u & 7) == 0) ls[2 * hh + (u >> 3)] = a + e;
-          else ls[2 * hh + (u >> 3)] += a + e;
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(a, e);
+          const float2 x = __ffma2_rn(make_float2(s[32 * hh + 2 * u], s[32 * hh + 2 * u + 1]), sl2, nm2);
+          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          if (u == 0) ls[hh] = pe;
+          else ls[hh] = __fadd2_rn(ls[hh], pe);
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(pe.x, pe.y);
           const float2 hf2 = __bfloat1622float2(hv);
-          const __nv_bfloat162 lv = __floats2bfloat162_rn(a - hf2.x, e - hf2.y);
+          const float2 r2 = __fadd2_rn(pe, make_float2(-hf2.x, -hf2.y));
+          const __nv_bfloat162 lv = __floats2bfloat162_rn(r2.x, r2.y);
           h[u] = *reinterpret_cast<const uint32_t*>(&hv);
           lo[u] = *reinterpret_cast<const uint32_t*>(&lv);
         }
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         tc::st16_nowait(tP + 32 + 16 * hh, lo);
       }
       tc::st_wait();
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
       const int kz = min(kKeysTC, n_keys - key0);      // tile keys kz .. 63: past the end
       const int hz = j == 0 && ks == 0 ? lo_blk - kbase : 0;  // tile keys 0 .. hz - 1: before the window
       if (kz < kKeysTC || hz > 0) {
