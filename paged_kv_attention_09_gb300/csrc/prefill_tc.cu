@@ -51,6 +51,14 @@ constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kThreadsTC = (kSoftWarps + 4) * 32;  // + two MMA issuers, K and V producers
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only beyond this margin
 
+#ifdef PKV_TEST_HOOKS
+// Test builds only: when set, each softmax group's first wait for scores gives up at once
+// (as a wait that ran out would), so that the timeout path runs: the other roles' waits
+// then run out on their own limits, every copy and product still drains, and the call
+// reports PKV_DEV_TIMEOUT with NaN rows.
+__device__ int g_test_prefill_fail_first_wait = 0;
+#endif
+
 struct TParams {
   const uint8_t* k;
   const uint8_t* v;
@@ -433,6 +441,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     for (int j = grp; j < n_tiles; j += 2, ++n_mine) {
       const int k = j >> 1;  // this group's k-th tile
       ok = mbar_wait(&s_full[0], k & 1) && !*abort_flag;  // the scores of pair k
+#ifdef PKV_TEST_HOOKS
+      if (k == 0 && g_test_prefill_fail_first_wait) ok = false;  // a wait that gives up
+#endif
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc::fence_after_sync();
       float s[64];
@@ -694,3 +705,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, int n_row_tiles, int ksplit,
 }
 
 }  // namespace pkv
+
+#ifdef PKV_TEST_HOOKS
+// Test builds only: switches the give-up-at-once first score wait (see above) on or off.
+extern "C" int pkv_test_prefill_fail_first_wait(int on) {
+  return cudaMemcpyToSymbol(pkv::g_test_prefill_fail_first_wait, &on, sizeof(int)) == cudaSuccess ? 0 : 1;
+}
+#endif

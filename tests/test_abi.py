@@ -194,3 +194,4 @@ def test_decode_entry_points_validate_alike(lib):
 def test_product_library_has_no_test_hooks(lib):
     """The give-up-at-once wait used by the timeout test exists only in test builds."""
     assert not hasattr(lib, "pkv_test_fail_first_wait")
+    assert not hasattr(lib, "pkv_test_prefill_fail_first_wait")
