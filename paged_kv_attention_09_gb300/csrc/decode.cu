@@ -1123,32 +1123,43 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   };
   int ids_cur = check_id(lane, raw_first), ids_nxt = load_ids(1);
 
-  // ---- copy issue: lane l < NK issues one copy of the iteration's page (K block, V
-  // block, and for the coded formats the two scale vectors), so a whole stage costs one
-  // warp instruction; lane 0 posts the byte count.  The lane's source base, page stride
-  // and destination are computed once.
-  constexpr int NK = quantised(KVT) ? 4 : 2;
-  const int ck = lane < NK ? lane : 0;
-  const uint32_t c_bytes = ck < 2 ? static_cast<uint32_t>(Lo::kBytes) : static_cast<uint32_t>(Lo::sBytes);
-  const uint32_t c_dst = smem_u32(my_stages) +
-                         (ck == 0 ? 0u : ck == 1 ? static_cast<uint32_t>(Lo::kBytes)
-                                                 : static_cast<uint32_t>(2 * Lo::kBytes + (ck - 2) * Lo::sBytes));
-  const uint8_t* c_src = (ck == 0 ? p.k : ck == 1 ? p.v
-                          : reinterpret_cast<const uint8_t*>(ck == 2 ? p.ks : p.vs)) +
-                         static_cast<size_t>(g) * c_bytes;
+  // ---- copy issue: lanes 0 and 1 issue one bulk copy each of the iteration's page (K
+  // block, V block), so a whole stage costs one warp instruction; lane 0 posts the byte
+  // count.  The coded formats' two 64-byte scale vectors come by per-thread 16-byte async
+  // copies of lanes 8..15, whose completion arrives on the same stage barrier: the
+  // bulk-copy engine then handles two copies per page instead of four (at the start of a
+  // launch, 28 warps of an SM request 3 stages each at once).  The lane's source base,
+  // page stride and destination are computed once.
+  constexpr int kScaleLanes = quantised(KVT) ? 8 : 0;
+  const int ck = lane < 2 ? lane : 0;
+  constexpr uint32_t c_bytes = static_cast<uint32_t>(Lo::kBytes);
+  const uint32_t c_dst = smem_u32(my_stages) + (ck == 0 ? 0u : c_bytes);
+  const uint8_t* c_src = (ck == 0 ? p.k : p.v) + static_cast<size_t>(g) * c_bytes;
   const uint32_t c_stride = static_cast<uint32_t>(p.Hkv) * c_bytes;  // from one page to the next
+  const int sl = lane - 8;  // scale lanes: sl / 4 = K or V vector, sl % 4 = 16-byte piece
+  const bool s_lane = kScaleLanes > 0 && sl >= 0 && sl < kScaleLanes;
+  const uint32_t s_dst = smem_u32(my_stages) + 2 * c_bytes +
+                         (s_lane ? static_cast<uint32_t>((sl >> 2) * Lo::sBytes + (sl & 3) * 16) : 0u);
+  const float* s_src = s_lane ? (sl >> 2 ? p.vs : p.ks) + static_cast<size_t>(g) * kPage + (sl & 3) * 4 : nullptr;
+  const size_t s_stride = static_cast<size_t>(p.Hkv) * kPage;  // floats from one page to the next
   const uint32_t bar0 = smem_u32(my_bars);
   const uint64_t pol = l2_evict_first_policy();  // streamed once: keep L2 for others
   auto issue = [&](int i, int stage) {
     const uint32_t pid = static_cast<uint32_t>(__shfl_sync(0xffffffffu, ids_cur, i & 31));
     const uint32_t bar = bar0 + 8 * stage;
-    mbar_arrive_expect_tx_if(lane == 0, bar, static_cast<uint32_t>(Lo::pageBytes));
-    bulk_g2s_if(lane < NK, c_dst + stage * Lo::stageBytes, c_src + static_cast<size_t>(pid) * c_stride,
+    mbar_arrive_expect_tx_if(lane == 0, bar, 2 * c_bytes);
+    bulk_g2s_if(lane < 2, c_dst + stage * Lo::stageBytes, c_src + static_cast<size_t>(pid) * c_stride,
                 c_bytes, bar, pol);
+    if (s_lane) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s_dst + stage * Lo::stageBytes),
+                   "l"(s_src + static_cast<size_t>(pid) * s_stride) : "memory");
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(bar) : "memory");
+    }
   };
   if (n_my > 0) {
     if (lane == 0) {
-      for (int i = 0; i < S; ++i) mbar_init(&my_bars[i], 1);
+      // one arrival with the bulk bytes, plus one per scale lane when its copy lands
+      for (int i = 0; i < S; ++i) mbar_init(&my_bars[i], 1 + kScaleLanes);
       fence_barrier_init();
     }
     __syncwarp();
