@@ -111,11 +111,16 @@ struct RowBytes {
 #ifndef PKV_BF16_STAGES
 #define PKV_BF16_STAGES 2
 #endif
+// (FP32, head_dim 64: 2 stages measured faster than 3, 15.2 against 16.0 us on the
+// SmolLM2-shaped workload; 4 cost a block per SM)
+#ifndef PKV_F32_STAGES
+#define PKV_F32_STAGES 2
+#endif
 template <int KVT, int D>
 struct Tune {
   static constexpr int S = quantised(KVT) ? PKV_INT8_STAGES
                          : KVT == kBF16 ? (D == 64 ? 3 : PKV_BF16_STAGES)
-                                        : (D == 64 ? 3 : 2);
+                                        : (D == 64 ? PKV_F32_STAGES : 2);
   // Warps per block.  (Three-warp INT8 blocks, which leave 96 registers at 7 blocks per
   // SM, measured slower than four warps at 72 registers.)
   static constexpr int W = 4;
