@@ -28,9 +28,9 @@
 //             f16 values 1152 + code with two byte permutes per 4 codes; the bias is removed
 //             afterwards: 1152 * sum(q) from each score, 1152 * sum(P) from the output.
 //             FP8 (E4M3) and INT4 KV take the same path: E4M3 codes convert to their exact
-//             f16 values (no bias), INT4 codes to (24 + code) / 16 with a shift and a
-//             mask-and-xor per pair (the TinyInfer review, item 2; "tinyloop Current
-//             Status", KV cache modes table).
+//             f16 values (no bias), INT4 codes to (8 + code) / 8 through the hardware
+//             FP6 (E2M3) conversion after one mask-and-xor per 4 codes (the TinyInfer
+//             review, item 2; "tinyloop Current Status", KV cache modes table).
 //             Queries are scaled by a power of two into [0.5, 1) and split hi/lo in f16
 //             (rows 0-7 / 8-15); per-token K scales multiply the scores and V scales the
 //             probabilities (split hi/lo) in FP32.  (The s8 MMA path is far slower on
@@ -179,6 +179,12 @@ __device__ __forceinline__ float4 load_q4(const void* q, int q_dtype, size_t i) 
   }
   return *reinterpret_cast<const float4*>(static_cast<const float*>(q) + i);
 }
+__device__ __forceinline__ float2 load_q2(const void* q, int q_dtype, size_t i) {
+  if (q_dtype == kBF16)
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
+        static_cast<const __nv_bfloat16*>(q) + i));
+  return *reinterpret_cast<const float2*>(static_cast<const float*>(q) + i);
+}
 
 // Split two floats into a packed high part and a packed remainder (f16 or bf16).
 __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -214,15 +220,22 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
       : "=r"(lo), "=r"(hi) : "r"(w));
 }
 
-// The INT4 codes at bits 4k .. 4k+3 and 16+4k .. 19+4k of w -> an f16x2 word holding
-// (24 + code) / 16 exactly: the nibble, its sign bit flipped (code + 8), becomes the top
-// four mantissa bits of 1.0.  (Placing it in the low mantissa bits of 1024 would cost no
-// shift, but its bias of 1032 would dominate the FP32 accumulator of P.V over long
-// contexts: a bias of 24 code units keeps the accumulator within ~7x of the signal.)
-template <int K>
-__device__ __forceinline__ uint32_t s4x2_to_f16x2_biased(uint32_t w) {
-  const uint32_t x = K <= 1 ? (w << (6 - 4 * K)) : (w >> (4 * K - 6));
-  return (x & 0x03C003C0u) ^ 0x3E003E00u;
+// INT4 codes -> (8 + code) / 8 as f16, exactly.  A nibble with its sign bit flipped
+// (code + 8, 0 .. 15) alone in the low bits of a byte is the FP6 E2M3 encoding of
+// (code + 8) / 8: exponent field 0 or 1 (bias 1) and three mantissa bits, so codes below
+// zero land on the subnormals k / 8 and the rest on 1 + k / 8.  Half H of w (0: the low
+// nibbles of its bytes, 1: the high nibbles) -> four such bytes; the hardware conversion
+// then turns each 16-bit half into an f16x2 word, byte b into half b % 2.  (An earlier
+// form built (24 + code) / 16 directly in the f16 bits with a shift and a mask-and-xor per
+// two codes; at the batch-256 shapes that cost ~5 us over INT8.)
+template <int H>
+__device__ __forceinline__ uint32_t s4x4_to_e2m3x4(uint32_t w) {
+  return ((H ? w >> 4 : w) & 0x0F0F0F0Fu) ^ 0x08080808u;
+}
+__device__ __forceinline__ void e2m3x4_to_f16x4(uint32_t m, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e2m3x2 %0, l;\n\tcvt.rn.f16x2.e2m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(m));
 }
 
 // ------------------------------------------------------------------ FP32 (CUDA cores)
@@ -549,8 +562,9 @@ struct Bf16Warp {
 
 // One path for the three coded formats: the codes become exact f16 MMA operands.
 //   INT8  1152 + code (two byte permutes per 4 stored codes); bias removed afterwards
-//   INT4  (24 + code) / 16 (one shift and one mask-and-xor per 2 codes); the factor 16
-//         goes into the score scale and the V scales, the bias is removed afterwards
+//   INT4  (8 + code) / 8 (one mask-and-xor per 4 codes, a shift for every second word,
+//         then the FP6 conversion, 2 codes per instruction); the factor 8 goes into the
+//         score scale and the V scales, the bias is removed afterwards
 //   FP8   the E4M3 value itself (hardware conversion, 2 codes per instruction), no bias
 // The per-page path is written against an explicit instruction budget: every shared
 // address is a per-lane base plus a constant (the ring of stages is unrolled), the V
@@ -572,8 +586,9 @@ struct QuantWarp {
   static constexpr int MT = D / 16;  // m-tiles (16 head-dim rows) of O^T = V^T P^T
   static constexpr int RB = RowBytes<KVT, D>::value;  // bytes of one stored K row
   // the operands are 2^kMulLog2 (kBias + code)
-  static constexpr float kBias = KVT == kINT8 ? 1152.f : KVT == kINT4 ? 24.f : 0.f;
-  static constexpr int kMulLog2 = KVT == kINT4 ? -4 : 0;
+  static constexpr float kBias = KVT == kINT8 ? 1152.f : KVT == kINT4 ? 8.f : 0.f;
+  static constexpr int kMulLog2 = KVT == kINT4 ? -3 : 0;
+  static constexpr float kUnit = KVT == kINT4 ? 0.125f : 1.f;  // 2^kMulLog2
   // per-lane shared-window addresses in stage 0 of this warp's ring (a stage adds a
   // constant): scale vectors, the two K rows, the ldmatrix row of the V block, and the
   // first query fragment
@@ -590,6 +605,24 @@ struct QuantWarp {
   // k-slot pair {2c, 2c+1} of k-step ks <-> head_dim 64(ks/4) + 16c + 4(ks%4): each lane's
   // K operand is then one contiguous 16-byte shared-memory load per n-tile.
   __device__ static int kslot_d(int ks, int c) { return 64 * (ks >> 2) + 16 * c + 4 * (ks & 3); }
+  // The query values of lane c's k-slots {2c, 2c+1, 2c+8, 2c+9} in k-step ks, from the
+  // row at q (shared floats, or the prefetched rows in dtype q_dtype).  INT4 K words hold
+  // 8 elements, element e at nibble (e / 2) + 4 (e % 2); the conversion's low-nibble half
+  // (even k-steps) gives element pairs (0, 4) and (1, 5) of the word, the high-nibble half
+  // (2, 6) and (3, 7), so the slots take elements 2h, 2h + 4, 2h + 1, 2h + 5 of the word
+  // 64 (ks / 4) + 16 c + 8 ((ks % 4) / 2), h = ks % 2.
+  __device__ static float4 q_slots(const float* sq, const void* q, int q_dtype, int ks, int c) {
+    if constexpr (KVT == kINT4) {
+      const int d = 64 * (ks >> 2) + 16 * c + 8 * ((ks & 3) >> 1) + 2 * (ks & 1);
+      const float2 a = sq ? *reinterpret_cast<const float2*>(sq + d) : load_q2(q, q_dtype, d);
+      const float2 b = sq ? *reinterpret_cast<const float2*>(sq + d + 4)
+                          : load_q2(q, q_dtype, d + 4);
+      return make_float4(a.x, b.x, a.y, b.y);
+    } else {
+      return sq ? *reinterpret_cast<const float4*>(sq + kslot_d(ks, c))
+                : load_q4(q, q_dtype, kslot_d(ks, c));
+    }
+  }
 
   // The block's query rows (heads h0 .. h0 + nh - 1 of sequence b, contiguous in q) are
   // requested by one bulk copy at block start, ahead of the block-table and length reads,
@@ -636,8 +669,9 @@ struct QuantWarp {
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         qv[ks] = !has ? make_float4(0.f, 0.f, 0.f, 0.f)
-                 : sq ? *reinterpret_cast<const float4*>(sq + r * D + kslot_d(ks, c))
-                      : load_q4(qraw, p.q_dtype, static_cast<size_t>(r) * D + kslot_d(ks, c));
+                      : q_slots(sq ? sq + r * D : nullptr,
+                                qraw + static_cast<size_t>(r) * D * (p.q_dtype == kBF16 ? 2 : 4),
+                                p.q_dtype, ks, c);
         qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(qv[ks].x), fabsf(qv[ks].y)),
                                  fmaxf(fabsf(qv[ks].z), fabsf(qv[ks].w))));
       }
@@ -727,14 +761,8 @@ struct QuantWarp {
       e4m3x4_to_f16x4(w, b0, b1);
     } else if constexpr (KVT == kINT8) {
       u8x4_to_f16x4_biased(w, b0, b1);
-    } else {  // INT4: nibbles 2 half and 2 half + 1 of the word
-      if (half) {
-        b0 = s4x2_to_f16x2_biased<2>(w);
-        b1 = s4x2_to_f16x2_biased<3>(w);
-      } else {
-        b0 = s4x2_to_f16x2_biased<0>(w);
-        b1 = s4x2_to_f16x2_biased<1>(w);
-      }
+    } else {  // INT4: elements (2 half, 2 half + 4) and (2 half + 1, 2 half + 5) of the word
+      e2m3x4_to_f16x4(half ? s4x4_to_e2m3x4<1>(w) : s4x4_to_e2m3x4<0>(w), b0, b1);
     }
   }
 
@@ -744,8 +772,9 @@ struct QuantWarp {
     const int c = lane & 3;
     const float4 k4 = lds_f4(a_sc + so);
     float4 v4 = lds_f4(a_sc + so + kPage * 4);
-    if constexpr (kMulLog2 != 0) {  // INT4: V operands enter as (kBias + code) / 16
-      v4.x *= 16.f; v4.y *= 16.f; v4.z *= 16.f; v4.w *= 16.f;
+    if constexpr (kMulLog2 != 0) {  // INT4: V operands enter as (kBias + code) / 8
+      constexpr float up = 1.f / kUnit;
+      v4.x *= up; v4.y *= up; v4.z *= up; v4.w *= up;
     }
     // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
     // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3 of head r.  The
@@ -828,10 +857,16 @@ struct QuantWarp {
     sp2 = __fadd2_rn(sp2, __fadd2_rn(pv01, pv23));
     // B = P^T (tokens x heads): lane (r, c) holds head r, tokens 4c .. 4c+3, which the
     // k-slot order {2c, 2c+1 | 2c+8, 2c+9} -> tokens {4c, 4c+1 | 4c+2, 4c+3} makes a
-    // ready-made fragment; the hi and lo parts accumulate into the same C.
+    // ready-made fragment (INT4: {4c, 4c+2 | 4c+1, 4c+3}, the order in which its V bytes
+    // are stored); the hi and lo parts accumulate into the same C.
     uint32_t bh0, bl0, bh1, bl1;
-    split_h2x(pv01, bh0, bl0);
-    split_h2x(pv23, bh1, bl1);
+    if constexpr (KVT == kINT4) {
+      split_h2x(make_float2(pv01.x, pv23.x), bh0, bl0);
+      split_h2x(make_float2(pv01.y, pv23.y), bh1, bl1);
+    } else {
+      split_h2x(pv01, bh0, bl0);
+      split_h2x(pv23, bh1, bl1);
+    }
     // A = V^T rows 16 j + r and 16 j + r + 8, tokens 4c .. 4c+3 (same k-slot order).
     // ldmatrix hands lane (r, c) bytes 4c .. 4c+3 of block rows r + 8 i.
     constexpr int NW = KVT == kINT4 ? MT : 2 * MT;  // words: V rows (pair rows for INT4)
@@ -848,10 +883,8 @@ struct QuantWarp {
       if constexpr (KVT == kINT4) {
         // one word: row pair 8 j + r, tokens 4c .. 4c+3 stored in the order 0, 2, 1, 3;
         // low nibbles row 16 j + r, high nibbles row 16 j + r + 8
-        a[0] = s4x2_to_f16x2_biased<0>(w[j]);
-        a[1] = s4x2_to_f16x2_biased<1>(w[j]);
-        a[2] = s4x2_to_f16x2_biased<2>(w[j]);
-        a[3] = s4x2_to_f16x2_biased<3>(w[j]);
+        e2m3x4_to_f16x4(s4x4_to_e2m3x4<0>(w[j]), a[0], a[2]);
+        e2m3x4_to_f16x4(s4x4_to_e2m3x4<1>(w[j]), a[1], a[3]);
       } else if constexpr (KVT == kFP8) {
         e4m3x4_to_f16x4(w[2 * j], a[0], a[2]);
         e4m3x4_to_f16x4(w[2 * j + 1], a[1], a[3]);
@@ -877,7 +910,7 @@ struct QuantWarp {
     }
     // V entered the MMA as 2^m (kBias + code) against P s_v 2^-m: remove kBias 2^m
     // sum(P s_v 2^-m) of heads 2c and 2c + 1
-    constexpr float vb = kBias * (kMulLog2 == 0 ? 1.f : 0.0625f);
+    constexpr float vb = kBias * kUnit;
     const float ba = vb * __shfl_sync(0xffffffffu, st, 8 * c);
     const float bb = vb * __shfl_sync(0xffffffffu, st, 8 * c + 4);
     float* oa = cO + (2 * c) * (D + 2);
