@@ -564,7 +564,7 @@ struct Bf16Warp {
 //   INT8  1152 + code (two byte permutes per 4 stored codes); bias removed afterwards
 //   INT4  (8 + code) / 8 (one mask-and-xor per 4 codes, a shift for every second word,
 //         then the FP6 conversion, 2 codes per instruction); the factor 8 goes into the
-//         score scale and the V scales, the bias is removed afterwards
+//         score scale and the block's final output, the bias is removed afterwards
 //   FP8   the E4M3 value itself (hardware conversion, 2 codes per instruction), no bias
 // The per-page path is written against an explicit instruction budget: every shared
 // address is a per-lane base plus a constant (the ring of stages is unrolled), the V
@@ -772,10 +772,6 @@ struct QuantWarp {
     const int c = lane & 3;
     const float4 k4 = lds_f4(a_sc + so);
     float4 v4 = lds_f4(a_sc + so + kPage * 4);
-    if constexpr (kMulLog2 != 0) {  // INT4: V operands enter as (kBias + code) / 8
-      constexpr float up = 1.f / kUnit;
-      v4.x *= up; v4.y *= up; v4.z *= up; v4.w *= up;
-    }
     // S = Q K^T over the page's 16 tokens: n-tile j column n holds token
     // 4(n/2) + 2j + (n%2), so lane (r, c) ends up with tokens 4c .. 4c+3 of head r.  The
     // accumulators of the hi rows start at -kbias: the code bias cancels in FP32.
@@ -908,19 +904,20 @@ struct QuantWarp {
       cm[r] = -nm2.x;  // the running max in log2 units, as the merge expects
       cl[r] = lt;
     }
-    // V entered the MMA as 2^m (kBias + code) against P s_v 2^-m: remove kBias 2^m
-    // sum(P s_v 2^-m) of heads 2c and 2c + 1
-    constexpr float vb = kBias * kUnit;
+    // V entered the MMA as 2^m (kBias + code) against P s_v: remove 2^m kBias sum(P s_v)
+    // of heads 2c and 2c + 1, then the factor 2^m (once here rather than on every page's
+    // V scales)
+    constexpr float vb = kBias * kUnit, up = 1.f / kUnit;
     const float ba = vb * __shfl_sync(0xffffffffu, st, 8 * c);
     const float bb = vb * __shfl_sync(0xffffffffu, st, 8 * c + 4);
     float* oa = cO + (2 * c) * (D + 2);
     float* ob = oa + (D + 2);
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
-      oa[16 * j + r] = o[j][0] - ba;
-      ob[16 * j + r] = o[j][1] - bb;
-      oa[16 * j + r + 8] = o[j][2] - ba;
-      ob[16 * j + r + 8] = o[j][3] - bb;
+      oa[16 * j + r] = (o[j][0] - ba) * up;
+      ob[16 * j + r] = (o[j][1] - bb) * up;
+      oa[16 * j + r + 8] = (o[j][2] - ba) * up;
+      ob[16 * j + r + 8] = (o[j][3] - bb) * up;
     }
   }
 };
