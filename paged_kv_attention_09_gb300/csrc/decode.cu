@@ -1383,6 +1383,8 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
   const int jl = np - 1 - pb - w;
   const int i_tail = (L & (kPage - 1)) != 0 && np == pe && jl >= 0 && jl % kW == 0 ? jl / kW : -1;
   const int i_head = WIN && (lo & (kPage - 1)) != 0 && split == 0 && w == 0 ? 0 : -1;
+  // the fused step: the iteration whose page (the sequence's last) takes the new row
+  const int i_patch = STEP && patch && jl >= 0 && jl % kW == 0 ? jl / kW : -1;
 
   // One ring step: wait for stage `stage`, consume its page, refill it with iteration
   // i + S.  For the tensor-core paths the loop below unrolls the ring, so every stage
@@ -1396,7 +1398,7 @@ __global__ void __launch_bounds__(Tune<KVT, D>::W * 32, Tune<KVT, D>::minBlocks)
     const int j0 = pb + w + i * kW;  // the block's page
     if constexpr (STEP) {
       // the fused step: the new token replaces whatever the cache held at its slot
-      if (patch && j0 == np - 1) {
+      if (i == i_patch) {
         constexpr int RB = RowBytes<KVT, D>::value;
         uint8_t* pg = my_stages + stage * Lo::stageBytes;
         const uint8_t* nk = nrow;
