@@ -573,6 +573,41 @@ def run_ours(args, rank, world):
             "e2e": e2e, "fused": pr.fused, "n_append": pr.n_append, "workloads": tables}
 
 
+class _Runtime:
+    """The CUDA runtime's copy and event calls, issued through ctypes: the end-to-end loop
+    orders its copies and launches with them at about a microsecond of host time each
+    (a torch copy or event call costs several)."""
+
+    def __init__(self):
+        import ctypes
+        import torch
+        self.ct = ctypes
+        self.rt = ctypes.CDLL(f"libcudart.so.{torch.version.cuda.split('.')[0]}")
+        V, U = ctypes.c_void_p, ctypes.c_uint
+        self.rt.cudaMemcpyAsync.argtypes = [V, V, ctypes.c_size_t, ctypes.c_int, V]
+        self.rt.cudaEventRecord.argtypes = [V, V]
+        self.rt.cudaStreamWaitEvent.argtypes = [V, V, U]
+        self.rt.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(V), U]
+        self.rt.cudaEventDestroy.argtypes = [V]
+        self.events = []
+
+    def event(self):
+        e = self.ct.c_void_p()
+        self.check(self.rt.cudaEventCreateWithFlags(self.ct.byref(e), 2), "event")  # no timing
+        self.events.append(e)
+        return e
+
+    @staticmethod
+    def check(code, what):
+        if code != 0:
+            raise RuntimeError(f"CUDA runtime error {code} ({what})")
+
+    def close(self):
+        for e in self.events:
+            self.rt.cudaEventDestroy(e)
+        self.events = []
+
+
 def run_e2e(args, pr, world, dev, acc, K):
     """The same step through the public API with host buffers: every step copies its
     inputs from pinned host memory and its outputs back, inside the timed region."""
@@ -627,9 +662,6 @@ def run_e2e(args, pr, world, dev, acc, K):
     step_r = [[pr.step_k.clone(), pr.step_v.clone(), pr.step_s.clone()] for _ in range(R)]
     h2d_s = torch.cuda.Stream(device=stream.device)
     d2h_s = torch.cuda.Stream(device=stream.device)
-    ev_in = [torch.cuda.Event() for _ in range(R)]
-    ev_done = [torch.cuda.Event() for _ in range(R)]
-    ev_out = [torch.cuda.Event() for _ in range(R)]
     used = [False] * R
 
     def dev_inputs(r):
@@ -668,31 +700,59 @@ def run_e2e(args, pr, world, dev, acc, K):
                     b.q_start_loc = next(it)
             dev_stage.append(buf)
 
+    # Per step: the input copy on h2d_s once the replica's previous step has read its
+    # inputs, the step's launches on `stream` once the inputs have landed and the
+    # replica's previous outputs were read back, then the output copy on d2h_s.  The
+    # copies and events go straight to the CUDA runtime and the library calls are bound
+    # once (pkv.BoundCall), so the host spends ~1 us per call instead of the ~45 us per
+    # step that torch copies, events and the full wrappers cost.
+    if graphs is None:
+        import ctypes as ct
+        rtm = _Runtime()
+        rt = rtm.rt
+        ev_in = [rtm.event() for _ in range(R)]
+        ev_done = [rtm.event() for _ in range(R)]
+        ev_out = [rtm.event() for _ in range(R)]
+        cs = ct.c_void_p(stream.cuda_stream)
+        hs = ct.c_void_p(h2d_s.cuda_stream)
+        ds = ct.c_void_p(d2h_s.cuda_stream)
+        nbytes = host_stage.numel()
+        h2d_args, d2h_args, calls = [], [], []
+        for r in range(R):
+            h2d_args.append((ct.c_void_p(dev_stage[r].data_ptr()), ct.c_void_p(host_stage.data_ptr()),
+                             nbytes, 1, hs))  # cudaMemcpyHostToDevice
+            d2h_args.append([(ct.c_void_p(h.data_ptr()), ct.c_void_p(b.out.data_ptr()),
+                              b.out.numel() * b.out.element_size(), 2, ds)  # DeviceToHost
+                             for b, h in zip(pr.reps[r].batches, host_out)])
+            sk, sv, ss = step_r[r]
+            cr = []
+            for dw in pr.layered[r]:
+                if pr.n_append:
+                    cr.append(pkv.pkv_append(dw.cache, sk, sv, ss, dw.dev_status, stream, bound=True))
+                for j in range(len(wl.batches)):
+                    if pr.fused and j == 0:
+                        cr.append(runner.run_decode_step(dw, dec_r[r], 0, ROPE_THETA, stream, bound=True))
+                    else:
+                        cr.append(runner.run_batch(dw, j, stream, bound=True))
+            calls.append(cr)
+        memcpy, record, wait, check = rt.cudaMemcpyAsync, rt.cudaEventRecord, rt.cudaStreamWaitEvent, rtm.check
+
     def piped_step(i):
         r = i % R
-        with torch.cuda.stream(h2d_s):
-            if used[r]:
-                h2d_s.wait_event(ev_done[r])  # the replica's previous step read its inputs
-            dev_stage[r].copy_(host_stage, non_blocking=True)
-            ev_in[r].record(h2d_s)
-        stream.wait_event(ev_in[r])
         if used[r]:
-            stream.wait_event(ev_out[r])  # its previous outputs were read back
-        sk, sv, ss = step_r[r]
-        for dw in pr.layered[r]:
-            if pr.n_append:
-                pkv.pkv_append(dw.cache, sk, sv, ss, dw.dev_status, stream)
-            for j in range(len(wl.batches)):
-                if pr.fused and j == 0:
-                    runner.run_decode_step(dw, dec_r[r], 0, ROPE_THETA, stream)
-                else:
-                    runner.run_batch(dw, j, stream)
-        ev_done[r].record(stream)
-        with torch.cuda.stream(d2h_s):
-            d2h_s.wait_event(ev_done[r])
-            for b, h in zip(pr.reps[r].batches, host_out):
-                h.copy_(b.out, non_blocking=True)
-            ev_out[r].record(d2h_s)
+            check(wait(hs, ev_done[r], 0), "wait")  # the replica's previous step read its inputs
+        check(memcpy(*h2d_args[r]), "input copy")
+        check(record(ev_in[r], hs), "record")
+        check(wait(cs, ev_in[r], 0), "wait")
+        if used[r]:
+            check(wait(cs, ev_out[r], 0), "wait")  # its previous outputs were read back
+        for c in calls[r]:
+            c()
+        check(record(ev_done[r], cs), "record")
+        check(wait(ds, ev_done[r], 0), "wait")
+        for a in d2h_args[r]:
+            check(memcpy(*a), "output copy")
+        check(record(ev_out[r], ds), "record")
         used[r] = True
 
     run = e2e_step if graphs is not None else piped_step
@@ -716,11 +776,14 @@ def run_e2e(args, pr, world, dev, acc, K):
     if graphs is not None:
         for g in graphs:
             g.close()
+    else:
+        rtm.close()
     return {"value": round(job_rate(acc["total"] * NL, world, e2e_ms * 1e-3) / 1e9, 2),
             "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 5),
             "launches": "one CUDA graph per step" if graphs is not None
-            else "direct; a step's input copies and the previous step's output copy overlap its kernels"}
+            else "direct; a step's input copies and the previous step's output copy overlap its "
+                 "kernels; copies and events through the CUDA runtime, library calls bound once"}
 
 
 def compare_lines(prev, line, threshold=0.10):

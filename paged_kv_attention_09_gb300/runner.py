@@ -100,16 +100,20 @@ def append_rows(dw: DeviceWorkload, rows: torch.Tensor, stream=None) -> None:
                    dw.slots[rows].contiguous(), dw.dev_status, stream)
 
 
-def run_batch(dw: DeviceWorkload, i: int, stream=None) -> torch.Tensor:
+def run_batch(dw: DeviceWorkload, i: int, stream=None, bound: bool = False):
+    """Batch ``i``'s attention; returns its output, or (bound=True) the call itself as a
+    pkv.BoundCall, not yet issued."""
     b = dw.batches[i]
     if b.kind == "decode":
-        pkv.pkv_decode_attn(dw.cache, b.q, b.block_tables, b.context_lens, dw.wl.scale, b.out,
-                            b.workspace, dw.dev_status, stream, split_pages=dw.split_pages)
+        call = pkv.pkv_decode_attn(dw.cache, b.q, b.block_tables, b.context_lens, dw.wl.scale,
+                                   b.out, b.workspace, dw.dev_status, stream,
+                                   split_pages=dw.split_pages, bound=bound)
     else:
-        pkv.pkv_prefill_chunk_attn(dw.cache, b.q, b.q_start_loc, b.max_q_len, b.block_tables,
-                                   b.context_lens, dw.wl.scale, b.out, b.workspace,
-                                   dw.dev_status, stream, key_split=dw.key_split)
-    return b.out
+        call = pkv.pkv_prefill_chunk_attn(dw.cache, b.q, b.q_start_loc, b.max_q_len,
+                                          b.block_tables, b.context_lens, dw.wl.scale, b.out,
+                                          b.workspace, dw.dev_status, stream,
+                                          key_split=dw.key_split, bound=bound)
+    return call if bound else b.out
 
 
 def run_step(dw: DeviceWorkload, step_k=None, step_v=None, step_slots=None, stream=None):
@@ -134,11 +138,12 @@ def decode_step_inputs(dw: DeviceWorkload, i: int = 0, rope: bool = True):
 
 
 def run_decode_step(dw: DeviceWorkload, inputs, i: int = 0, rope_theta: float = 10000.0,
-                    stream=None) -> torch.Tensor:
-    """Decode batch ``i`` as one fused step (rotate, append the new rows, attend)."""
+                    stream=None, bound: bool = False):
+    """Decode batch ``i`` as one fused step (rotate, append the new rows, attend); returns
+    its output, or (bound=True) the call as a pkv.BoundCall, not yet issued."""
     b = dw.batches[i]
     k, v, slots, pos = inputs
-    pkv.pkv_decode_step(dw.cache, b.q, k, v, slots, pos, rope_theta, b.block_tables,
-                        b.context_lens, dw.wl.scale, b.out, b.workspace, dw.dev_status, stream,
-                        split_pages=dw.split_pages)
-    return b.out
+    call = pkv.pkv_decode_step(dw.cache, b.q, k, v, slots, pos, rope_theta, b.block_tables,
+                               b.context_lens, dw.wl.scale, b.out, b.workspace, dw.dev_status,
+                               stream, split_pages=dw.split_pages, bound=bound)
+    return call if bound else b.out
