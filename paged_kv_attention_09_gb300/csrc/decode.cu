@@ -225,9 +225,10 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
 // (code + 8) / 8: exponent field 0 or 1 (bias 1) and three mantissa bits, so codes below
 // zero land on the subnormals k / 8 and the rest on 1 + k / 8.  Half H of w (0: the low
 // nibbles of its bytes, 1: the high nibbles) -> four such bytes; the hardware conversion
-// then turns each 16-bit half into an f16x2 word, byte b into half b % 2.  (An earlier
-// form built (24 + code) / 16 directly in the f16 bits with a shift and a mask-and-xor per
-// two codes; at the batch-256 shapes that cost ~5 us over INT8.)
+// then turns each 16-bit half into an f16x2 word, byte b into half b % 2.  (Measured at
+// the batch-256 shapes against two other forms: (24 + code) / 16 built in the f16 bits
+// with a shift and a mask-and-xor per two codes, 31.1 us, and the codes themselves by a
+// mask-and-xor plus an f16x2 multiply-add per two codes, 30.3-30.6 us; this form 29.6-29.8.)
 template <int H>
 __device__ __forceinline__ uint32_t s4x4_to_e2m3x4(uint32_t w) {
   return ((H ? w >> 4 : w) & 0x0F0F0F0Fu) ^ 0x08080808u;
